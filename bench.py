@@ -1,0 +1,519 @@
+"""Benchmark of the DiLoCo outer synchronisation step on GB300.
+
+Workload (default): the 1.1B decoder-shaped fp32 tensor set (201 tensors,
+22 layers, d=2048, FFN 5632, 32 q / 4 kv heads, vocab 32000), K=4 learner
+replicas resident in HBM, split by the LPT planner into P=24 fragments. One
+step = one outer synchronisation of the whole model: every fragment goes
+through stats -> quantise -> merge + Nesterov (the planner call is included).
+Inputs are synthetic (seeded generator), each fragment call streams >= 0.9 GB,
+far more than the 129 MB L2, so no L2 flush is needed between calls.
+
+Metric: outer-step params/s (whole job) and achieved HBM GB/s of each call,
+against the measured copy bandwidth in MEASURED_PEAKS.json.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun as N independent replicas of the workload (one per
+GPU; the path has no data exchange), timed with a barrier and the max over
+ranks. The reference arm (--impl reference) times the CPU oracle on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "outer-step params/s & achieved HBM GB/s (quantise+merge+Nesterov, K learners)"
+UNIT = "params/s"
+
+
+def algo_bytes(K):
+    """Algorithmic HBM bytes per fragment element of each call (minimum traffic:
+    Delta never stored, codes written once and read once)."""
+    return {"stats": 4 * (K + 1), "quantize": 4 * (K + 1) + K, "merge": K + 16}
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.uuid = device_uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload data
+
+
+def fragment_tensors(wl, frag_of):
+    return [[t for t in range(wl.n_tensors) if frag_of[t] == f] for f in range(wl.n_frags)]
+
+
+def generate_host(wl, frags, pin):
+    """theta_g and K replicas of every fragment as (pinned) host tensors."""
+    import torch
+
+    out = []
+    for tensors in frags:
+        n = sum(wl.numels[t] for t in tensors)
+        g = torch.empty(n, dtype=torch.float32, pin_memory=pin)
+        reps = [torch.empty(n, dtype=torch.float32, pin_memory=pin) for _ in range(wl.K)]
+        gn, rn = g.numpy(), [r.numpy() for r in reps]
+        o = 0
+        for t in tensors:
+            m = wl.numels[t]
+            wl.theta_global(t, out=gn[o:o + m])
+            for k in range(wl.K):
+                wl.replica(k, t, gn[o:o + m], out=rn[k][o:o + m])
+            o += m
+        out.append((g, reps))
+    return out
+
+
+class DeviceRun:
+    """Device-resident state of every fragment plus shared scratch buffers."""
+
+    def __init__(self, wl, frags, host, dev):
+        import torch
+
+        import pseudo_grad_sync_gb300 as dl
+
+        self.dl, self.wl, self.frags = dl, wl, frags
+        K = wl.K
+        self.F = [dl.Fragment([wl.numels[t] for t in ts], dev) for ts in frags]
+        self.g = [h[0].to(dev, non_blocking=True) for h in host]
+        self.m = [torch.zeros_like(x) for x in self.g]
+        self.reps = [[r.to(dev, non_blocking=True) for r in h[1]] for h in host]
+        max_n = max(f.n for f in self.F)
+        max_t = max(f.T for f in self.F)
+        self.codes = [torch.empty(max_n, dtype=torch.uint8, device=dev) for _ in range(K)]
+        self.codebook = torch.empty((K, max_t, 256), dtype=torch.float32, device=dev)
+        self.stats = dl.new_stats(K, max_t, dev)
+        self.ws_s = dl.new_workspace(max(dl.stats_workspace_bytes(f, K) for f in self.F), dev)
+        self.ws_q = dl.new_workspace(max(dl.quantize_workspace_bytes(f, K) for f in self.F), dev)
+        torch.cuda.synchronize()
+
+    def step(self, reps=None, events=None, stream=None):
+        dl, K = self.dl, self.wl.K
+        dl.plan_fragments(self.wl.numels, self.wl.n_frags)
+        for f, F in enumerate(self.F):
+            # stats / codebook buffers are used as flat [K*T] / [K*T*256] arrays
+            r = self.reps[f] if reps is None else reps[f]
+            if events is not None:
+                events[f][0].record(stream)
+            dl.pseudograd_stats(self.g[f], r, F, 6.0, self.stats, self.ws_s, stream)
+            if events is not None:
+                events[f][1].record(stream)
+            dl.quantize(self.g[f], r, F, self.stats, self.codes, self.codebook, None, self.ws_q,
+                        stream)
+            if events is not None:
+                events[f][2].record(stream)
+            dl.merge_outer_step(self.g[f], self.m[f], F, self.codes, self.codebook, K=K,
+                                lr=0.7, mu=0.9, stream=stream)
+            if events is not None:
+                events[f][3].record(stream)
+
+
+LAUNCHES_PER_FRAGMENT = {"stats": 3, "quantize": 2, "merge": 1}
+
+
+def traffic_record(name):
+    """Per-element DRAM traffic of a kernel from a committed ncu summary, valid
+    only while the kernel's source is unchanged (hash recorded with it)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh).get(name)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as fh:
+            h.update(fh.read())
+    return rec if h.hexdigest() == rec["sha256"] else None
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import pseudo_grad_sync_gb300 as dl
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = synthetic.WORKLOADS[args.workload]()
+    frag_of, load = dl.plan_fragments(wl.numels, wl.n_frags)
+    frags = fragment_tensors(wl, frag_of)
+    K = wl.K
+    n_total = wl.n_elems
+    t0 = time.time()
+    host = generate_host(wl, frags, pin=not args.no_e2e)
+    gen_s = time.time() - t0
+    run = DeviceRun(wl, frags, host, dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        run.step()
+    barrier()
+
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in frags]
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    start.record(stream)
+    for s in range(args.steps):
+        run.step(events=ev[s], stream=stream)
+    end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+
+    # per-call device time (CUDA events inside the timed region)
+    per_call = {"stats": 0.0, "quantize": 0.0, "merge": 0.0}
+    for s in range(args.steps):
+        for f in range(len(frags)):
+            e = ev[s][f]
+            per_call["stats"] += e[0].elapsed_time(e[1])
+            per_call["quantize"] += e[1].elapsed_time(e[2])
+            per_call["merge"] += e[2].elapsed_time(e[3])
+    peak, peak_kind = load_peaks()
+    ab = algo_bytes(K)
+    calls = {}
+    for name, tot_ms in per_call.items():
+        launches = args.steps * len(frags)
+        avg_s = tot_ms / launches / 1e3
+        bytes_per_launch = ab[name] * n_total / len(frags)
+        gbs = bytes_per_launch / avg_s / 1e9
+        calls[name] = {"ms_per_step": tot_ms / args.steps, "avg_launch_us": avg_s * 1e6,
+                       "algo_bytes_per_elem": ab[name], "achieved_gbs": gbs,
+                       "frac": gbs / peak}
+    full_gbs = (sum(ab.values()) * n_total) / (ms_per_step / 1e3) / 1e9
+    dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
+    kernel_of = {"stats": "k_stats", "quantize": "k_quantize", "merge": "k_merge_q"}
+    tr = traffic_record(kernel_of[dominant])
+    traffic = None
+    if tr is not None:
+        traffic = tr["dram_bytes_per_elem"] * n_total / len(frags)
+    roofline = {"bound": "hbm", "achieved": round(calls[dominant]["achieved_gbs"], 1),
+                "peak": peak, "unit": "GB/s",
+                "frac": round(calls[dominant]["frac"], 4), "traffic": traffic,
+                "kernel": kernel_of[dominant],
+                "note": (f"call '{dominant}' timed with CUDA events around its C-ABI call "
+                         f"(includes its small setup/finalise kernels); peak = {peak_kind} "
+                         "copy bandwidth from MEASURED_PEAKS.json; traffic = ncu DRAM "
+                         "bytes per launch (null if not captured for this source)")}
+
+    # end to end: replicas arrive from pinned host memory, theta_g goes back
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(run, host, args, world, dev)
+
+    value = world * n_total / (ms_per_step / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name + ": " + wl.description, "K": K,
+                   "fragments": wl.n_frags, "params": n_total,
+                   "fragment_elems_min_max": [int(load.min()), int(load.max())],
+                   "l2": "no flush: every call streams >= 0.9 GB, inputs larger than L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "full_step_gbs": full_gbs, "full_step_frac": full_gbs / peak,
+        "calls": calls, "roofline": roofline, "clocks": clk,
+        "gpu_launches": args.steps * len(frags) * sum(LAUNCHES_PER_FRAGMENT.values()),
+        "e2e": e2e, "setup_generate_s": gen_s,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, frags, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(run, host, args, world, dev):
+    """Same step through the public API with host buffers: each fragment's K
+    replicas are copied from pinned host memory (double-buffered on a copy
+    stream) and the updated theta_g is copied back, all inside the timed
+    region."""
+    import torch
+
+    K = run.wl.K
+    max_n = max(f.n for f in run.F)
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    stage = [[torch.empty(max_n, dtype=torch.float32, device=dev) for _ in range(K)]
+             for _ in range(2)]
+    g_out = [torch.empty_like(h[0], pin_memory=True) for h in host]
+    nF = len(run.F)
+    bi = sum(K * f.n * 4 for f in run.F)
+    bo = sum(f.n * 4 for f in run.F)
+
+    def one_step():
+        ready = [torch.cuda.Event() for _ in range(nF)]
+        done = [torch.cuda.Event() for _ in range(nF)]
+        for f in range(nF):
+            buf = stage[f % 2]
+            n = run.F[f].n
+            with torch.cuda.stream(copy):
+                if f >= 2:
+                    copy.wait_event(done[f - 2])
+                for k in range(K):
+                    buf[k][:n].copy_(host[f][1][k], non_blocking=True)
+                ready[f].record(copy)
+            comp.wait_event(ready[f])
+            reps = [b[:n] for b in buf]
+            F = run.F[f]
+            run.dl.pseudograd_stats(run.g[f], reps, F, 6.0, run.stats, run.ws_s, comp)
+            run.dl.quantize(run.g[f], reps, F, run.stats, run.codes, run.codebook, None,
+                            run.ws_q, comp)
+            run.dl.merge_outer_step(run.g[f], run.m[f], F, run.codes, run.codebook, K=K,
+                                    lr=0.7, mu=0.9, stream=comp)
+            done[f].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[f])
+                g_out[f].copy_(run.g[f], non_blocking=True)
+        comp.wait_stream(copy)
+
+    steps = max(2, min(args.steps, 5))
+    for _ in range(2):
+        one_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": world * run.wl.n_elems * steps / dt, "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
+            "ms_per_step": dt / steps * 1e3,
+            "note": "replicas H2D from pinned memory on a copy stream (double-buffered), "
+                    "updated theta_g D2H; momentum and theta_g state stay on the device"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings
+
+
+def oracle_sample(wl, frags, target_elems):
+    """A bounded sample of the workload: whole tensors, in fragment order,
+    skipping any that would overshoot target_elems."""
+    chosen = []
+    tot = 0
+    for ts in frags:
+        for t in ts:
+            if tot + wl.numels[t] <= target_elems:
+                chosen.append(t)
+                tot += wl.numels[t]
+    if not chosen:
+        chosen = [min(range(wl.n_tensors), key=lambda t: wl.numels[t])]
+    numels = [wl.numels[t] for t in chosen]
+    n = sum(numels)
+    g = np.empty(n, dtype=np.float32)
+    reps = [np.empty(n, dtype=np.float32) for _ in range(wl.K)]
+    o = 0
+    for t in chosen:
+        m = wl.numels[t]
+        wl.theta_global(t, out=g[o:o + m])
+        for k in range(wl.K):
+            wl.replica(k, t, g[o:o + m], out=reps[k][o:o + m])
+        o += m
+    off = np.zeros(len(numels) + 1, dtype=np.int64)
+    np.cumsum(numels, out=off[1:])
+    return g, reps, off, chosen
+
+
+def time_oracle(g, reps, off, reps_min=1, budget_s=10.0):
+    import oracle
+
+    m = np.zeros_like(g)
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < reps_min or (time.perf_counter() - t_start < budget_s and len(times) < 5):
+        t0 = time.perf_counter()
+        oracle.outer_step(g, m, reps, offsets=off)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), len(times)
+
+
+def cpu_baseline(wl, frags, budget_s=10.0):
+    import oracle
+
+    g, reps, off, chosen = oracle_sample(wl, frags, target_elems=24_000_000)
+    t, nrep = time_oracle(g, reps, off, budget_s=budget_s)
+    return {"value": g.size / t, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(chosen)} whole tensors, {g.size} elements x K={wl.K} of the "
+                      f"workload, full outer step (stats+quantise+merge+Nesterov), median "
+                      f"of {nrep} runs of {t:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    import oracle
+
+    if rank != 0:
+        return
+    wl = synthetic.WORKLOADS[args.workload]()
+    import pseudo_grad_sync_gb300  # noqa: F401  (planner only: host code, no GPU work)
+    frag_of, _ = oracle.plan_fragments(wl.numels, wl.n_frags)
+    frags = fragment_tensors(wl, frag_of)
+    g, reps, off, chosen = oracle_sample(wl, frags, target_elems=8_000_000)
+    m = np.zeros_like(g)
+    for _ in range(args.warmup):
+        oracle.outer_step(g, m, reps, offsets=off)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.outer_step(g, m, reps, offsets=off)
+    dt = time.perf_counter() - t0
+    value = g.size * args.steps / dt
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic",
+           "config": {"workload": wl.name + ": " + wl.description, "K": wl.K,
+                      "fragments": wl.n_frags, "params": wl.n_elems},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
+                            "kind": "oracle",
+                            "sample": f"each step: {len(chosen)} whole tensors, {g.size} "
+                                      f"elements x K={wl.K}, full outer step on the host"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synthetic.WORKLOADS), default="decoder_1b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    rank, world, local = env_rank()
+    if world > 1:
+        import torch.distributed as dist
+
+        if args.impl == "ours":
+            import torch
+
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

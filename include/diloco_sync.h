@@ -1,0 +1,193 @@
+/*
+ * diloco_sync.h - C ABI of the GB300 DiLoCo outer-synchronisation library.
+ *
+ * One call sequence syncs one fragment of a model whose K learner replicas
+ * already sit in this GPU's memory:
+ *
+ *   dl_plan_fragments      (host, once)  tensors -> P balanced fragments
+ *   dl_pseudograd_stats    (device)      per-(learner, tensor) mu / sigma
+ *   dl_quantize            (device)      uint8 codes + bucket-mean codebooks
+ *   dl_merge_outer_step    (device)      decode, weighted fp32 mean, Nesterov
+ *
+ * Sources: the INTELLECT-1 paper notes ("INTELLECT-1: Training a 10B Model
+ * Across 3 Continents", sections 3.2, 4.1 and 4.2) define the pseudo-gradient,
+ * the 6-sigma / 256-bucket quantiser with a bucket-mean codebook, the fp32
+ * accumulation rule and the outer Nesterov step (lr 0.7, momentum 0.9); the
+ * Decoupled DiLoCo note ("Decoupled DiLoCo: Resilient, Distributed AI
+ * Training at Scale", architecture item 4 and fault-tolerance items 1 and 3)
+ * defines fragments packed by greedy bin-packing, the minimum quorum and the
+ * token-weighted merge.
+ *
+ * Conventions for every call:
+ *  - A fragment is a flat run of n fp32 elements made of T tensors; tensor t
+ *    occupies [offsets[t], offsets[t+1]). Every per-fragment buffer (theta_g,
+ *    momentum, each learner replica, each learner's codes) is a separate flat
+ *    buffer of n elements.
+ *  - All buffers are owned by the caller. "d_" pointers and the pointers
+ *    inside pointer arrays are device pointers; pointer arrays themselves
+ *    (theta_k, codes) and offsets / weights / present are host arrays read
+ *    during the call only.
+ *  - Device buffers of fp32 or uint8 elements must be 16-byte aligned.
+ *    Workspaces must be 256-byte aligned.
+ *  - Device work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and runs asynchronously; the call returns once it is
+ *    enqueued. Host-side validation happens before anything is enqueued, so
+ *    an error return means nothing was launched (DL_ERR_CUDA excepted).
+ *  - No call allocates device memory; scratch comes from the caller's
+ *    workspace, sized by the matching *_workspace_bytes query.
+ *  - n = 0 is a valid no-op. Outputs must not alias inputs, except that
+ *    theta_g and momentum are updated in place by the merge.
+ *  - No C++ exception crosses the ABI. Calls are thread-safe as long as
+ *    concurrent calls use different workspaces.
+ */
+#ifndef DILOCO_SYNC_H
+#define DILOCO_SYNC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (0 = success, negative = error). */
+#define DL_OK 0
+#define DL_ERR_ARG (-1)       /* bad argument: null pointer, bad size, bad weight */
+#define DL_ERR_ALIGN (-2)     /* a buffer violates the alignment rule */
+#define DL_ERR_QUORUM (-3)    /* fewer present learners than the minimum quorum */
+#define DL_ERR_CUDA (-4)      /* a CUDA runtime call or launch failed */
+#define DL_ERR_SHAPE (-5)     /* offsets not starting at 0 or decreasing */
+#define DL_ERR_WORKSPACE (-6) /* workspace missing or too small */
+#define DL_ERR_DEVICE (-7)    /* a kernel reported a failure (see dl_read_device_status) */
+
+#define DL_NBUCKETS 256      /* uint8 code space */
+#define DL_MAX_LEARNERS 32   /* largest K accepted by every call */
+
+/* Statistics of one (learner k, tensor t) pseudo-gradient segment; arrays of
+ * these are laid out [K][T] (index k * T + t). 48 bytes. */
+typedef struct dl_stats {
+    int64_t count;     /* elements in the tensor */
+    int64_t nonfinite; /* elements whose pseudo-gradient is Inf or NaN */
+    double mean;       /* mu; NaN when nonfinite > 0; 0 for an empty tensor */
+    double std;        /* population sigma */
+    double lo;         /* mu - clip_sigmas * sigma */
+    double hi;         /* mu + clip_sigmas * sigma */
+} dl_stats;
+
+/* Tensor layout of one fragment. offsets (host) and d_offsets (device) hold
+ * the same T+1 non-decreasing values with offsets[0] = 0; n = offsets[T]. */
+typedef struct dl_fragment {
+    const int64_t* offsets;
+    const int64_t* d_offsets;
+    int32_t n_tensors;
+} dl_fragment;
+
+/* Version of this ABI (major * 100 + minor). */
+int dl_version(void);
+
+/* Human-readable name of a status code. Never returns NULL. */
+const char* dl_status_string(int status);
+
+/*
+ * Balanced tensor fragmentation (Decoupled DiLoCo note, architecture item 4:
+ * tensors packed into P fragments of similar size, like greedy bin-packing).
+ * Host only. Longest-processing-time greedy: tensors taken by numel
+ * descending (index ascending on ties), each placed on the fragment with the
+ * smallest load so far (lowest fragment index on ties). Tensors are never
+ * split, so a tensor larger than the average fragment gets one to itself.
+ *   numel          [n_tensors] element counts, each >= 0
+ *   frag_of_tensor [n_tensors] out: fragment index of each tensor
+ *   frag_load      [n_frags]   out: total elements per fragment
+ * Returns DL_ERR_ARG for n_frags <= 0, n_tensors < 0, negative numel or
+ * null outputs (when n_tensors > 0).
+ */
+int dl_plan_fragments(const int64_t* numel, int32_t n_tensors, int32_t n_frags,
+                      int32_t* frag_of_tensor, int64_t* frag_load);
+
+/* Workspace bytes needed by dl_pseudograd_stats for this fragment and K. */
+size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K);
+
+/*
+ * Per-tensor statistics of every learner's pseudo-gradient (INTELLECT-1
+ * notes, section 3.2 step 4 and section 4.1 steps 1-2).
+ * Delta_k[i] = fl32(theta_g[i] - theta_k[k][i]) is formed on the fly and
+ * never stored. For each (k, t): mean, population std, lo = mean -
+ * clip_sigmas * std, hi = mean + clip_sigmas * std, computed to fp64
+ * accuracy, plus the element and non-finite counts.
+ *   theta_g      device [n] fp32, global parameters at the start of the round
+ *   theta_k      host [K] of device [n] fp32, learner replicas
+ *   clip_sigmas  > 0, 6 in the pages
+ *   d_stats      device [K*T] dl_stats, out (8-byte aligned)
+ *   d_workspace  device scratch of dl_stats_workspace_bytes(frag, K) bytes
+ */
+int dl_pseudograd_stats(const float* theta_g, const float* const* theta_k, int32_t K,
+                        const dl_fragment* frag, double clip_sigmas, dl_stats* d_stats,
+                        void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes needed by dl_quantize for this fragment and K. */
+size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K);
+
+/*
+ * Uniform quantisation with clipping and a bucket-mean codebook (INTELLECT-1
+ * notes, section 4.1 steps 2-4). For each (k, t) with lo < hi:
+ *   code   = clamp(floor((Delta - lo) * 256 / (hi - lo)), 0, 255), decided
+ *            exactly as in fp64 (a value on an interior edge goes up);
+ *   cb[b]  = mean of clamp(Delta, lo, hi) over the elements with code b, or
+ *            the bucket midpoint lo + (b + 1/2)(hi - lo)/256 when empty.
+ * A segment whose range is below 256 * FLT_MIN (sigma = 0 included) gets
+ * code 0 everywhere and cb[b] = (float)mean; a segment with non-finite
+ * elements gets code 0 everywhere and a NaN codebook.
+ *   d_stats     device [K*T], as written by dl_pseudograd_stats
+ *   codes       host [K] of device [n] uint8, out
+ *   d_codebook  device [K*T*256] fp32, out, index (k*T + t)*256 + b
+ *   d_counts    device [K*T*256] uint32 bucket populations, out; may be NULL
+ *   d_workspace device scratch of dl_quantize_workspace_bytes(frag, K) bytes
+ */
+int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
+                const dl_fragment* frag, const dl_stats* d_stats, uint8_t* const* codes,
+                float* d_codebook, uint32_t* d_counts, void* d_workspace,
+                size_t workspace_bytes, void* stream);
+
+/*
+ * Dequantise, merge and apply the outer Nesterov step (INTELLECT-1 notes,
+ * section 3.2 steps 6-7 and section 4.2; Decoupled DiLoCo note,
+ * fault-tolerance items 1 and 3), in place on theta_g and momentum:
+ *   w_hat_k = weights[k] / sum_{j present} weights[j]   (fp64, then fp32)
+ *   D[i]    = sum over present k, ascending, of fmaf(w_hat_k, v_k[i], .)
+ *             with v_k = codebook value of code k (fp32, never summed in
+ *             code space) or, in unquantised mode, the fp32 Delta_k;
+ *   m'      = fmaf(mu, m, D);  g = fmaf(mu, m', D);  theta' = fmaf(-lr, g, theta)
+ *   theta_g, momentum  device [n] fp32, in/out
+ *   codes       host [K] of device [n] uint8, or NULL for unquantised mode
+ *   d_codebook  device [K*T*256] fp32 (ignored in unquantised mode)
+ *   theta_k     host [K] of device [n] fp32 (read only in unquantised mode)
+ *   weights     host [K] fp32 >= 0 (tokens processed), or NULL for all 1
+ *   present     host [K] 0/1, or NULL for all present; absent learners'
+ *               buffers are never read and their pointers may be NULL
+ *   min_quorum  fewer present learners than max(1, min_quorum) gives
+ *               DL_ERR_QUORUM and leaves the state untouched
+ *   delta_bar_out device [n] fp32, out (D); may be NULL
+ * A zero total weight or a negative / non-finite weight gives DL_ERR_ARG.
+ */
+int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
+                        const float* d_codebook, const float* const* theta_k, int32_t K,
+                        const dl_fragment* frag, const float* weights, const uint8_t* present,
+                        int32_t min_quorum, float lr, float mu, float* delta_bar_out,
+                        void* stream);
+
+/*
+ * Device-side failure word of a workspace (0 = none). Kernels that wait on
+ * a bulk copy give up after a bounded time instead of hanging; they then set
+ * a bit here and the call's outputs are undefined. Blocks until the stream
+ * has finished, then copies the word to the host and clears it.
+ *   d_workspace  a workspace previously passed to dl_pseudograd_stats or
+ *                dl_quantize
+ *   status_out   host, out
+ */
+int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DILOCO_SYNC_H */

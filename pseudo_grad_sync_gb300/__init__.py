@@ -1,0 +1,236 @@
+"""Python binding of libdiloco_sync.so, the GB300 DiLoCo outer-sync library.
+
+Argument marshalling only: every step of the outer synchronisation runs in
+the library's CUDA kernels. PyTorch provides device memory and streams. The
+C entry points (see include/diloco_sync.h) keep their names here:
+
+    plan_fragments       balanced tensor -> fragment assignment (host)
+    pseudograd_stats     per-(learner, tensor) mu / sigma / clip range
+    quantize             uint8 codes + bucket-mean codebooks
+    merge_outer_step     decode, weighted fp32 mean, outer Nesterov (in place)
+
+``OuterSync`` bundles the three device calls of one fragment with their
+workspaces.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import _build
+
+DL_OK = 0
+DL_NBUCKETS = 256
+DL_MAX_LEARNERS = 32
+STATS_FIELDS = ("count", "nonfinite", "mean", "std", "lo", "hi")
+
+_lib = None
+
+
+class _Fragment(ctypes.Structure):
+    _fields_ = [("offsets", ctypes.c_void_p), ("d_offsets", ctypes.c_void_p),
+                ("n_tensors", ctypes.c_int32)]
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(f"{_build.LIB} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i32, i64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                      ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+        fr = ctypes.POINTER(_Fragment)
+        L.dl_version.restype = ctypes.c_int
+        L.dl_status_string.restype = ctypes.c_char_p
+        L.dl_status_string.argtypes = [ctypes.c_int]
+        L.dl_plan_fragments.restype = ctypes.c_int
+        L.dl_plan_fragments.argtypes = [vp, i32, i32, vp, vp]
+        L.dl_stats_workspace_bytes.restype = sz
+        L.dl_stats_workspace_bytes.argtypes = [fr, i32]
+        L.dl_pseudograd_stats.restype = ctypes.c_int
+        L.dl_pseudograd_stats.argtypes = [vp, vp, i32, fr, f64, vp, vp, sz, vp]
+        L.dl_quantize_workspace_bytes.restype = sz
+        L.dl_quantize_workspace_bytes.argtypes = [fr, i32]
+        L.dl_quantize.restype = ctypes.c_int
+        L.dl_quantize.argtypes = [vp, vp, i32, fr, vp, vp, vp, vp, vp, sz, vp]
+        L.dl_merge_outer_step.restype = ctypes.c_int
+        L.dl_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, fr, vp, vp, i32, f32, f32, vp,
+                                          vp]
+        L.dl_read_device_status.restype = ctypes.c_int
+        L.dl_read_device_status.argtypes = [vp, vp, vp]
+        _lib = L
+    return _lib
+
+
+class DLError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {lib().dl_status_string(status).decode()} (status {status})")
+
+
+def _check(fn, status):
+    if status != DL_OK:
+        raise DLError(fn, status)
+
+
+def status_string(status: int) -> str:
+    return lib().dl_status_string(status).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _ptr_array(tensors):
+    return (ctypes.c_void_p * len(tensors))(*[None if t is None else t.data_ptr() for t in tensors])
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Fragment:
+    """Tensor layout of one fragment: offsets on the host and on the device."""
+
+    def __init__(self, numels, device="cuda"):
+        numels = [int(x) for x in numels]
+        self.numels = numels
+        self.offsets = np.zeros(len(numels) + 1, dtype=np.int64)
+        np.cumsum(np.asarray(numels, dtype=np.int64), out=self.offsets[1:])
+        self.d_offsets = torch.from_numpy(self.offsets).to(device)
+        self.n = int(self.offsets[-1])
+        self.T = len(numels)
+        self._c = _Fragment(self.offsets.ctypes.data, self.d_offsets.data_ptr(), self.T)
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+
+def plan_fragments(numel, n_frags: int):
+    numel = np.ascontiguousarray(numel, dtype=np.int64)
+    frag = np.empty(len(numel), dtype=np.int32)
+    load = np.empty(n_frags, dtype=np.int64)
+    _check("dl_plan_fragments", lib().dl_plan_fragments(
+        numel.ctypes.data, len(numel), n_frags, frag.ctypes.data, load.ctypes.data))
+    return frag, load
+
+
+def stats_workspace_bytes(frag: Fragment, K: int) -> int:
+    return int(lib().dl_stats_workspace_bytes(frag.c, K))
+
+
+def quantize_workspace_bytes(frag: Fragment, K: int) -> int:
+    return int(lib().dl_quantize_workspace_bytes(frag.c, K))
+
+
+def new_workspace(nbytes: int, device="cuda"):
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def new_stats(K: int, T: int, device="cuda"):
+    """Device array of dl_stats, shape [K, T, 6] int64 (fields as raw 8-byte words)."""
+    return torch.zeros((K, T, 6), dtype=torch.int64, device=device)
+
+
+def stats_to_host(stats: torch.Tensor) -> dict:
+    """dl_stats array -> dict of numpy arrays [K, T] (count, nonfinite, mean, std, lo, hi)."""
+    raw = stats.detach().cpu().numpy()
+    f = raw.view(np.float64)
+    return {"count": raw[..., 0].copy(), "nonfinite": raw[..., 1].copy(), "mean": f[..., 2].copy(),
+            "std": f[..., 3].copy(), "lo": f[..., 4].copy(), "hi": f[..., 5].copy()}
+
+
+def pseudograd_stats(theta_g, replicas, frag: Fragment, clip_sigmas=6.0, stats=None,
+                     workspace=None, stream=None):
+    K = len(replicas)
+    if stats is None:
+        stats = new_stats(K, frag.T, theta_g.device)
+    need = stats_workspace_bytes(frag, K)
+    if workspace is None:
+        workspace = new_workspace(need, theta_g.device)
+    _check("dl_pseudograd_stats", lib().dl_pseudograd_stats(
+        _ptr(theta_g), _ptr_array(replicas), K, frag.c, float(clip_sigmas), _ptr(stats),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return stats
+
+
+def quantize(theta_g, replicas, frag: Fragment, stats, codes=None, codebook=None, counts=None,
+             workspace=None, stream=None):
+    K = len(replicas)
+    dev = theta_g.device
+    if codes is None:
+        codes = [torch.empty(frag.n, dtype=torch.uint8, device=dev) for _ in range(K)]
+    if codebook is None:
+        codebook = torch.empty((K, frag.T, DL_NBUCKETS), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(quantize_workspace_bytes(frag, K), dev)
+    _check("dl_quantize", lib().dl_quantize(
+        _ptr(theta_g), _ptr_array(replicas), K, frag.c, _ptr(stats), _ptr_array(codes),
+        _ptr(codebook), _ptr(counts), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return codes, codebook
+
+
+def merge_outer_step(theta_g, momentum, frag: Fragment, codes=None, codebook=None,
+                     replicas=None, weights=None, present=None, min_quorum=1, lr=0.7, mu=0.9,
+                     delta_bar=None, stream=None, K=None):
+    if K is None:
+        K = len(codes) if codes is not None else len(replicas)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
+    p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    _check("dl_merge_outer_step", lib().dl_merge_outer_step(
+        _ptr(theta_g), _ptr(momentum), None if codes is None else _ptr_array(codes),
+        _ptr(codebook), None if replicas is None else _ptr_array(replicas), K, frag.c,
+        None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
+        int(min_quorum), float(lr), float(mu), _ptr(delta_bar), _stream(stream)))
+
+
+def read_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check("dl_read_device_status",
+           lib().dl_read_device_status(_ptr(workspace), ctypes.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+class OuterSync:
+    """The three device calls of one fragment with preallocated buffers.
+
+    ``step`` computes stats, codes and codebooks of the K replicas, then merges
+    them into theta_g / momentum in place. Buffers are reused across calls.
+    """
+
+    def __init__(self, frag: Fragment, K: int, device="cuda", clip_sigmas=6.0, lr=0.7, mu=0.9):
+        self.frag, self.K, self.clip, self.lr, self.mu = frag, K, clip_sigmas, lr, mu
+        self.stats = new_stats(K, frag.T, device)
+        self.ws_stats = new_workspace(stats_workspace_bytes(frag, K), device)
+        self.ws_quant = new_workspace(quantize_workspace_bytes(frag, K), device)
+        self.codes = [torch.empty(max(frag.n, 1), dtype=torch.uint8, device=device)
+                      for _ in range(K)]
+        self.codebook = torch.empty((K, max(frag.T, 1), DL_NBUCKETS), dtype=torch.float32,
+                                    device=device)
+
+    def step(self, theta_g, momentum, replicas, weights=None, present=None, min_quorum=1,
+             delta_bar=None, stream=None, counts=None):
+        """One outer step; only present learners' replicas are read (others may be None)."""
+        idx = [k for k in range(len(replicas)) if present is None or present[k]]
+        if len(idx) < max(1, int(min_quorum)):
+            raise DLError("OuterSync.step", -3)
+        reps = [replicas[k] for k in idx]
+        kp = len(idx)
+        w = None if weights is None else np.asarray(weights, dtype=np.float32)[idx]
+        pseudograd_stats(theta_g, reps, self.frag, self.clip, self.stats[:kp], self.ws_stats,
+                         stream)
+        quantize(theta_g, reps, self.frag, self.stats[:kp], self.codes[:kp], self.codebook[:kp],
+                 counts, self.ws_quant, stream)
+        merge_outer_step(theta_g, momentum, self.frag, self.codes[:kp], self.codebook[:kp],
+                         weights=w, min_quorum=min_quorum, lr=self.lr, mu=self.mu,
+                         delta_bar=delta_bar, stream=stream)
+        return idx

@@ -1,0 +1,252 @@
+// Shared device helpers and host-side validation for the outer-sync kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "diloco_sync.h"
+
+namespace dl {
+
+// ---------------------------------------------------------------------------
+// work decomposition: a fragment is cut into fixed chunks of kChunk elements;
+// a chunk meets one or more tensors ("pieces"). Chunk c starts at c * kChunk,
+// so every chunk start is 32 KB aligned in an fp32 buffer.
+constexpr int kChunk = 8192;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kGroups = kChunk / 4 / kThreads;  // float4 groups per thread
+constexpr int kNB = DL_NBUCKETS;
+constexpr unsigned kFull = 0xffffffffu;
+
+// device failure bits (workspace status word)
+constexpr uint32_t kDevErrCopyTimeout = 1u;
+
+// bounded spin on an mbarrier: ~2^22 try_wait polls, each of which may
+// suspend for a short hardware-chosen time; far longer than any bulk copy.
+constexpr long kSpinLimit = 1L << 22;
+
+// tensors shorter than this take the fp64 per-element statistics path
+constexpr int64_t kSmallTensor = 4096;
+
+// workspace header: status word and padding
+constexpr size_t kWsHeader = 256;
+
+__host__ __device__ inline int64_t n_chunks_of(int64_t n) { return (n + kChunk - 1) / kChunk; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier + bulk (TMA engine) copies, sm_90+ forms.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// make the initialised barrier visible to the async (bulk copy) proxy
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// order this thread's earlier generic-proxy shared accesses before later
+// async-proxy writes into the same buffer
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; false after kSpinLimit polls (the caller records the failure).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (long i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// Stage [base, base+cn) of src into shared memory: the 16-byte multiple goes
+// through one bulk copy issued by thread 0, the 0..3 trailing floats through
+// plain loads. Every thread returns true when the data is visible to it;
+// on a copy that never lands, all threads return false and the status word
+// records it. `iter` counts completed phases of `bar`.
+__device__ __forceinline__ bool stage_chunk(float* dst, const float* src, int cn, uint64_t* bar,
+                                            uint32_t iter, int* flag, uint32_t* status) {
+    const int nvec = cn >> 2;
+    if (threadIdx.x == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvec) * 16u);
+        if (nvec > 0) bulk_copy_g2s(dst, src, static_cast<uint32_t>(nvec) * 16u, bar);
+    }
+    const int tail = cn & 3;
+    if (static_cast<int>(threadIdx.x) < tail) dst[nvec * 4 + threadIdx.x] = src[nvec * 4 + threadIdx.x];
+    if (threadIdx.x == 0) {
+        bool ok = mbar_wait_bounded(bar, iter & 1u);
+        if (!ok) {
+            atomicOr(status, kDevErrCopyTimeout);
+            mbar_wait_bounded(bar, iter & 1u);  // give the copy one more bounded chance to land
+        }
+        *flag = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (*flag == 0) return false;
+    // acquire the phase thread 0 saw complete (returns at once in every thread)
+    (void)mbar_try_wait(bar, iter & 1u);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Tensor lookup: smallest t with off[t+1] > pos (empty tensors are skipped).
+__device__ __forceinline__ int tensor_containing(const int64_t* __restrict__ off, int T,
+                                                 int64_t pos) {
+    int lo = 0, hi = T - 1;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(off + mid + 1) > pos)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// float-float (unevaluated sum hi + lo) accumulation, fp32 operations only.
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float b) {
+    float s = __fadd_rn(hi, b);
+    float v = __fsub_rn(s, hi);
+    float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, v)), __fsub_rn(b, v));
+    lo = __fadd_rn(lo, e);
+    hi = s;
+}
+
+__device__ __forceinline__ void ff_add_ff(float& ahi, float& alo, float bhi, float blo) {
+    float s = __fadd_rn(ahi, bhi);
+    float v = __fsub_rn(s, ahi);
+    float e = __fadd_rn(__fsub_rn(ahi, __fsub_rn(s, v)), __fsub_rn(bhi, v));
+    e = __fadd_rn(e, __fadd_rn(alo, blo));
+    float h = __fadd_rn(s, e);
+    alo = __fsub_rn(e, __fsub_rn(h, s));
+    ahi = h;
+}
+
+// ---------------------------------------------------------------------------
+// Quantiser parameters of one segment, derived identically by the encode
+// kernel and the codebook finalisation from (lo, hi, nonfinite).
+struct SegQuant {
+    int kind;         // 0 fast, 1 slow (all elements in fp64), 2 degenerate, 3 invalid
+    double lo, hi, s; // s = 256 / (hi - lo)
+    float lo_f, w_f, s_f, guard;
+    float scale;      // 2^ks as fp32 (fast kind only)
+    int ks;           // residual fixed-point exponent
+    double ref0, refw; // slow kind: residual reference ref0 + b * refw (fp64)
+};
+
+constexpr int kSegFast = 0, kSegSlow = 1, kSegDegenerate = 2, kSegInvalid = 3;
+// residual fixed point: q = rint(r * 2^ks) with w * 2^ks in [2^26, 2^27),
+// biased by 2^25 and packed as (1 << 44) + q + bias into one u64 counter
+constexpr int kResBits = 26;
+constexpr int64_t kResBias = int64_t(1) << 25;
+constexpr int kCountShift = 44;
+
+__device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long nonfinite) {
+    SegQuant q;
+    q.lo = lo;
+    q.hi = hi;
+    q.s = 0.0;
+    q.lo_f = q.w_f = q.s_f = q.guard = q.scale = 0.f;
+    q.ks = 0;
+    q.ref0 = q.refw = 0.0;
+    if (nonfinite > 0) {
+        q.kind = kSegInvalid;
+        return q;
+    }
+    if (!(hi - lo >= 256.0 * 1.17549435082228750797e-38)) {  // 256 * FLT_MIN
+        q.kind = kSegDegenerate;
+        return q;
+    }
+    q.s = 256.0 / (hi - lo);
+    const double w = (hi - lo) / 256.0;
+    q.lo_f = static_cast<float>(lo);
+    q.w_f = static_cast<float>(w);
+    q.s_f = static_cast<float>(q.s);
+    // |uf - u| <= (s |lo| + 3 * 257) 2^-24 for uf in [-1, 257]; guard twice that
+    const double g = (q.s * fabs(lo) + 800.0) * 0x1p-23;
+    q.guard = static_cast<float>(g);
+    int e_w;
+    frexp(static_cast<double>(q.w_f), &e_w);  // w_f = f * 2^e_w, f in [0.5, 1)
+    q.ks = kResBits + 1 - e_w;                  // w_f * 2^ks in [2^26, 2^27)
+    const bool fast = isfinite(q.lo_f) && isfinite(q.s_f) && q.w_f > 0.f && g < 0.25 &&
+                      q.ks >= -126 && q.ks <= 127 && fabs(hi) < 1e37 && fabs(lo) < 1e37;
+    if (fast) {
+        q.kind = kSegFast;
+        q.scale = ldexpf(1.0f, q.ks);
+    } else {
+        q.kind = kSegSlow;
+        q.ref0 = lo;
+        q.refw = w;
+        e_w = 0;
+        frexp(w, &e_w);
+        q.ks = kResBits + 1 - e_w;
+    }
+    return q;
+}
+
+// Residual reference of bucket b: the fp32 edge fmaf(b, w_f, lo_f) for the
+// fast kind (the element minus it is exact or within 2^-24 of a bucket width),
+// lo + b * w in fp64 for the slow kind. Encoder and finaliser both call this.
+__device__ __forceinline__ double seg_ref(const SegQuant& q, int b) {
+    if (q.kind == kSegFast) return static_cast<double>(__fmaf_rn(static_cast<float>(b), q.w_f, q.lo_f));
+    return fma(static_cast<double>(b), q.refw, q.ref0);
+}
+
+}  // namespace dl
+
+// ---------------------------------------------------------------------------
+// host side (defined in dl_host.cu)
+namespace dl {
+struct HostFrag {
+    const int64_t* offsets;
+    const int64_t* d_offsets;
+    int T;
+    int64_t n;
+};
+int check_fragment(const dl_fragment* frag, HostFrag* out);
+bool aligned16(const void* p);
+int sm_count();
+int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items);
+int cuda_status(cudaError_t e);
+int launch_status();
+}  // namespace dl

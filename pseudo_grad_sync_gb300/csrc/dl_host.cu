@@ -1,0 +1,128 @@
+// Host-side pieces of the C ABI: status strings, the fragment planner,
+// argument validation and launch sizing.
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "dl_common.cuh"
+
+extern "C" int dl_version(void) { return 100; }
+
+extern "C" const char* dl_status_string(int status) {
+    switch (status) {
+        case DL_OK: return "DL_OK";
+        case DL_ERR_ARG: return "DL_ERR_ARG: invalid argument";
+        case DL_ERR_ALIGN: return "DL_ERR_ALIGN: buffer not 16-byte (workspace: 256-byte) aligned";
+        case DL_ERR_QUORUM: return "DL_ERR_QUORUM: fewer present learners than the minimum quorum";
+        case DL_ERR_CUDA: return "DL_ERR_CUDA: CUDA runtime call or launch failed";
+        case DL_ERR_SHAPE: return "DL_ERR_SHAPE: offsets must start at 0 and not decrease";
+        case DL_ERR_WORKSPACE: return "DL_ERR_WORKSPACE: workspace missing or too small";
+        case DL_ERR_DEVICE: return "DL_ERR_DEVICE: a kernel reported a failure";
+        default: return "unknown status";
+    }
+}
+
+// Balanced tensor fragmentation, longest-processing-time greedy (Decoupled
+// DiLoCo note, architecture item 4). Fragments are kept in a min-heap keyed
+// by (load, index) so that ties go to the lowest fragment index.
+extern "C" int dl_plan_fragments(const int64_t* numel, int32_t n_tensors, int32_t n_frags,
+                                 int32_t* frag_of_tensor, int64_t* frag_load) {
+    if (n_frags <= 0 || n_tensors < 0 || !frag_load) return DL_ERR_ARG;
+    if (n_tensors > 0 && (!numel || !frag_of_tensor)) return DL_ERR_ARG;
+    for (int32_t t = 0; t < n_tensors; ++t)
+        if (numel[t] < 0) return DL_ERR_ARG;
+    std::vector<int32_t> order(static_cast<size_t>(n_tensors));
+    for (int32_t t = 0; t < n_tensors; ++t) order[t] = t;
+    std::sort(order.begin(), order.end(), [numel](int32_t a, int32_t b) {
+        return numel[a] != numel[b] ? numel[a] > numel[b] : a < b;
+    });
+    using Slot = std::pair<int64_t, int32_t>;  // (load, fragment)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t p = 0; p < n_frags; ++p) heap.push(Slot(0, p));
+    for (int32_t t : order) {
+        Slot s = heap.top();
+        heap.pop();
+        frag_of_tensor[t] = s.second;
+        s.first += numel[t];
+        heap.push(s);
+    }
+    while (!heap.empty()) {
+        frag_load[heap.top().second] = heap.top().first;
+        heap.pop();
+    }
+    return DL_OK;
+}
+
+extern "C" int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream) {
+    if (!d_workspace || !status_out) return DL_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, d_workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_workspace, 0, sizeof(v), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return DL_ERR_CUDA;
+    *status_out = v;
+    return DL_OK;
+}
+
+namespace dl {
+
+int check_fragment(const dl_fragment* frag, HostFrag* out) {
+    if (!frag || frag->n_tensors < 0) return DL_ERR_ARG;
+    out->T = frag->n_tensors;
+    out->offsets = frag->offsets;
+    out->d_offsets = frag->d_offsets;
+    out->n = 0;
+    if (frag->n_tensors == 0) return DL_OK;
+    if (!frag->offsets || !frag->d_offsets) return DL_ERR_ARG;
+    if (frag->offsets[0] != 0) return DL_ERR_SHAPE;
+    for (int32_t t = 0; t < frag->n_tensors; ++t)
+        if (frag->offsets[t + 1] < frag->offsets[t]) return DL_ERR_SHAPE;
+    out->n = frag->offsets[frag->n_tensors];
+    return DL_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 1;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+// Persistent grid: as many blocks as fit on every SM at once, never more than
+// there are work items. DL_GRID_LIMIT (environment) caps it further; tests
+// use that to make single blocks cover many chunks.
+int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess ||
+        per_sm <= 0)
+        per_sm = 1;
+    int64_t g = static_cast<int64_t>(per_sm) * sm_count();
+    if (const char* cap = getenv("DL_GRID_LIMIT")) {
+        const long v = strtol(cap, nullptr, 10);
+        if (v > 0 && v < g) g = v;
+    }
+    if (work_items < g) g = work_items;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DL_OK : DL_ERR_CUDA; }
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? DL_OK : DL_ERR_CUDA; }
+
+}  // namespace dl

@@ -1,0 +1,158 @@
+"""GPU path vs oracle on identical inputs: run both and check every output.
+
+Bars (per the outer-step tolerance contract):
+  * codes bit-exact, except elements whose oracle bucket coordinate u lies
+    within 1e-6 bucket widths of an integer (boundary exceptions, counted);
+  * mu within 5e-9 sigma and sigma within 5e-9 relative (fp64-grade stats:
+    the bucket rule is shifted by about 128 * dsigma/sigma + 21 * dmu/sigma
+    bucket widths, which must stay well below the 1e-6 exception band);
+  * codebook values within 2 fp32 ulps plus 2^-23 bucket widths (fixed-point
+    residual sums with 2^-26 steps, one final rounding), bucket counts exact
+    (both only where no boundary exception moved an element);
+  * relative L2 <= 1e-6 on Delta_bar, theta' and momentum'.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import pseudo_grad_sync_gb300 as dl
+
+TOL_REL_L2 = 1e-6
+TOL_BOUNDARY = 1e-6
+TOL_STATS = 5e-9
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    num = np.linalg.norm(a - b)
+    return float(num / den) if den > 0 else float(num)
+
+
+def gpu_outer_step(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, lr=0.7,
+                   mu=0.9, clip_sigmas=6.0, quantized=True):
+    dev = "cuda"
+    frag = dl.Fragment(numels, dev)
+    g_d = torch.from_numpy(np.ascontiguousarray(g)).to(dev)
+    reps_d = [torch.from_numpy(np.ascontiguousarray(r)).to(dev) for r in reps]
+    m_d = (torch.zeros_like(g_d) if m is None else torch.from_numpy(np.ascontiguousarray(m)).to(dev))
+    K = len(reps)
+    out = {}
+    db = torch.empty_like(g_d)
+    if quantized:
+        stats = dl.pseudograd_stats(g_d, reps_d, frag, clip_sigmas)
+        counts = torch.empty((K, frag.T, 256), dtype=torch.int32, device=dev)
+        codes, cb = dl.quantize(g_d, reps_d, frag, stats, counts=counts)
+        dl.merge_outer_step(g_d, m_d, frag, codes, cb, weights=weights, present=present,
+                            min_quorum=min_quorum, lr=lr, mu=mu, delta_bar=db)
+        torch.cuda.synchronize()
+        out["stats"] = dl.stats_to_host(stats)
+        out["codes"] = np.stack([c.cpu().numpy() for c in codes]) if K else None
+        out["codebook"] = cb.cpu().numpy()
+        out["counts"] = counts.cpu().numpy().view(np.uint32)
+    else:
+        dl.merge_outer_step(g_d, m_d, frag, replicas=reps_d, weights=weights, present=present,
+                            min_quorum=min_quorum, lr=lr, mu=mu, delta_bar=db)
+        torch.cuda.synchronize()
+    out["theta_g"] = g_d.cpu().numpy()
+    out["momentum"] = m_d.cpu().numpy()
+    out["delta_bar"] = db.cpu().numpy()
+    return out
+
+
+def check_stats(o_st, g_st, K, T):
+    assert np.array_equal(g_st["count"], o_st.count)
+    assert np.array_equal(g_st["nonfinite"], o_st.nonfinite)
+    for k in range(K):
+        for t in range(T):
+            if o_st.nonfinite[k, t] > 0:
+                assert np.isnan(g_st["mean"][k, t]) and np.isnan(g_st["lo"][k, t])
+                continue
+            s_o, s_g = o_st.std[k, t], g_st["std"][k, t]
+            m_o, m_g = o_st.mean[k, t], g_st["mean"][k, t]
+            if s_o == 0.0:
+                assert s_g == 0.0 and m_g == m_o, (k, t, m_o, m_g, s_g)
+                continue
+            assert abs(s_g - s_o) <= TOL_STATS * s_o, (k, t, s_o, s_g)
+            assert abs(m_g - m_o) <= TOL_STATS * s_o + 1e-15 * abs(m_o), (k, t, m_o, m_g, s_o)
+
+
+def check_codes(o, gp, g, reps, offsets):
+    """Returns the number of boundary exceptions; asserts there are no others."""
+    K = len(reps)
+    st = o["stats"]
+    exceptions = 0
+    moved = np.zeros((K, len(offsets) - 1, 256), dtype=bool)
+    for k in range(K):
+        diff = np.nonzero(gp["codes"][k] != o["codes"][k])[0]
+        if diff.size == 0:
+            continue
+        t_of = np.searchsorted(offsets, diff, side="right") - 1
+        for t in np.unique(t_of):
+            idx = diff[t_of == t]
+            u = oracle.bucket_coord(g, reps[k], idx, st.lo[k, t], st.hi[k, t])
+            dist = np.abs(u - np.round(u))
+            assert np.all(dist < TOL_BOUNDARY), (k, t, idx[dist >= TOL_BOUNDARY][:5],
+                                                 u[dist >= TOL_BOUNDARY][:5])
+            assert np.all(np.abs(gp["codes"][k][idx].astype(int) - o["codes"][k][idx]) == 1)
+            moved[k, t, gp["codes"][k][idx]] = True
+            moved[k, t, o["codes"][k][idx]] = True
+        exceptions += diff.size
+    return exceptions, moved
+
+
+def check_codebook(o, gp, moved):
+    st = o["stats"]
+    cb_o, cb_g = o["codebook"], gp["codebook"]
+    cnt_o, cnt_g = o["counts"], gp["counts"]
+    K, T, _ = cb_o.shape
+    for k in range(K):
+        for t in range(T):
+            keep = ~moved[k, t]
+            assert np.array_equal(cnt_g[k, t][keep], cnt_o[k, t][keep]), (k, t)
+            if st.nonfinite[k, t] > 0:
+                assert np.isnan(cb_g[k, t]).all()
+                continue
+            w = (st.hi[k, t] - st.lo[k, t]) / 256
+            a = cb_g[k, t][keep].astype(np.float64)
+            b = cb_o[k, t][keep].astype(np.float64)
+            tol = 2 * np.spacing(np.abs(cb_o[k, t][keep])).astype(np.float64) + w * 2.0**-23
+            assert np.all(np.abs(a - b) <= tol), (k, t, np.max(np.abs(a - b) - tol))
+
+
+def compare(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, lr=0.7, mu=0.9,
+            clip_sigmas=6.0, quantized=True, nan_ok=False):
+    offsets = np.zeros(len(numels) + 1, dtype=np.int64)
+    np.cumsum(numels, out=offsets[1:])
+    m0 = np.zeros_like(g) if m is None else m
+    o = oracle.outer_step(g, m0, reps, offsets=offsets, weights=weights, present=present,
+                          min_quorum=min_quorum, lr=lr, mu=mu, clip_sigmas=clip_sigmas,
+                          quantized=quantized)
+    assert o["status"] == 0
+    gp = gpu_outer_step(g, reps, numels, m0, weights, present, min_quorum, lr, mu, clip_sigmas,
+                        quantized)
+    report = {}
+    if quantized:
+        check_stats(o["stats"], gp["stats"], len(reps), len(numels))
+        exc, moved = check_codes(o, gp, g, reps, offsets)
+        check_codebook(o, gp, moved)
+        report["boundary_exceptions"] = exc
+    for key in ("delta_bar", "theta_g", "momentum"):
+        a, b = gp[key], o[key]
+        if nan_ok:
+            nan = np.isnan(b)
+            assert np.array_equal(np.isnan(a), nan), key
+            a, b = a[~nan], b[~nan]
+        r = rel_l2(a, b)
+        report[key] = r
+        assert r <= TOL_REL_L2, (key, r)
+    upd_o = (o["theta_g"].astype(np.float64) - g)
+    upd_g = (gp["theta_g"].astype(np.float64) - g)
+    if nan_ok:
+        keep = ~np.isnan(upd_o)
+        upd_o, upd_g = upd_o[keep], upd_g[keep]
+    report["update"] = rel_l2(upd_g, upd_o)
+    return report, o, gp

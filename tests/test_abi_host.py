@@ -1,0 +1,131 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared
+symbol, and its host logic (planner, argument validation, quorum) behaves -
+all without a GPU. Calls that would launch work are not made here; every
+case below returns during host-side validation."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import pseudo_grad_sync_gb300 as dl
+from pseudo_grad_sync_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return dl.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:[\w\s\*]+?)\b(dl_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"dl_plan_fragments", "dl_pseudograd_stats", "dl_quantize",
+            "dl_merge_outer_step"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.dl_version() == 100
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, 12345):
+        assert dl.status_string(code)
+
+
+def test_planner_matches_oracle(L):
+    rng = np.random.default_rng(0)
+    for _ in range(100):
+        T = int(rng.integers(0, 300))
+        P = int(rng.integers(1, 30))
+        sizes = rng.integers(0, 1 << 40, T) if rng.random() < 0.5 else rng.integers(0, 5, T)
+        f1, l1 = dl.plan_fragments(sizes, P)
+        f2, l2 = oracle.plan_fragments(sizes, P)
+        assert np.array_equal(f1, f2) and np.array_equal(l1, l2)
+
+
+def test_planner_rejects_bad_args(L):
+    with pytest.raises(dl.DLError):
+        dl.plan_fragments([1, 2, 3], 0)
+    with pytest.raises(dl.DLError):
+        dl.plan_fragments([1, -2, 3], 2)
+
+
+def _frag(offsets, dptr=16):
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    f = dl._Fragment(off.ctypes.data, dptr, len(off) - 1)
+    return f, off
+
+
+FAKE = 1 << 20  # a 16-byte aligned, never dereferenced device address
+
+
+def _ptrs(*vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def test_validation_errors_before_any_launch(L):
+    f, off = _frag([0, 10, 30])
+    fb = ctypes.byref(f)
+    ws = L.dl_stats_workspace_bytes(fb, 2)
+    assert ws > 0
+    # bad K, null arrays, misaligned pointers, short or misaligned workspace
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, FAKE), 0, fb, 6.0, FAKE, FAKE, ws, None) == -1
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, FAKE), 33, fb, 6.0, FAKE, FAKE, ws, None) == -1
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, None), 2, fb, 6.0, FAKE, FAKE, ws, None) == -1
+    assert L.dl_pseudograd_stats(FAKE + 4, _ptrs(FAKE, FAKE), 2, fb, 6.0, FAKE, FAKE, ws, None) == -2
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, FAKE), 2, fb, 0.0, FAKE, FAKE, ws, None) == -1
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, FAKE), 2, fb, 6.0, FAKE, FAKE, ws - 1, None) == -6
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE, FAKE), 2, fb, 6.0, FAKE, FAKE + 16, ws, None) == -2
+    # offsets must start at 0 and not decrease
+    g, _o = _frag([1, 10, 30])
+    assert L.dl_pseudograd_stats(FAKE, _ptrs(FAKE), 1, ctypes.byref(g), 6.0, FAKE, FAKE, ws, None) == -5
+    h, _o2 = _frag([0, 10, 5])
+    assert L.dl_quantize(FAKE, _ptrs(FAKE), 1, ctypes.byref(h), FAKE, _ptrs(FAKE), FAKE, None,
+                         FAKE, 1 << 30, None) == -5
+    # quantize: misaligned codes buffer, short workspace
+    wq = L.dl_quantize_workspace_bytes(fb, 1)
+    assert L.dl_quantize(FAKE, _ptrs(FAKE), 1, fb, FAKE, _ptrs(FAKE + 1), FAKE, None, FAKE, wq,
+                         None) == -2
+    assert L.dl_quantize(FAKE, _ptrs(FAKE), 1, fb, FAKE, _ptrs(FAKE), FAKE, None, FAKE, wq - 8,
+                         None) == -6
+
+
+def _merge(L, fb, K, weights=None, present=None, min_quorum=1, codes=True):
+    c = _ptrs(*([FAKE] * K))
+    w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+    p = None if present is None else np.ascontiguousarray(present, np.uint8)
+    return L.dl_merge_outer_step(
+        FAKE, FAKE, c if codes else None, FAKE, None if codes else c, K, fb,
+        None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
+        min_quorum, 0.7, 0.9, None, None)
+
+
+def test_merge_quorum_and_weight_rules_match_oracle(L):
+    # empty fragment (n = 0): validation still runs, nothing is launched
+    f, off = _frag([0, 0])
+    fb = ctypes.byref(f)
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        K = int(rng.integers(1, 9))
+        w = rng.choice([0.0, 0.5, 1.0, 2.0, -1.0, np.inf], K, p=[.2, .3, .2, .2, .05, .05])
+        p = (rng.random(K) < 0.6).astype(np.uint8)
+        q = int(rng.integers(0, 5))
+        st_or, _ = oracle.merge_weights(w.astype(np.float32), p, K, q)
+        st_dl = _merge(L, fb, K, w, p, q)
+        expect = st_or if st_or < 0 else 0
+        assert st_dl == expect, (w, p, q, st_or, st_dl)
+    assert _merge(L, fb, 33) == -1
+    assert _merge(L, fb, 0) == -1

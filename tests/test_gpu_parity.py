@@ -1,0 +1,165 @@
+"""CUDA path vs oracle on seeded inputs, element by element (needs a GPU).
+
+Sizes span several 8192-element chunks, ragged tensor boundaries, a ragged
+tail and the degenerate cases the method has (sigma = 0, empty tensors,
+non-finite values, |mu| >> sigma, a single learner, the largest K).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import synthetic
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import pseudo_grad_sync_gb300 as dl
+    dl.lib()
+
+
+def _make(numels, K, seed, scales=None, theta_std=0.02, dist="normal", mean_shift=None):
+    rng = np.random.default_rng(seed)
+    n = int(sum(numels))
+    g = (rng.standard_normal(n) * theta_std).astype(np.float32)
+    if scales is None:
+        scales = [1.2e-3] * len(numels)
+    sc = np.repeat(np.asarray(scales, dtype=np.float64), numels)
+    reps = []
+    for k in range(K):
+        if dist == "t3":
+            z = rng.standard_normal(n)
+            chi = rng.chisquare(3, n)
+            x = z / np.sqrt(chi / 3)
+        else:
+            x = rng.standard_normal(n)
+        d = sc * x
+        if mean_shift is not None:
+            d = d + np.repeat(np.asarray(mean_shift, dtype=np.float64), numels)
+        reps.append((g - d).astype(np.float32))
+    return g, reps
+
+
+RAGGED = [1, 3, 4095, 4096, 4097, 8191, 8192, 8193, 12345, 0, 70000, 64, 5, 16384, 2]
+
+
+def test_worked_example_full_size():
+    w = synthetic.worked_example(K=3)
+    g = w.theta_global(0)
+    reps = [w.replica(k, 0, g) for k in range(3)]
+    rep, o, gp = compare(g, reps, w.numels)
+    print("worked example:", rep)
+    assert rep["boundary_exceptions"] <= 20
+
+
+@pytest.mark.parametrize("K", [1, 3, 5])
+def test_ragged_fragment(K):
+    scales = [10 ** (-4 + 2 * (i % 3) / 2) for i in range(len(RAGGED))]
+    g, reps = _make(RAGGED, K, seed=K, scales=scales)
+    m = (np.random.default_rng(99).standard_normal(g.size) * 1e-3).astype(np.float32)
+    rep, _, _ = compare(g, reps, RAGGED, m=m)
+    print(K, rep)
+
+
+def test_max_learners_and_weights():
+    K = 32
+    sizes = [9000, 33, 20000]
+    g, reps = _make(sizes, K, seed=7)
+    rng = np.random.default_rng(8)
+    w = (0.5 + rng.random(K)).astype(np.float32)
+    present = (rng.random(K) < 0.7).astype(np.uint8)
+    present[3] = 1
+    rep, _, _ = compare(g, reps, sizes, weights=w, present=present, min_quorum=4)
+    print(rep)
+
+
+@pytest.mark.parametrize("np_", [1, 4, 5, 8, 9, 16, 17])
+def test_present_subsets(np_):
+    K = 17
+    sizes = [8192 * 3 + 100]
+    g, reps = _make(sizes, K, seed=np_)
+    present = np.zeros(K, dtype=np.uint8)
+    present[np.random.default_rng(np_).permutation(K)[:np_]] = 1
+    w = np.linspace(0.5, 1.5, K).astype(np.float32)
+    compare(g, reps, sizes, weights=w, present=present)
+
+
+def test_unquantised_mode_and_identity():
+    sizes = [8192 * 2 + 3, 77]
+    g, reps = _make(sizes, 4, seed=11)
+    compare(g, reps, sizes, quantized=False)
+    # K=1, no quantisation, lr=1, mu=0 returns theta_k exactly
+    g1 = (1.0 + np.random.default_rng(1).random(30001)).astype(np.float32)
+    r1 = (g1 - np.random.default_rng(2).standard_normal(30001) * 1e-3).astype(np.float32)
+    from parity import gpu_outer_step
+    out = gpu_outer_step(g1, [r1], [30001], lr=1.0, mu=0.0, quantized=False)
+    assert np.array_equal(out["theta_g"], r1)
+
+
+def test_degenerate_segments():
+    # sigma = 0 (constant Delta), |mu| >> sigma (fp64 guard path for every
+    # element), sigma far below the fp32 bucket-width range (fp64 residuals),
+    # |mu| ~ 100 sigma (fast path with a wide guard)
+    sizes = [10000, 9000, 5000, 7000, 300]
+    n = sum(sizes)
+    rng = np.random.default_rng(5)
+    g = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g[:10000] = 1.0
+    g[19000:24000] = 0.0
+    reps = []
+    for k in range(2):
+        d = np.empty(n)
+        d[:10000] = 0.25 * k
+        d[10000:19000] = 3.0 + rng.standard_normal(9000) * 1e-6
+        d[19000:24000] = rng.standard_normal(5000) * 1e-30
+        d[24000:31000] = 0.1 + rng.standard_normal(7000) * 1e-3
+        d[31000:] = rng.standard_normal(300) * 1e-3
+        reps.append((g - d).astype(np.float32))
+    rep, o, gp = compare(g, reps, sizes)
+    assert o["stats"].std[0, 0] == 0.0 and o["stats"].std[1, 0] == 0.0
+    assert (gp["codes"][:, :10000] == 0).all()
+    assert gp["codebook"][1, 0, 7] == np.float32(0.25)
+
+
+def test_nonfinite_segment_is_invalid():
+    sizes = [5000, 9000]
+    g, reps = _make(sizes, 2, seed=3)
+    reps[1][6000] = np.float32(np.inf)
+    rep, o, gp = compare(g, reps, sizes, nan_ok=True)
+    assert gp["stats"]["nonfinite"][1, 1] == 1
+    assert (gp["codes"][1, 5000:] == 0).all()
+    assert np.isnan(gp["theta_g"][5000:]).all() and np.isfinite(gp["theta_g"][:5000]).all()
+
+
+def test_heavy_tail_clipping():
+    sizes = [50000, 4096, 130000]
+    g, reps = _make(sizes, 3, seed=21, scales=[1e-3] * 3, dist="t3")
+    rep, o, gp = compare(g, reps, sizes)
+    clipped = (o["counts"][:, :, 0] + o["counts"][:, :, 255]).sum()
+    assert clipped > 100  # Student-t(3) puts ~2e-3 of the mass beyond 6 sigma
+
+
+def test_flush_path_with_one_block(monkeypatch):
+    # one block covers every chunk: the histogram must flush on capacity
+    monkeypatch.setenv("DL_GRID_LIMIT", "1")
+    sizes = [8192 * 20 + 5, 3000]
+    g, reps = _make(sizes, 2, seed=31)
+    compare(g, reps, sizes)
+
+
+def test_tail_not_multiple_of_four():
+    for n in (1, 2, 3, 5, 8191, 8193, 24579):
+        g, reps = _make([n], 2, seed=n)
+        compare(g, reps, [n])
+
+
+def test_empty_fragment_and_empty_tensors():
+    g, reps = _make([0, 0, 10, 0], 2, seed=1)
+    compare(g, reps, [0, 0, 10, 0])
