@@ -4,10 +4,13 @@
 //
 // Three launches on the caller's stream:
 //  k_shift     one warp per (k, t): c = mean of the first min(N, 64) values
-//              of Delta in fp64, rounded to fp32. Every block later sums
+//              of Delta in fp64, snapped to a power-of-two grid below their
+//              spread and rounded to fp32. Every block later sums
 //              y = Delta - c, which keeps the one-pass variance free of
 //              cancellation when |mu| >> sigma; c is computed once so all
-//              chunks of a tensor share it.
+//              chunks of a tensor share it. The snapping keeps the fp32
+//              rounding of y unbiased (a shift with low-order bits below
+//              ulp(y) biases every rounding the same way).
 //  k_stats     persistent blocks over 8192-element chunks of the fragment.
 //              theta_g's chunk is staged in shared memory by one bulk (TMA)
 //              copy and reused for all K learners; each learner's chunk is
@@ -15,7 +18,8 @@
 //              groups of four, folded into float-float (hi + lo) sums;
 //              per warp: a float-float butterfly; per block: an fp64 sum of
 //              the 8 warps, written as one partial per (k, chunk, tensor)
-//              piece. Tensors shorter than 4096 elements and rare large or
+//              piece. Tensors shorter than 4096 elements and groups of rare
+//              huge, tiny (squares would leave the fp32 normal range) or
 //              non-finite values take an fp64 path.
 //  k_stats_fin one warp per (k, t): fixed-order fp64 sum of its pieces, then
 //              mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population).
@@ -55,10 +59,27 @@ __global__ void __launch_bounds__(kThreads) k_shift(StatsArgs a) {
     const int64_t o = a.off[t];
     const int64_t N = a.off[t + 1] - o;
     const int m = N < 64 ? static_cast<int>(N) : 64;
-    double s = 0.0;
-    for (int i = lane; i < m; i += 32) s += static_cast<double>(__fsub_rn(a.g[o + i], a.r[k][o + i]));
+    const bool h0 = lane < m, h1 = lane + 32 < m;
+    const double v0 = h0 ? static_cast<double>(__fsub_rn(a.g[o + lane], a.r[k][o + lane])) : 0.0;
+    const double v1 = h1 ? static_cast<double>(__fsub_rn(a.g[o + lane + 32], a.r[k][o + lane + 32])) : 0.0;
+    double s = v0 + v1;
     for (int sh = 16; sh; sh >>= 1) s += __shfl_xor_sync(kFull, s, sh);
-    if (lane == 0) a.shift[w] = m > 0 ? static_cast<float>(s / m) : 0.0f;
+    const double mean = m > 0 ? s / m : 0.0;
+    double q = (h0 ? (v0 - mean) * (v0 - mean) : 0.0) + (h1 ? (v1 - mean) * (v1 - mean) : 0.0);
+    for (int sh = 16; sh; sh >>= 1) q += __shfl_xor_sync(kFull, q, sh);
+    if (lane != 0) return;
+    const double sd = m > 0 ? sqrt(q / m) : 0.0;
+    double c = mean;
+    if (sd > 0.0 && isfinite(sd) && isfinite(mean)) {
+        // snap to a power-of-two grid no finer than sd/8: the shift then has
+        // no bits below the ulp of any typical y = Delta - c, so rounding
+        // y to fp32 is unbiased
+        int ex;
+        frexp(sd, &ex);  // sd in [2^(ex-1), 2^ex)
+        const double grid = ldexp(1.0, ex - 3);
+        c = rint(mean / grid) * grid;
+    }
+    a.shift[w] = static_cast<float>(c);
 }
 
 // fp64 contribution of one value (small tensors, huge or non-finite values)
@@ -123,7 +144,8 @@ __global__ void __launch_bounds__(kThreads) k_stats(StatsArgs a) {
                         const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
                         const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
                         const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
-                        if (mx <= 0x1p48f) {  // false for NaN
+                        // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
+                        if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
                             const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
                             const float b2 = __fmaf_rn(
                                 y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
@@ -146,7 +168,8 @@ __global__ void __launch_bounds__(kThreads) k_stats(StatsArgs a) {
                             if (e < la || e >= lb) continue;
                             const float d = __fsub_rn(sg[e], __ldcs(rk + e));
                             const float y = __fsub_rn(d, csh);
-                            if (!small && fabsf(y) <= 0x1p48f) {
+                            const float ay = fabsf(y);
+                            if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
                                 ff_add(s1h, s1l, y);
                                 ff_add(s2h, s2l, __fmul_rn(y, y));
                             } else {
