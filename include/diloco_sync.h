@@ -176,6 +176,34 @@ int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* c
                         void* stream);
 
 /*
+ * dl_quantize without a caller-provided workspace. The pages have no
+ * counterpart: this is a library convenience, not part of the method.
+ *
+ * For callers that cannot allocate device memory - code whose device memory
+ * is owned by another allocator or budget (a framework's caching allocator,
+ * a plugin host), or code for which cudaMalloc is not allowed or too costly
+ * (it may synchronise the device). The scratch lives in one static device
+ * array of DL_QUANTIZE_NOALLOC_MAX_BYTES inside the library; every GPU that
+ * loads the library holds it until the process exits. Inputs and outputs
+ * are the caller's, exactly as for dl_quantize; results are identical.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, which keeps the last call's contents
+ *    (the call clears what must start at zero). Calls whose GPU work may
+ *    overlap - on different streams or from different host threads - race
+ *    on it and give wrong results; order them on one stream.
+ *  - A fragment whose scratch need (dl_quantize_workspace_bytes) exceeds the
+ *    array, i.e. K * n_tensors > 2047, gets DL_ERR_WORKSPACE and nothing is
+ *    launched.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define DL_QUANTIZE_NOALLOC_MAX_BYTES (8u * 1024u * 1024u)
+int dl_quantize_noalloc(const float* theta_g, const float* const* theta_k, int32_t K,
+                        const dl_fragment* frag, const dl_stats* d_stats, uint8_t* const* codes,
+                        float* d_codebook, uint32_t* d_counts, void* stream);
+
+/*
  * Device-side failure word of a workspace (0 = none). Kernels that wait on
  * a bulk copy give up after a bounded time instead of hanging; they then set
  * a bit here and the call's outputs are undefined. Blocks until the stream

@@ -22,6 +22,8 @@
 // k_cb_fin     one thread per (k, t, b): codebook value = reference + mean
 //              residual (fp64, rounded once to fp32), midpoint for an empty
 //              bucket, and the optional counts.
+#include <mutex>
+
 #include "dl_common.cuh"
 
 namespace dl {
@@ -298,4 +300,45 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     const int64_t cells = static_cast<int64_t>(K) * f.T * kNB;
     k_cb_fin<<<static_cast<unsigned>((cells + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
     return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// dl_quantize for callers that cannot allocate: the workspace is this static
+// device array (one per device, alive until the process exits). In host code
+// the symbol is only a stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device on the first call.
+
+namespace {
+static __device__ __align__(256) unsigned char g_quant_scratch[DL_QUANTIZE_NOALLOC_MAX_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+int scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DL_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_quant_scratch) != cudaSuccess || !p) return DL_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return DL_OK;
+}
+}  // namespace
+
+extern "C" int dl_quantize_noalloc(const float* theta_g, const float* const* theta_k, int32_t K,
+                                   const dl_fragment* frag, const dl_stats* d_stats,
+                                   uint8_t* const* codes, float* d_codebook, uint32_t* d_counts,
+                                   void* stream) {
+    HostFrag f;
+    int st = check_fragment(frag, &f);
+    if (st != DL_OK) return st;
+    if (K <= 0 || K > DL_MAX_LEARNERS) return DL_ERR_ARG;
+    if (dl_quantize_workspace_bytes(frag, K) > DL_QUANTIZE_NOALLOC_MAX_BYTES) return DL_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if ((st = scratch_address(&scratch)) != DL_OK) return st;
+    return dl_quantize(theta_g, theta_k, K, frag, d_stats, codes, d_codebook, d_counts, scratch,
+                       DL_QUANTIZE_NOALLOC_MAX_BYTES, stream);
 }
