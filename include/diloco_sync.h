@@ -193,12 +193,13 @@ int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* c
  *    (the call clears what must start at zero). Calls whose GPU work may
  *    overlap - on different streams or from different host threads - race
  *    on it and give wrong results; order them on one stream.
- *  - A fragment whose scratch need (dl_quantize_workspace_bytes) exceeds the
- *    array, i.e. K * n_tensors > 2047, gets DL_ERR_WORKSPACE and nothing is
- *    launched.
+ *  - A fragment with K * n_tensors > DL_QUANTIZE_NOALLOC_MAX_SEGMENTS (its
+ *    scratch need would not fit the array) gets DL_ERR_WORKSPACE and nothing
+ *    is launched.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 #define DL_QUANTIZE_NOALLOC_MAX_BYTES (8u * 1024u * 1024u)
+#define DL_QUANTIZE_NOALLOC_MAX_SEGMENTS 2000
 int dl_quantize_noalloc(const float* theta_g, const float* const* theta_k, int32_t K,
                         const dl_fragment* frag, const dl_stats* d_stats, uint8_t* const* codes,
                         float* d_codebook, uint32_t* d_counts, void* stream);

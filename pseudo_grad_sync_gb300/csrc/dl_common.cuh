@@ -32,6 +32,11 @@ constexpr int64_t kSmallTensor = 4096;
 // workspace header: status word and padding
 constexpr size_t kWsHeader = 256;
 
+// learner-major grids: block b serves learner b % K and every (G/K)-th chunk
+// from b / K; at most this many blocks per learner, and in all
+constexpr int kMaxBlocksPerLearner = 1024;
+constexpr int kMaxBlocksTotal = 2048;
+
 __host__ __device__ inline int64_t n_chunks_of(int64_t n) { return (n + kChunk - 1) / kChunk; }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -175,11 +180,11 @@ struct SegQuant {
 };
 
 constexpr int kSegFast = 0, kSegSlow = 1, kSegDegenerate = 2, kSegInvalid = 3;
-// residual fixed point: q = rint(r * 2^ks) with w * 2^ks in [2^26, 2^27),
-// biased by 2^25 and packed as (1 << 44) + q + bias into one u64 counter
-constexpr int kResBits = 26;
-constexpr int64_t kResBias = int64_t(1) << 25;
-constexpr int kCountShift = 44;
+// residual fixed point: q = rint(r * 2^ks) with w * 2^ks in [2^22, 2^23),
+// biased by 2^14 so that the small negative residuals of elements at a bucket
+// edge stay positive; the biased value is below 2^24
+constexpr int kResBits = 22;
+constexpr int64_t kResBias = int64_t(1) << 14;
 
 __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long nonfinite) {
     SegQuant q;
@@ -207,7 +212,7 @@ __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long no
     q.guard = static_cast<float>(g);
     int e_w;
     frexp(static_cast<double>(q.w_f), &e_w);  // w_f = f * 2^e_w, f in [0.5, 1)
-    q.ks = kResBits + 1 - e_w;                  // w_f * 2^ks in [2^26, 2^27)
+    q.ks = kResBits + 1 - e_w;                  // w_f * 2^ks in [2^22, 2^23)
     const bool fast = isfinite(q.lo_f) && isfinite(q.s_f) && q.w_f > 0.f && g < 0.25 &&
                       q.ks >= -126 && q.ks <= 127 && fabs(hi) < 1e37 && fabs(lo) < 1e37;
     if (fast) {
@@ -247,6 +252,7 @@ int check_fragment(const dl_fragment* frag, HostFrag* out);
 bool aligned16(const void* p);
 int sm_count();
 int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items);
+int blocks_per_learner(const void* kernel, int threads, size_t smem, int K, int64_t n_chunks);
 int cuda_status(cudaError_t e);
 int launch_status();
 }  // namespace dl

@@ -121,6 +121,17 @@ int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items) {
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Learner-major persistent grid: J blocks per learner, K * J blocks in all,
+// as many as fit on the GPU at once (never more than there are chunks).
+int blocks_per_learner(const void* kernel, int threads, size_t smem, int K, int64_t n_chunks) {
+    const int total = grid_for(kernel, threads, smem, int64_t(1) << 40);
+    int64_t j = total / K;
+    if (j < 1) j = 1;
+    if (j > kMaxBlocksPerLearner) j = kMaxBlocksPerLearner;
+    if (j > n_chunks) j = n_chunks;
+    return static_cast<int>(j < 1 ? 1 : j);
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? DL_OK : DL_ERR_CUDA; }
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DL_OK : DL_ERR_CUDA; }

@@ -1,24 +1,29 @@
 // Uniform quantisation with clipping and a bucket-mean codebook (INTELLECT-1
 // notes, section 4.1 steps 2-4), fused with the uint8 encode.
 //
-// k_quantize   persistent blocks over 8192-element chunks; theta_g's chunk is
-//              staged in shared memory by one bulk (TMA) copy and reused for
-//              all K learners. Per element of learner k:
+// k_qparams    one thread per (k, t): the segment's quantiser parameters.
+// k_quantize   learner-major persistent grid: block b serves learner k = b % K
+//              and every J-th 8192-element chunk, so the K blocks reading one
+//              chunk of theta_g run together (theta_g crosses HBM once, then
+//              comes from L2). Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
 //                  fp32; when u is within a proven error guard of an integer
 //                  (or outside (0, 256)) the element is redone in fp64 with
 //                  the exact definition, so codes equal the fp64 rule;
 //                * codebook sum: the residual r = clamp(Delta) - e_b, e_b the
 //                  fp32 bucket edge fmaf(b, w_f, lo_f), is exact or within
-//                  2^-24 bucket widths; it becomes a fixed-point integer (2^26 steps per bucket
-//                  width) and added, together with a count of one, as a single
-//                  64-bit shared-memory atomic into the block's histogram
-//                  (count in bits 44..63). Integer sums make the result
-//                  independent of the order of the additions;
+//                  2^-24 bucket widths; it becomes a biased fixed-point
+//                  integer q (2^22 steps per bucket width, below 2^24) that is
+//                  added with two 32-bit shared-memory atomics: word A gets
+//                  (1 << 18) + (q >> 19) (count in bits 18..31), word B gets
+//                  q & (2^19 - 1). Both stay exact for up to 8192 elements;
 //                * the code byte is written with 32-bit stores (4 per store).
-//              Block histograms are flushed into a [K][T][256] global
-//              (count, residual-sum) table with integer atomics whenever the
-//              block moves to another tensor or may reach 2^16 elements.
+//              After each chunk (one block barrier) thread b folds bin b of
+//              the chunk's histogram into 64-bit per-bin sums it owns (the
+//              histograms are double-buffered, so one barrier suffices);
+//              those go to a [K][T][256] (count, residual-sum) table with
+//              integer atomics when the block moves to another tensor.
+//              Integer sums make the result independent of addition order.
 // k_cb_fin     one thread per (k, t, b): codebook value = reference + mean
 //              residual (fp64, rounded once to fp32), midpoint for an empty
 //              bucket, and the optional counts.
@@ -29,13 +34,19 @@
 namespace dl {
 namespace {
 
+struct SegRt {  // quantiser parameters of one (k, t) segment
+    SegQuant q;
+    float mid_g;  // 0.5 - guard
+};
+
 struct QuantArgs {
     const float* g;
     const float* r[DL_MAX_LEARNERS];
     uint8_t* codes[DL_MAX_LEARNERS];
     const int64_t* off;
     const dl_stats* stats;
-    unsigned long long* acc;  // [K*T*256] x (count, residual sum)
+    SegRt* seg;               // [K*T]
+    unsigned long long* acc;  // [K*T*256] x (count, biased residual sum)
     float* cb;
     uint32_t* counts;
     uint32_t* status;
@@ -43,19 +54,25 @@ struct QuantArgs {
     int64_t n_chunks;
     int T;
     int K;
+    int J;  // blocks per learner
 };
 
-// elements a block may add to one bucket between flushes: every packed
-// value is < 2^28 and the low field holds 44 bits
-constexpr int kFlushLimit = 1 << 16;
+constexpr uint32_t kLoMask = (1u << 19) - 1;
+constexpr uint32_t kCountOne = 1u << 18;
+constexpr uint32_t kQMax = (1u << 24) - 1;
 
-struct SegRt {  // per-(k, current tensor) parameters kept in shared memory
-    SegQuant q;
-    float hi_g;   // 256 - guard
-    float mid_g;  // 0.5 - guard
-};
+__global__ void __launch_bounds__(kThreads) k_qparams(QuantArgs a) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= a.K * a.T) return;
+    const dl_stats st = a.stats[i];
+    SegRt p;
+    p.q = seg_quant(st.lo, st.hi, st.nonfinite);
+    p.mid_g = 0.5f - p.q.guard;
+    a.seg[i] = p;
+}
 
-__device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, int& qv) {
+// fp64 path of one element: the exact bucket rule and residual
+__device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, uint32_t& qv) {
     const double u = __dmul_rn(__dsub_rn(static_cast<double>(d), q.lo), q.s);
     int bb = u < 0.0 ? 0 : (u >= 256.0 ? 255 : static_cast<int>(floor(u)));
     if (bb > 255) bb = 255;
@@ -63,137 +80,124 @@ __device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, in
     if (v < q.lo) v = q.lo;
     if (v > q.hi) v = q.hi;
     const double r = __dsub_rn(v, seg_ref(q, bb));
+    long long x = llrint(ldexp(r, q.ks)) + kResBias;
+    x = x < 0 ? 0 : (x > static_cast<long long>(kQMax) ? static_cast<long long>(kQMax) : x);
     b = bb;
-    qv = static_cast<int>(llrint(ldexp(r, q.ks))) + static_cast<int>(kResBias);
+    qv = static_cast<uint32_t>(x);
 }
 
 // bucket of one value and its histogram update; returns the code
-__device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p,
-                                               unsigned long long* __restrict__ hk) {
-    int b, qv;
+__device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p, uint32_t* __restrict__ hA) {
     const float t = __fsub_rn(d, p.q.lo_f);
     const float uf = __fmul_rn(t, p.q.s_f);
     const float bf = floorf(uf);
     const float fr = __fsub_rn(uf, bf);
-    if (p.q.kind == kSegFast && uf >= p.q.guard && uf <= p.hi_g &&
+    int b = static_cast<int>(bf);
+    uint32_t qv;
+    if (p.q.kind == kSegFast && static_cast<unsigned>(b) < 256u &&
         fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
-        b = static_cast<int>(bf);
         const float r = __fsub_rn(d, __fmaf_rn(bf, p.q.w_f, p.q.lo_f));
-        qv = __float2int_rn(__fmul_rn(r, p.q.scale)) + static_cast<int>(kResBias);
+        qv = min(__float2uint_rn(__fmaf_rn(r, p.q.scale, static_cast<float>(kResBias))), kQMax);
     } else {
         rare_code(d, p.q, b, qv);
     }
-    atomicAdd(hk + b, (1ull << kCountShift) + static_cast<unsigned long long>(static_cast<unsigned>(qv)));
+    atomicAdd(hA + b, kCountOne + (qv >> 19));
+    atomicAdd(hA + kNB + b, qv & kLoMask);
     return static_cast<uint32_t>(b);
 }
 
-__device__ void flush_hist(unsigned long long* hist, const QuantArgs& a, int t) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < a.K * kNB; i += kThreads) {
-        const unsigned long long v = hist[i];
-        if (v) {
-            const int k = i >> 8, b = i & (kNB - 1);
-            unsigned long long* dst =
-                a.acc + ((static_cast<int64_t>(k) * a.T + t) * kNB + b) * 2;
-            atomicAdd(dst, v >> kCountShift);
-            atomicAdd(dst + 1, v & ((1ull << kCountShift) - 1));
-            hist[i] = 0ull;
-        }
+__device__ __forceinline__ void flush_bin(const QuantArgs& a, int k, int t, int b,
+                                          unsigned long long* l2) {
+    if (l2[b] != 0ull) {
+        unsigned long long* dst = a.acc + ((static_cast<int64_t>(k) * a.T + t) * kNB + b) * 2;
+        atomicAdd(dst, l2[b]);
+        atomicAdd(dst + 1, l2[kNB + b]);
     }
-    __syncthreads();
+    l2[b] = 0ull;
+    l2[kNB + b] = 0ull;
 }
 
-__global__ void __launch_bounds__(kThreads) k_quantize(QuantArgs a) {
-    extern __shared__ __align__(16) float sg[];  // kChunk floats, then K*256 u64
-    unsigned long long* hist = reinterpret_cast<unsigned long long*>(sg + kChunk);
-    __shared__ uint64_t bar;
-    __shared__ int flag;
-    __shared__ SegRt seg[DL_MAX_LEARNERS];
+__global__ void __launch_bounds__(kThreads, 2) k_quantize(QuantArgs a) {
+    __shared__ uint32_t l1[2][2 * kNB];             // [parity][word A bins | word B bins]
+    __shared__ unsigned long long l2[2 * kNB];       // [count bins | residual-sum bins]
 
     const int tid = threadIdx.x;
-    for (int i = tid; i < a.K * kNB; i += kThreads) hist[i] = 0ull;
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_barrier_init();
-    }
+    const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
+    const float* __restrict__ g = a.g;
+    const float* __restrict__ rk = a.r[k];
+    uint8_t* __restrict__ ck = a.codes[k];
+    l1[0][tid] = l1[0][kNB + tid] = l1[1][tid] = l1[1][kNB + tid] = 0u;
+    l2[tid] = l2[kNB + tid] = 0ull;
     __syncthreads();
 
-    int cur_t = -1;
-    int acc_elems = 0;
-    uint32_t iter = 0;
-    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++iter) {
+    int cur_t = -1;  // tensor whose sums are in l2
+    int seg_t = -1;  // tensor whose parameters are in p
+    int par = 0;
+    SegRt p;
+    for (int64_t c = j; c < a.n_chunks; c += a.J) {
         const int64_t base = c * kChunk;
-        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        if (!stage_chunk(sg, a.g + base, cn, &bar, iter, &flag, a.status)) return;
-        const int64_t cend = base + cn;
+        const int64_t cend = min(base + kChunk, a.n);
         for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
             const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
             if (o0 >= cend) break;
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            const int plen = static_cast<int>(pb - pa);
-            if (t != cur_t || acc_elems + plen > kFlushLimit) {
-                if (cur_t >= 0) flush_hist(hist, a, cur_t);
-                if (t != cur_t) {
-                    if (tid < a.K) {
-                        const dl_stats st = a.stats[static_cast<int64_t>(tid) * a.T + t];
-                        SegRt p;
-                        p.q = seg_quant(st.lo, st.hi, st.nonfinite);
-                        p.hi_g = 256.0f - p.q.guard;
-                        p.mid_g = 0.5f - p.q.guard;
-                        seg[tid] = p;
-                    }
-                    __syncthreads();
-                }
-                cur_t = t;
-                acc_elems = 0;
+            if (t != seg_t) {
+                p = a.seg[static_cast<int64_t>(k) * a.T + t];
+                seg_t = t;
             }
-            acc_elems += plen;
             const bool full = (pa == base) && (pb == base + kChunk);
-            const int la = static_cast<int>(pa - base), lb = static_cast<int>(pb - base);
-
-            for (int k = 0; k < a.K; ++k) {
-                const SegRt p = seg[k];
-                uint8_t* ck = a.codes[k] + base;
-                const float* rk = a.r[k] + base;
-                unsigned long long* hk = hist + k * kNB;
-                if (p.q.kind >= kSegDegenerate) {  // every code is 0
-                    if (full) {
-#pragma unroll
-                        for (int j = 0; j < kGroups; ++j)
-                            reinterpret_cast<uint32_t*>(ck)[tid + j * kThreads] = 0u;
-                    } else {
-                        for (int e = la + tid; e < lb; e += kThreads) ck[e] = 0;
-                    }
-                    continue;
-                }
+            if (p.q.kind >= kSegDegenerate) {  // every code is 0, no sums
                 if (full) {
-                    float4 v[kGroups];
 #pragma unroll
-                    for (int j = 0; j < kGroups; ++j)
-                        v[j] = __ldcs(reinterpret_cast<const float4*>(rk) + tid + j * kThreads);
-#pragma unroll
-                    for (int j = 0; j < kGroups; ++j) {
-                        const float4 gg = reinterpret_cast<const float4*>(sg)[tid + j * kThreads];
-                        const uint32_t b0 = encode_one(__fsub_rn(gg.x, v[j].x), p, hk);
-                        const uint32_t b1 = encode_one(__fsub_rn(gg.y, v[j].y), p, hk);
-                        const uint32_t b2 = encode_one(__fsub_rn(gg.z, v[j].z), p, hk);
-                        const uint32_t b3 = encode_one(__fsub_rn(gg.w, v[j].w), p, hk);
-                        reinterpret_cast<uint32_t*>(ck)[tid + j * kThreads] =
-                            b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                    }
+                    for (int q = 0; q < kGroups; ++q)
+                        reinterpret_cast<uint32_t*>(ck + base)[tid + q * kThreads] = 0u;
                 } else {
-                    for (int e = la + tid; e < lb; e += kThreads) {
-                        const float d = __fsub_rn(sg[e], __ldcs(rk + e));
-                        ck[e] = static_cast<uint8_t>(encode_one(d, p, hk));
-                    }
+                    for (int64_t e = pa + tid; e < pb; e += kThreads) ck[e] = 0;
+                }
+                continue;
+            }
+            uint32_t* hA = l1[par];
+            if (full) {
+                const float4* g4 = reinterpret_cast<const float4*>(g + base);
+                const float4* r4 = reinterpret_cast<const float4*>(rk + base);
+                uint32_t* c4 = reinterpret_cast<uint32_t*>(ck + base);
+                float4 gv[kGroups], rv[kGroups];
+#pragma unroll
+                for (int q = 0; q < kGroups; ++q) gv[q] = __ldg(g4 + tid + q * kThreads);
+#pragma unroll
+                for (int q = 0; q < kGroups; ++q) rv[q] = __ldcs(r4 + tid + q * kThreads);
+#pragma unroll
+                for (int q = 0; q < kGroups; ++q) {
+                    const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
+                    const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
+                    const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
+                    const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
+                    c4[tid + q * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                }
+            } else {
+                for (int64_t e = pa + tid; e < pb; e += kThreads) {
+                    const float d = __fsub_rn(__ldg(g + e), __ldcs(rk + e));
+                    ck[e] = static_cast<uint8_t>(encode_one(d, p, hA));
                 }
             }
+            __syncthreads();  // every update of this piece is in l1[par]
+            if (cur_t != t) {
+                if (cur_t >= 0) flush_bin(a, k, cur_t, tid, l2);
+                cur_t = t;
+            }
+            const uint32_t va = hA[tid], vb = hA[kNB + tid];
+            if (va != 0u) {
+                l2[tid] += va >> 18;
+                l2[kNB + tid] += (static_cast<unsigned long long>(va & ((1u << 18) - 1)) << 19) + vb;
+                hA[tid] = 0u;
+                hA[kNB + tid] = 0u;
+            }
+            par ^= 1;
         }
-        __syncthreads();  // the staged chunk is about to be overwritten
     }
-    if (cur_t >= 0) flush_hist(hist, a, cur_t);
+    if (cur_t >= 0) flush_bin(a, k, cur_t, tid, l2);
 }
 
 __global__ void __launch_bounds__(kThreads) k_cb_fin(QuantArgs a) {
@@ -227,6 +231,8 @@ __global__ void __launch_bounds__(kThreads) k_cb_fin(QuantArgs a) {
     if (a.counts) a.counts[idx] = static_cast<uint32_t>(cnt);
 }
 
+size_t seg_bytes(int K, int T) { return align256(sizeof(SegRt) * static_cast<size_t>(K) * T); }
+
 size_t acc_bytes(int K, int T) {
     return align256(sizeof(unsigned long long) * 2 * static_cast<size_t>(K) * T * kNB);
 }
@@ -239,7 +245,7 @@ using namespace dl;
 extern "C" size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    return kWsHeader + acc_bytes(K, f.T);
+    return kWsHeader + seg_bytes(K, f.T) + acc_bytes(K, f.T);
 }
 
 extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
@@ -278,7 +284,8 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     a.stats = d_stats;
     char* ws = static_cast<char*>(d_workspace);
     a.status = reinterpret_cast<uint32_t*>(ws);
-    a.acc = reinterpret_cast<unsigned long long*>(ws + kWsHeader);
+    a.seg = reinterpret_cast<SegRt*>(ws + kWsHeader);
+    a.acc = reinterpret_cast<unsigned long long*>(ws + kWsHeader + seg_bytes(K, f.T));
     a.cb = d_codebook;
     a.counts = d_counts;
     a.n = f.n;
@@ -288,13 +295,12 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, acc_bytes(K, f.T), s))) != DL_OK) return st;
+    const int segs = K * f.T;
+    k_qparams<<<(segs + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
+    if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        const size_t smem = sizeof(float) * kChunk + sizeof(unsigned long long) * kNB * K;
-        if ((st = cuda_status(cudaFuncSetAttribute(k_quantize, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem)))) != DL_OK)
-            return st;
-        const int grid = grid_for(reinterpret_cast<const void*>(k_quantize), kThreads, smem, a.n_chunks);
-        k_quantize<<<grid, kThreads, smem, s>>>(a);
+        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_quantize), kThreads, 0, K, a.n_chunks);
+        k_quantize<<<K * a.J, kThreads, 0, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     const int64_t cells = static_cast<int64_t>(K) * f.T * kNB;
@@ -336,7 +342,9 @@ extern "C" int dl_quantize_noalloc(const float* theta_g, const float* const* the
     int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
     if (K <= 0 || K > DL_MAX_LEARNERS) return DL_ERR_ARG;
-    if (dl_quantize_workspace_bytes(frag, K) > DL_QUANTIZE_NOALLOC_MAX_BYTES) return DL_ERR_WORKSPACE;
+    if (static_cast<int64_t>(K) * f.T > DL_QUANTIZE_NOALLOC_MAX_SEGMENTS ||
+        dl_quantize_workspace_bytes(frag, K) > DL_QUANTIZE_NOALLOC_MAX_BYTES)
+        return DL_ERR_WORKSPACE;
     void* scratch = nullptr;
     if ((st = scratch_address(&scratch)) != DL_OK) return st;
     return dl_quantize(theta_g, theta_k, K, frag, d_stats, codes, d_codebook, d_counts, scratch,

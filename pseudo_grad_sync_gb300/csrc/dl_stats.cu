@@ -11,17 +11,19 @@
 //              chunks of a tensor share it. The snapping keeps the fp32
 //              rounding of y unbiased (a shift with low-order bits below
 //              ulp(y) biases every rounding the same way).
-//  k_stats     persistent blocks over 8192-element chunks of the fragment.
-//              theta_g's chunk is staged in shared memory by one bulk (TMA)
-//              copy and reused for all K learners; each learner's chunk is
-//              streamed with 128-bit loads. Per thread: fp32 sums over
-//              groups of four, folded into float-float (hi + lo) sums;
-//              per warp: a float-float butterfly; per block: an fp64 sum of
-//              the 8 warps, written as one partial per (k, chunk, tensor)
-//              piece. Tensors shorter than 4096 elements and groups of rare
-//              huge, tiny (squares would leave the fp32 normal range) or
+//  k_stats     learner-major persistent grid: block b serves learner
+//              k = b % K and every J-th 8192-element chunk, so the K blocks
+//              that read one chunk of theta_g run together and theta_g comes
+//              from HBM once, then from L2. Loads are 128-bit (8 of theta_g
+//              and 8 of the replica per thread in flight). Per thread: fp32
+//              sums over groups of four, folded into float-float (hi + lo)
+//              sums that persist across all chunks of a tensor; the block
+//              reduces them (float-float butterfly, fp64 over the 8 warps)
+//              only when it moves to another tensor, into partial slot
+//              (k, t, j). Tensors shorter than 4096 elements and groups of
+//              rare huge, tiny (squares would leave the fp32 normal range) or
 //              non-finite values take an fp64 path.
-//  k_stats_fin one warp per (k, t): fixed-order fp64 sum of its pieces, then
+//  k_stats_fin one warp per (k, t): fixed-order fp64 sum of its J partials, then
 //              mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population).
 // The result is deterministic: every sum has a fixed order.
 #include "dl_common.cuh"
@@ -45,9 +47,9 @@ struct StatsArgs {
     uint32_t* status;
     int64_t n;
     int64_t n_chunks;
-    int64_t P;  // partial slots per learner: n_chunks + T
     int T;
     int K;
+    int J;  // blocks per learner
     double clip;
 };
 
@@ -93,164 +95,170 @@ __device__ __forceinline__ void side_add(float d, float c, double& s1, double& s
     s2 = fma(y, y, s2);
 }
 
-__global__ void __launch_bounds__(kThreads) k_stats(StatsArgs a) {
-    extern __shared__ __align__(16) float sg[];  // kChunk floats of theta_g
-    __shared__ uint64_t bar;
-    __shared__ int flag;
-    __shared__ float red_ff[DL_MAX_LEARNERS][kWarps][4];
-    __shared__ double red_side[DL_MAX_LEARNERS][kWarps][2];
-    __shared__ int red_bad[DL_MAX_LEARNERS][kWarps];
+struct Acc {
+    float s1h, s1l, s2h, s2l;  // float-float sums of y and y^2
+    double s1d, s2d;           // fp64 side sums
+    int bad;
+    bool side;
+    __device__ __forceinline__ void reset() {
+        s1h = s1l = s2h = s2l = 0.f;
+        s1d = s2d = 0.0;
+        bad = 0;
+        side = false;
+    }
+};
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_barrier_init();
+// Block-wide reduction of the per-thread sums of tensor t into its partial
+// slot (k, t, j). Fixed order everywhere, so the result is deterministic.
+__device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
+                              float (*red_ff)[4], double (*red_side)[2], int* red_bad) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int sh = 16; sh; sh >>= 1) {
+        const float o1h = __shfl_xor_sync(kFull, acc.s1h, sh);
+        const float o1l = __shfl_xor_sync(kFull, acc.s1l, sh);
+        const float o2h = __shfl_xor_sync(kFull, acc.s2h, sh);
+        const float o2l = __shfl_xor_sync(kFull, acc.s2l, sh);
+        ff_add_ff(acc.s1h, acc.s1l, o1h, o1l);
+        ff_add_ff(acc.s2h, acc.s2l, o2h, o2l);
+    }
+    if (__any_sync(kFull, acc.side)) {
+        for (int sh = 16; sh; sh >>= 1) {
+            acc.s1d += __shfl_xor_sync(kFull, acc.s1d, sh);
+            acc.s2d += __shfl_xor_sync(kFull, acc.s2d, sh);
+            acc.bad += __shfl_xor_sync(kFull, acc.bad, sh);
+        }
+    } else {
+        acc.s1d = acc.s2d = 0.0;
+        acc.bad = 0;
+    }
+    if (lane == 0) {
+        red_ff[warp][0] = acc.s1h;
+        red_ff[warp][1] = acc.s1l;
+        red_ff[warp][2] = acc.s2h;
+        red_ff[warp][3] = acc.s2l;
+        red_side[warp][0] = acc.s1d;
+        red_side[warp][1] = acc.s2d;
+        red_bad[warp] = acc.bad;
     }
     __syncthreads();
+    if (threadIdx.x == 0) {
+        double s1 = 0.0, s2 = 0.0;
+        long long bad = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            s1 += static_cast<double>(red_ff[w][0]) + static_cast<double>(red_ff[w][1]) + red_side[w][0];
+            s2 += static_cast<double>(red_ff[w][2]) + static_cast<double>(red_ff[w][3]) + red_side[w][1];
+            bad += red_bad[w];
+        }
+        Partial p;
+        p.s1 = s1;
+        p.s2 = s2;
+        p.bad = bad;
+        p.pad = 0;
+        a.part[(static_cast<int64_t>(k) * a.T + t) * a.J + j] = p;
+    }
+    __syncthreads();
+}
 
-    uint32_t iter = 0;
-    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++iter) {
+// Learner-major persistent grid: block b serves learner k = b % K and chunks
+// j, j + J, j + 2J, ... with j = b / K. The K blocks that read the same chunk
+// of theta_g run side by side, so theta_g crosses HBM once and is served to
+// the other K - 1 from L2. Each thread keeps its sums across every chunk of
+// a tensor; the block reduces them only when the tensor changes.
+__global__ void __launch_bounds__(kThreads) k_stats(StatsArgs a) {
+    __shared__ float red_ff[kWarps][4];
+    __shared__ double red_side[kWarps][2];
+    __shared__ int red_bad[kWarps];
+
+    const int tid = threadIdx.x;
+    const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
+    const float* __restrict__ rk = a.r[k];
+    const float* __restrict__ g = a.g;
+    int cur_t = -1;
+    float csh = 0.f;
+    bool small = false;
+    Acc acc;
+    acc.reset();
+
+    for (int64_t c = j; c < a.n_chunks; c += a.J) {
         const int64_t base = c * kChunk;
-        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        if (!stage_chunk(sg, a.g + base, cn, &bar, iter, &flag, a.status)) return;
-        const int64_t cend = base + cn;
+        const int64_t cend = min(base + kChunk, a.n);
         for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
             const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
             if (o0 >= cend) break;
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            const bool small = (o1 - o0) < kSmallTensor;
-            const bool full = (pa == base) && (pb == base + kChunk);
-            const int la = static_cast<int>(pa - base), lb = static_cast<int>(pb - base);
-
-            for (int k = 0; k < a.K; ++k) {
-                const float csh = __ldg(a.shift + k * a.T + t);
-                const float* rk = a.r[k] + base;
-                float s1h = 0.f, s1l = 0.f, s2h = 0.f, s2l = 0.f;
-                double s1d = 0.0, s2d = 0.0;
-                int bad = 0;
-                bool side = false;
-                if (full && !small) {
-                    float4 v[kGroups];
+            if (t != cur_t) {
+                if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
+                cur_t = t;
+                csh = __ldg(a.shift + k * a.T + t);
+                small = (o1 - o0) < kSmallTensor;
+                acc.reset();
+            }
+            if (pa == base && pb == base + kChunk && !small) {
+                const float4* g4 = reinterpret_cast<const float4*>(g + base);
+                const float4* r4 = reinterpret_cast<const float4*>(rk + base);
+                float4 gv[kGroups], rv[kGroups];
 #pragma unroll
-                    for (int j = 0; j < kGroups; ++j)
-                        v[j] = __ldcs(reinterpret_cast<const float4*>(rk) + tid + j * kThreads);
+                for (int q = 0; q < kGroups; ++q) gv[q] = __ldg(g4 + tid + q * kThreads);
 #pragma unroll
-                    for (int j = 0; j < kGroups; ++j) {
-                        const float4 gg = reinterpret_cast<const float4*>(sg)[tid + j * kThreads];
-                        const float d0 = __fsub_rn(gg.x, v[j].x), d1 = __fsub_rn(gg.y, v[j].y);
-                        const float d2 = __fsub_rn(gg.z, v[j].z), d3 = __fsub_rn(gg.w, v[j].w);
-                        const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
-                        const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
-                        const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
-                        // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
-                        if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
-                            const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
-                            const float b2 = __fmaf_rn(
-                                y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
-                            ff_add(s1h, s1l, b1);
-                            ff_add(s2h, s2l, b2);
-                        } else {
-                            side = true;
-                            side_add(d0, csh, s1d, s2d, bad);
-                            side_add(d1, csh, s1d, s2d, bad);
-                            side_add(d2, csh, s1d, s2d, bad);
-                            side_add(d3, csh, s1d, s2d, bad);
-                        }
-                    }
-                } else {
-                    for (int j = 0; j < kGroups; ++j) {
-                        const int e0 = 4 * (tid + j * kThreads);
-                        if (e0 >= lb || e0 + 4 <= la) continue;
-                        for (int i = 0; i < 4; ++i) {
-                            const int e = e0 + i;
-                            if (e < la || e >= lb) continue;
-                            const float d = __fsub_rn(sg[e], __ldcs(rk + e));
-                            const float y = __fsub_rn(d, csh);
-                            const float ay = fabsf(y);
-                            if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
-                                ff_add(s1h, s1l, y);
-                                ff_add(s2h, s2l, __fmul_rn(y, y));
-                            } else {
-                                side = true;
-                                side_add(d, csh, s1d, s2d, bad);
-                            }
-                        }
+                for (int q = 0; q < kGroups; ++q) rv[q] = __ldcs(r4 + tid + q * kThreads);
+#pragma unroll
+                for (int q = 0; q < kGroups; ++q) {
+                    const float d0 = __fsub_rn(gv[q].x, rv[q].x), d1 = __fsub_rn(gv[q].y, rv[q].y);
+                    const float d2 = __fsub_rn(gv[q].z, rv[q].z), d3 = __fsub_rn(gv[q].w, rv[q].w);
+                    const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
+                    const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
+                    const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
+                    // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
+                    if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
+                        const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
+                        const float b2 = __fmaf_rn(
+                            y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
+                        ff_add(acc.s1h, acc.s1l, b1);
+                        ff_add(acc.s2h, acc.s2l, b2);
+                    } else {
+                        acc.side = true;
+                        side_add(d0, csh, acc.s1d, acc.s2d, acc.bad);
+                        side_add(d1, csh, acc.s1d, acc.s2d, acc.bad);
+                        side_add(d2, csh, acc.s1d, acc.s2d, acc.bad);
+                        side_add(d3, csh, acc.s1d, acc.s2d, acc.bad);
                     }
                 }
-                // warp: float-float butterfly (symmetric, so every lane ends equal)
-#pragma unroll
-                for (int sh = 16; sh; sh >>= 1) {
-                    const float o1h = __shfl_xor_sync(kFull, s1h, sh);
-                    const float o1l = __shfl_xor_sync(kFull, s1l, sh);
-                    const float o2h = __shfl_xor_sync(kFull, s2h, sh);
-                    const float o2l = __shfl_xor_sync(kFull, s2l, sh);
-                    ff_add_ff(s1h, s1l, o1h, o1l);
-                    ff_add_ff(s2h, s2l, o2h, o2l);
-                }
-                if (__any_sync(kFull, side)) {
-                    for (int sh = 16; sh; sh >>= 1) {
-                        s1d += __shfl_xor_sync(kFull, s1d, sh);
-                        s2d += __shfl_xor_sync(kFull, s2d, sh);
-                        bad += __shfl_xor_sync(kFull, bad, sh);
+            } else {
+                for (int64_t e = pa + tid; e < pb; e += kThreads) {
+                    const float d = __fsub_rn(__ldg(g + e), __ldcs(rk + e));
+                    const float y = __fsub_rn(d, csh);
+                    const float ay = fabsf(y);
+                    if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
+                        ff_add(acc.s1h, acc.s1l, y);
+                        ff_add(acc.s2h, acc.s2l, __fmul_rn(y, y));
+                    } else {
+                        acc.side = true;
+                        side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
                     }
-                } else {
-                    s1d = s2d = 0.0;
-                    bad = 0;
-                }
-                if (lane == 0) {
-                    red_ff[k][warp][0] = s1h;
-                    red_ff[k][warp][1] = s1l;
-                    red_ff[k][warp][2] = s2h;
-                    red_ff[k][warp][3] = s2l;
-                    red_side[k][warp][0] = s1d;
-                    red_side[k][warp][1] = s2d;
-                    red_bad[k][warp] = bad;
                 }
             }
-            __syncthreads();
-            if (tid < a.K) {
-                double s1 = 0.0, s2 = 0.0;
-                long long bad = 0;
-                for (int w = 0; w < kWarps; ++w) {
-                    s1 += static_cast<double>(red_ff[tid][w][0]) + static_cast<double>(red_ff[tid][w][1]) +
-                          red_side[tid][w][0];
-                    s2 += static_cast<double>(red_ff[tid][w][2]) + static_cast<double>(red_ff[tid][w][3]) +
-                          red_side[tid][w][1];
-                    bad += red_bad[tid][w];
-                }
-                Partial p;
-                p.s1 = s1;
-                p.s2 = s2;
-                p.bad = bad;
-                p.pad = 0;
-                a.part[static_cast<int64_t>(tid) * a.P + c + t] = p;
-            }
-            __syncthreads();
         }
-        __syncthreads();  // the staged chunk is about to be overwritten
     }
+    if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
 }
 
 __global__ void __launch_bounds__(kThreads) k_stats_fin(StatsArgs a) {
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= a.K * a.T) return;
-    const int k = w / a.T, t = w % a.T;
-    const int64_t o0 = a.off[t], o1 = a.off[t + 1];
-    const int64_t N = o1 - o0;
+    const int t = w % a.T;
+    const int64_t N = a.off[t + 1] - a.off[t];
     double s1 = 0.0, s2 = 0.0;
     long long bad = 0;
-    if (N > 0) {
-        const int64_t c0 = o0 / kChunk, c1 = (o1 - 1) / kChunk;
-        const Partial* pk = a.part + static_cast<int64_t>(k) * a.P + t;
-        for (int64_t c = c0 + lane; c <= c1; c += 32) {
-            const Partial p = pk[c];
-            s1 += p.s1;
-            s2 += p.s2;
-            bad += p.bad;
-        }
+    const Partial* pw = a.part + static_cast<int64_t>(w) * a.J;
+    for (int jj = lane; jj < a.J; jj += 32) {
+        const Partial p = pw[jj];
+        s1 += p.s1;
+        s2 += p.s2;
+        bad += p.bad;
     }
     for (int sh = 16; sh; sh >>= 1) {
         s1 += __shfl_xor_sync(kFull, s1, sh);
@@ -282,6 +290,8 @@ __global__ void __launch_bounds__(kThreads) k_stats_fin(StatsArgs a) {
 
 size_t shift_bytes(int K, int T) { return align256(sizeof(float) * static_cast<size_t>(K) * T); }
 
+int max_blocks_per_learner(int K) { return kMaxBlocksTotal / K; }
+
 }  // namespace
 }  // namespace dl
 
@@ -290,8 +300,8 @@ using namespace dl;
 extern "C" size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    const int64_t P = n_chunks_of(f.n) + f.T;
-    return kWsHeader + shift_bytes(K, f.T) + align256(sizeof(Partial) * static_cast<size_t>(K) * P);
+    return kWsHeader + shift_bytes(K, f.T) +
+           align256(sizeof(Partial) * static_cast<size_t>(K) * f.T * max_blocks_per_learner(K));
 }
 
 extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* theta_k, int32_t K,
@@ -330,20 +340,24 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     a.out = d_stats;
     a.n = f.n;
     a.n_chunks = n_chunks_of(f.n);
-    a.P = a.n_chunks + f.T;
     a.T = f.T;
     a.K = K;
     a.clip = clip_sigmas;
+    a.J = 1;
+    if (a.n_chunks > 0) {
+        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_stats), kThreads, 0, K, a.n_chunks);
+        if (a.J > max_blocks_per_learner(K)) a.J = max_blocks_per_learner(K);
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(K) * f.T * a.J;
+    if ((st = cuda_status(cudaMemsetAsync(a.part, 0, part_bytes, s))) != DL_OK) return st;
     const int warps = K * f.T;
     const int small_grid = (warps * 32 + kThreads - 1) / kThreads;
     k_shift<<<small_grid, kThreads, 0, s>>>(a);
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        const size_t smem = sizeof(float) * kChunk;
-        const int grid = grid_for(reinterpret_cast<const void*>(k_stats), kThreads, smem, a.n_chunks);
-        k_stats<<<grid, kThreads, smem, s>>>(a);
+        k_stats<<<K * a.J, kThreads, 0, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     k_stats_fin<<<small_grid, kThreads, 0, s>>>(a);
