@@ -133,6 +133,65 @@ __device__ __forceinline__ bool stage_chunk(float* dst, const float* src, int cn
 }
 
 // ---------------------------------------------------------------------------
+// Tile pipeline: a producer warp streams (theta_g, theta_k) tiles of TILE
+// elements into a ring of STAGES shared-memory stages with bulk copies;
+// consumer warps wait on the stage's "full" mbarrier and release it through
+// its "empty" mbarrier (one arrival per consumer warp). Waits are bounded: a
+// wait that runs out records kDevErrCopyTimeout and goes on, so no warp ever
+// blocks a barrier the others wait at.
+constexpr int kConsumerWarps = kWarps;
+constexpr int kPipeThreads = kThreads + 32;  // + one producer warp
+constexpr int kMaxStages = 4;
+
+struct PipeBarriers {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+};
+
+template <int STAGES>
+__device__ __forceinline__ void pipe_init(PipeBarriers* pb) {
+    static_assert(STAGES <= kMaxStages, "too many stages");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&pb->full[s], 1);
+            mbar_init(&pb->empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    if (!mbar_wait_bounded(bar, parity)) atomicOr(status, kDevErrCopyTimeout);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// barrier among the consumer warps only (named barrier 1)
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory");
+}
+
+// Producer side: lane 0 of the producer warp issues the bulk copies of tile
+// number `it` (its stage is it % STAGES) covering [tb, tb + tn) of two arrays.
+template <int TILE, int STAGES>
+__device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float* sb, const float* ga,
+                                             const float* gb, int64_t tb, int tn, uint32_t it,
+                                             uint32_t* status) {
+    const int s = static_cast<int>(it % STAGES);
+    if (it >= STAGES) wait_or_flag(&pb->empty[s], ((it / STAGES) - 1) & 1u, status);
+    const uint32_t bytes = static_cast<uint32_t>(tn >> 2) * 16u;
+    fence_proxy_async();
+    mbar_arrive_expect_tx(&pb->full[s], 2u * bytes);
+    if (bytes) {
+        bulk_copy_g2s(sa + s * TILE, ga + tb, bytes, &pb->full[s]);
+        bulk_copy_g2s(sb + s * TILE, gb + tb, bytes, &pb->full[s]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Tensor lookup: smallest t with off[t+1] > pos (empty tensors are skipped).
 __device__ __forceinline__ int tensor_containing(const int64_t* __restrict__ off, int T,
                                                  int64_t pos) {
@@ -174,6 +233,7 @@ struct SegQuant {
     int kind;         // 0 fast, 1 slow (all elements in fp64), 2 degenerate, 3 invalid
     double lo, hi, s; // s = 256 / (hi - lo)
     float lo_f, w_f, s_f, guard;
+    float c_f;        // fl32(-lo_f * s_f): u is evaluated as fmaf(d, s_f, c_f)
     float scale;      // 2^ks as fp32 (fast kind only)
     int ks;           // residual fixed-point exponent
     double ref0, refw; // slow kind: residual reference ref0 + b * refw (fp64)
@@ -191,7 +251,7 @@ __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long no
     q.lo = lo;
     q.hi = hi;
     q.s = 0.0;
-    q.lo_f = q.w_f = q.s_f = q.guard = q.scale = 0.f;
+    q.lo_f = q.w_f = q.s_f = q.guard = q.scale = q.c_f = 0.f;
     q.ks = 0;
     q.ref0 = q.refw = 0.0;
     if (nonfinite > 0) {
@@ -207,8 +267,11 @@ __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long no
     q.lo_f = static_cast<float>(lo);
     q.w_f = static_cast<float>(w);
     q.s_f = static_cast<float>(q.s);
-    // |uf - u| <= (s |lo| + 3 * 257) 2^-24 for uf in [-1, 257]; guard twice that
-    const double g = (q.s * fabs(lo) + 800.0) * 0x1p-23;
+    q.c_f = static_cast<float>(-static_cast<double>(q.lo_f) * static_cast<double>(q.s_f));
+    // u_f = fl(d * s_f + c_f) against u = (d - lo) s: s_f, lo_f and c_f each
+    // carry one fp32 rounding and the fma one more, so for u_f in [-1, 257]
+    // |u_f - u| <= (4 s|lo| + 2 * 258) 2^-24; the guard is twice that
+    const double g = (4.0 * q.s * fabs(lo) + 520.0) * 0x1p-23;
     q.guard = static_cast<float>(g);
     int e_w;
     frexp(static_cast<double>(q.w_f), &e_w);  // w_f = f * 2^e_w, f in [0.5, 1)

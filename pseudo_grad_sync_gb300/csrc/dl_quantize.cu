@@ -5,9 +5,10 @@
 // k_quantize   learner-major persistent grid: block b serves learner k = b % K
 //              and every J-th 8192-element chunk, so the K blocks reading one
 //              chunk of theta_g run together (theta_g crosses HBM once, then
-//              comes from L2). Per element of learner k:
+//              comes from L2); each chunk is loaded in two halves with
+//              128-bit loads. Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
-//                  fp32; when u is within a proven error guard of an integer
+//                  fp32 with one fma; when u is within a proven error guard of an integer
 //                  (or outside (0, 256)) the element is redone in fp64 with
 //                  the exact definition, so codes equal the fp64 rule;
 //                * codebook sum: the residual r = clamp(Delta) - e_b, e_b the
@@ -18,9 +19,9 @@
 //                  (1 << 18) + (q >> 19) (count in bits 18..31), word B gets
 //                  q & (2^19 - 1). Both stay exact for up to 8192 elements;
 //                * the code byte is written with 32-bit stores (4 per store).
-//              After each chunk (one block barrier) thread b folds bin b of
-//              the chunk's histogram into 64-bit per-bin sums it owns (the
-//              histograms are double-buffered, so one barrier suffices);
+//              After each piece (chunk x tensor; one block barrier) thread b
+//              folds bin b of the histogram into 64-bit per-bin sums it owns
+//              (the histograms are double-buffered, so one barrier suffices);
 //              those go to a [K][T][256] (count, residual-sum) table with
 //              integer atomics when the block moves to another tensor.
 //              Integer sums make the result independent of addition order.
@@ -87,20 +88,28 @@ __device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, ui
 }
 
 // bucket of one value and its histogram update; returns the code
-__device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p, uint32_t* __restrict__ hA) {
-    const float t = __fsub_rn(d, p.q.lo_f);
-    const float uf = __fmul_rn(t, p.q.s_f);
+__device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_t* __restrict__ hA) {
+    const float uf = __fmaf_rn(d, p.q.s_f, p.q.c_f);
     const float bf = floorf(uf);
     const float fr = __fsub_rn(uf, bf);
     int b = static_cast<int>(bf);
     uint32_t qv;
-    if (p.q.kind == kSegFast && static_cast<unsigned>(b) < 256u &&
-        fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
+    if (static_cast<unsigned>(b) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
         const float r = __fsub_rn(d, __fmaf_rn(bf, p.q.w_f, p.q.lo_f));
-        qv = min(__float2uint_rn(__fmaf_rn(r, p.q.scale, static_cast<float>(kResBias))), kQMax);
+        qv = __float2uint_rn(__fmaf_rn(r, p.q.scale, static_cast<float>(kResBias)));
     } else {
         rare_code(d, p.q, b, qv);
     }
+    atomicAdd(hA + b, kCountOne + (qv >> 19));
+    atomicAdd(hA + kNB + b, qv & kLoMask);
+    return static_cast<uint32_t>(b);
+}
+
+__device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p, uint32_t* __restrict__ hA) {
+    if (p.q.kind == kSegFast) return encode_fast(d, p, hA);
+    int b;
+    uint32_t qv;
+    rare_code(d, p.q, b, qv);
     atomicAdd(hA + b, kCountOne + (qv >> 19));
     atomicAdd(hA + kNB + b, qv & kLoMask);
     return static_cast<uint32_t>(b);
@@ -117,7 +126,7 @@ __device__ __forceinline__ void flush_bin(const QuantArgs& a, int k, int t, int 
     l2[kNB + b] = 0ull;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_quantize(QuantArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     __shared__ uint32_t l1[2][2 * kNB];             // [parity][word A bins | word B bins]
     __shared__ unsigned long long l2[2 * kNB];       // [count bins | residual-sum bins]
 
@@ -163,18 +172,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_quantize(QuantArgs a) {
                 const float4* g4 = reinterpret_cast<const float4*>(g + base);
                 const float4* r4 = reinterpret_cast<const float4*>(rk + base);
                 uint32_t* c4 = reinterpret_cast<uint32_t*>(ck + base);
-                float4 gv[kGroups], rv[kGroups];
+#pragma unroll 1
+                for (int h = 0; h < kGroups; h += kGroups / 2) {  // two halves: fewer registers
+                    float4 gv[kGroups / 2], rv[kGroups / 2];
 #pragma unroll
-                for (int q = 0; q < kGroups; ++q) gv[q] = __ldg(g4 + tid + q * kThreads);
+                    for (int q = 0; q < kGroups / 2; ++q) gv[q] = __ldg(g4 + tid + (h + q) * kThreads);
 #pragma unroll
-                for (int q = 0; q < kGroups; ++q) rv[q] = __ldcs(r4 + tid + q * kThreads);
+                    for (int q = 0; q < kGroups / 2; ++q) rv[q] = __ldcs(r4 + tid + (h + q) * kThreads);
+                    if (p.q.kind == kSegFast) {
 #pragma unroll
-                for (int q = 0; q < kGroups; ++q) {
-                    const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
-                    const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
-                    const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
-                    const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
-                    c4[tid + q * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        for (int q = 0; q < kGroups / 2; ++q) {
+                            const uint32_t b0 = encode_fast(__fsub_rn(gv[q].x, rv[q].x), p, hA);
+                            const uint32_t b1 = encode_fast(__fsub_rn(gv[q].y, rv[q].y), p, hA);
+                            const uint32_t b2 = encode_fast(__fsub_rn(gv[q].z, rv[q].z), p, hA);
+                            const uint32_t b3 = encode_fast(__fsub_rn(gv[q].w, rv[q].w), p, hA);
+                            c4[tid + (h + q) * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        }
+                    } else {
+                        for (int q = 0; q < kGroups / 2; ++q) {
+                            const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
+                            const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
+                            const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
+                            const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
+                            c4[tid + (h + q) * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        }
+                    }
                 }
             } else {
                 for (int64_t e = pa + tid; e < pb; e += kThreads) {

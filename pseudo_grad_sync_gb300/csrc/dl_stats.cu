@@ -14,8 +14,10 @@
 //  k_stats     learner-major persistent grid: block b serves learner
 //              k = b % K and every J-th 8192-element chunk, so the K blocks
 //              that read one chunk of theta_g run together and theta_g comes
-//              from HBM once, then from L2. Loads are 128-bit (8 of theta_g
-//              and 8 of the replica per thread in flight). Per thread: fp32
+//              from HBM once, then from L2. A producer warp streams the
+//              (theta_g, theta_k) tiles into a 3-stage shared-memory ring
+//              with bulk copies (TMA engine), 8 consumer warps compute from
+//              shared memory. Per thread: fp32
 //              sums over groups of four, folded into float-float (hi + lo)
 //              sums that persist across all chunks of a tensor; the block
 //              reduces them (float-float butterfly, fp64 over the 8 warps)
@@ -108,8 +110,9 @@ struct Acc {
     }
 };
 
-// Block-wide reduction of the per-thread sums of tensor t into its partial
-// slot (k, t, j). Fixed order everywhere, so the result is deterministic.
+// Reduction over the consumer warps of the per-thread sums of tensor t into
+// its partial slot (k, t, j). Fixed order everywhere, so the result is
+// deterministic.
 __device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
                               float (*red_ff)[4], double (*red_side)[2], int* red_bad) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -141,11 +144,11 @@ __device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
         red_side[warp][1] = acc.s2d;
         red_bad[warp] = acc.bad;
     }
-    __syncthreads();
+    consumer_sync();
     if (threadIdx.x == 0) {
         double s1 = 0.0, s2 = 0.0;
         long long bad = 0;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kConsumerWarps; ++w) {
             s1 += static_cast<double>(red_ff[w][0]) + static_cast<double>(red_ff[w][1]) + red_side[w][0];
             s2 += static_cast<double>(red_ff[w][2]) + static_cast<double>(red_ff[w][3]) + red_side[w][1];
             bad += red_bad[w];
@@ -157,89 +160,129 @@ __device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
         p.pad = 0;
         a.part[(static_cast<int64_t>(k) * a.T + t) * a.J + j] = p;
     }
-    __syncthreads();
+    consumer_sync();
+}
+
+__device__ __forceinline__ void add_group(Acc& acc, float4 gv, float4 rv, float csh) {
+    const float d0 = __fsub_rn(gv.x, rv.x), d1 = __fsub_rn(gv.y, rv.y);
+    const float d2 = __fsub_rn(gv.z, rv.z), d3 = __fsub_rn(gv.w, rv.w);
+    const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
+    const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
+    const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
+    // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
+    if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
+        const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
+        const float b2 = __fmaf_rn(y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
+        ff_add(acc.s1h, acc.s1l, b1);
+        ff_add(acc.s2h, acc.s2l, b2);
+    } else {
+        acc.side = true;
+        side_add(d0, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(d1, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(d2, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(d3, csh, acc.s1d, acc.s2d, acc.bad);
+    }
 }
 
 // Learner-major persistent grid: block b serves learner k = b % K and chunks
 // j, j + J, j + 2J, ... with j = b / K. The K blocks that read the same chunk
 // of theta_g run side by side, so theta_g crosses HBM once and is served to
-// the other K - 1 from L2. Each thread keeps its sums across every chunk of
-// a tensor; the block reduces them only when the tensor changes.
-__global__ void __launch_bounds__(kThreads) k_stats(StatsArgs a) {
-    __shared__ float red_ff[kWarps][4];
-    __shared__ double red_side[kWarps][2];
-    __shared__ int red_bad[kWarps];
+// the other K - 1 from L2. A producer warp streams the (theta_g, theta_k)
+// tiles of those chunks into a 3-stage shared-memory ring with bulk copies;
+// 8 consumer warps compute from shared memory. Each consumer thread keeps its
+// sums across every tile of a tensor; the consumers reduce them only when
+// they move to another tensor.
+constexpr int kTile = 4096;   // elements per pipeline tile
+constexpr int kStages = 3;    // tiles in flight per block
 
-    const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kPipeThreads, 2) k_stats(StatsArgs a) {
+    extern __shared__ __align__(128) float smem[];  // [kStages][kTile] theta_g, then theta_k
+    float* sg = smem;
+    float* sr = smem + kStages * kTile;
+    __shared__ PipeBarriers pb;
+    __shared__ float red_ff[kConsumerWarps][4];
+    __shared__ double red_side[kConsumerWarps][2];
+    __shared__ int red_bad[kConsumerWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31;
     const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
     const float* __restrict__ rk = a.r[k];
     const float* __restrict__ g = a.g;
+    pipe_init<kStages>(&pb);
+
+    if ((tid >> 5) == kConsumerWarps) {  // producer warp
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = j; c < a.n_chunks; c += a.J) {
+                const int64_t base = c * kChunk;
+                const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+                for (int o = 0; o < cn; o += kTile, ++it)
+                    pipe_produce<kTile, kStages>(&pb, sg, sr, g, rk, base + o, min(kTile, cn - o), it, a.status);
+            }
+        }
+        return;
+    }
+
     int cur_t = -1;
     float csh = 0.f;
     bool small = false;
     Acc acc;
     acc.reset();
-
+    uint32_t it = 0;
     for (int64_t c = j; c < a.n_chunks; c += a.J) {
         const int64_t base = c * kChunk;
-        const int64_t cend = min(base + kChunk, a.n);
-        for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
-            const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-            if (o0 >= cend) break;
-            const int64_t pa = o0 > base ? o0 : base;
-            const int64_t pb = o1 < cend ? o1 : cend;
-            if (pa >= pb) continue;
-            if (t != cur_t) {
-                if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
-                cur_t = t;
-                csh = __ldg(a.shift + k * a.T + t);
-                small = (o1 - o0) < kSmallTensor;
-                acc.reset();
-            }
-            if (pa == base && pb == base + kChunk && !small) {
-                const float4* g4 = reinterpret_cast<const float4*>(g + base);
-                const float4* r4 = reinterpret_cast<const float4*>(rk + base);
-                float4 gv[kGroups], rv[kGroups];
-#pragma unroll
-                for (int q = 0; q < kGroups; ++q) gv[q] = __ldg(g4 + tid + q * kThreads);
-#pragma unroll
-                for (int q = 0; q < kGroups; ++q) rv[q] = __ldcs(r4 + tid + q * kThreads);
-#pragma unroll
-                for (int q = 0; q < kGroups; ++q) {
-                    const float d0 = __fsub_rn(gv[q].x, rv[q].x), d1 = __fsub_rn(gv[q].y, rv[q].y);
-                    const float d2 = __fsub_rn(gv[q].z, rv[q].z), d3 = __fsub_rn(gv[q].w, rv[q].w);
-                    const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
-                    const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
-                    const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
-                    // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
-                    if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
-                        const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
-                        const float b2 = __fmaf_rn(
-                            y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
-                        ff_add(acc.s1h, acc.s1l, b1);
-                        ff_add(acc.s2h, acc.s2l, b2);
-                    } else {
-                        acc.side = true;
-                        side_add(d0, csh, acc.s1d, acc.s2d, acc.bad);
-                        side_add(d1, csh, acc.s1d, acc.s2d, acc.bad);
-                        side_add(d2, csh, acc.s1d, acc.s2d, acc.bad);
-                        side_add(d3, csh, acc.s1d, acc.s2d, acc.bad);
-                    }
+        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+        int t0 = tensor_containing(a.off, a.T, base);  // first tensor of the chunk
+        for (int o = 0; o < cn; o += kTile, ++it) {
+            const int s = static_cast<int>(it % kStages);
+            const int64_t tb = base + o;
+            const int tn = min(kTile, cn - o);
+            const int tvec = tn & ~3;  // elements staged in shared memory
+            const int64_t tend = tb + tn;
+            wait_or_flag(&pb.full[s], (it / kStages) & 1u, a.status);
+            const float* tg = sg + s * kTile;
+            const float* tr = sr + s * kTile;
+            for (int t = t0; t < a.T; ++t) {
+                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+                if (o0 >= tend) break;
+                const int64_t pa = o0 > tb ? o0 : tb;
+                const int64_t pe = o1 < tend ? o1 : tend;
+                if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
+                if (pa >= pe) continue;
+                if (t != cur_t) {
+                    if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
+                    cur_t = t;
+                    csh = __ldg(a.shift + k * a.T + t);
+                    small = (o1 - o0) < kSmallTensor;
+                    acc.reset();
                 }
-            } else {
-                for (int64_t e = pa + tid; e < pb; e += kThreads) {
-                    const float d = __fsub_rn(__ldg(g + e), __ldcs(rk + e));
-                    const float y = __fsub_rn(d, csh);
-                    const float ay = fabsf(y);
-                    if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
-                        ff_add(acc.s1h, acc.s1l, y);
-                        ff_add(acc.s2h, acc.s2l, __fmul_rn(y, y));
-                    } else {
-                        acc.side = true;
-                        side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
+                if (pa == tb && pe == tb + kTile && !small) {
+#pragma unroll
+                    for (int q = 0; q < kTile / 4 / kThreads; ++q) {
+                        const int v = tid + q * kThreads;
+                        add_group(acc, reinterpret_cast<const float4*>(tg)[v],
+                                  reinterpret_cast<const float4*>(tr)[v], csh);
+                    }
+                } else {
+                    for (int64_t e = pa + tid; e < pe; e += kThreads) {
+                        const int l = static_cast<int>(e - tb);
+                        const float gv = l < tvec ? tg[l] : __ldg(g + e);
+                        const float rv = l < tvec ? tr[l] : __ldg(rk + e);
+                        const float d = __fsub_rn(gv, rv);
+                        const float y = __fsub_rn(d, csh);
+                        const float ay = fabsf(y);
+                        if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
+                            ff_add(acc.s1h, acc.s1l, y);
+                            ff_add(acc.s2h, acc.s2l, __fmul_rn(y, y));
+                        } else {
+                            acc.side = true;
+                            side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
+                        }
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pb.empty[s]);
         }
     }
     if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
@@ -344,8 +387,12 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     a.K = K;
     a.clip = clip_sigmas;
     a.J = 1;
+    const size_t smem = sizeof(float) * 2 * kStages * kTile;
     if (a.n_chunks > 0) {
-        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_stats), kThreads, 0, K, a.n_chunks);
+        if ((st = cuda_status(cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem)))) != DL_OK)
+            return st;
+        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_stats), kPipeThreads, smem, K, a.n_chunks);
         if (a.J > max_blocks_per_learner(K)) a.J = max_blocks_per_learner(K);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -357,7 +404,7 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     k_shift<<<small_grid, kThreads, 0, s>>>(a);
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        k_stats<<<K * a.J, kThreads, 0, s>>>(a);
+        k_stats<<<K * a.J, kPipeThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     k_stats_fin<<<small_grid, kThreads, 0, s>>>(a);
