@@ -10,7 +10,13 @@ Bars (per the outer-step tolerance contract):
     residuals with 2^-22-width steps: half a step per element, plus 2^-24
     widths of residual rounding, then one final rounding), bucket counts exact
     (both only where no boundary exception moved an element);
-  * relative L2 <= 1e-6 on Delta_bar, theta' and momentum'.
+  * relative L2 <= 1e-6 on Delta_bar, theta' and momentum' over the elements
+    whose codes match; at a counted boundary exception the decoded value of
+    that learner moves by one bucket, so there the difference must be exactly
+    what the flipped code explains (sum over learners of w_hat_k times the
+    difference of the two decoded values). Without this split a handful of
+    permitted exceptions in a 500M-element tensor would alone move the
+    relative L2 of Delta_bar by ~1e-6 each.
 """
 from __future__ import annotations
 
@@ -64,7 +70,7 @@ def gpu_outer_step(g, reps, numels, m=None, weights=None, present=None, min_quor
     return out
 
 
-def check_stats(o_st, g_st, K, T):
+def check_stats(o_st, g_st, K, T, tol=TOL_STATS):
     assert np.array_equal(g_st["count"], o_st.count)
     assert np.array_equal(g_st["nonfinite"], o_st.nonfinite)
     for k in range(K):
@@ -77,8 +83,8 @@ def check_stats(o_st, g_st, K, T):
             if s_o == 0.0:
                 assert s_g == 0.0 and m_g == m_o, (k, t, m_o, m_g, s_g)
                 continue
-            assert abs(s_g - s_o) <= TOL_STATS * s_o, (k, t, s_o, s_g)
-            assert abs(m_g - m_o) <= TOL_STATS * s_o + 1e-15 * abs(m_o), (k, t, m_o, m_g, s_o)
+            assert abs(s_g - s_o) <= tol * s_o, (k, t, s_o, s_g)
+            assert abs(m_g - m_o) <= tol * s_o + 1e-15 * abs(m_o), (k, t, m_o, m_g, s_o)
 
 
 def check_codes(o, gp, g, reps, offsets):
@@ -124,6 +130,37 @@ def check_codebook(o, gp, moved):
             assert np.all(np.abs(a - b) <= tol), (k, t, np.max(np.abs(a - b) - tol))
 
 
+def check_merge(gp_vals, o_vals, codes_g, codes_o, cb_g, cb_o, w_hat, t_of=None, tol=TOL_REL_L2):
+    """Relative L2 of (delta_bar, theta_g, momentum) over elements whose codes
+    match, and the explained-difference check at boundary exceptions.
+
+    gp_vals / o_vals: dicts of 1-D arrays; codes_*: [K, n]; cb_*: [K, T, 256];
+    w_hat: [K] fp32 weights of the learners in codes order; t_of: tensor index
+    of every element (None = one tensor)."""
+    n = codes_g.shape[1]
+    t_of = np.zeros(n, dtype=np.int64) if t_of is None else t_of
+    diff = (codes_g != codes_o).any(axis=0)
+    keep = ~diff
+    out = {"exception_elems": int(diff.sum())}
+    for key in ("delta_bar", "theta_g", "momentum"):
+        a, b = gp_vals[key], o_vals[key]
+        r = rel_l2(a[keep], b[keep])
+        out[key] = r
+        assert r <= tol, (key, r)
+    if diff.any():
+        idx = np.nonzero(diff)[0]
+        expl = np.zeros(idx.size)
+        for k in range(codes_g.shape[0]):
+            vg = cb_g[k, t_of[idx], codes_g[k, idx]].astype(np.float64)
+            vo = cb_o[k, t_of[idx], codes_o[k, idx]].astype(np.float64)
+            expl += float(w_hat[k]) * np.abs(vg - vo)
+        for key in ("delta_bar", "momentum"):
+            d = np.abs(gp_vals[key][idx].astype(np.float64) - o_vals[key][idx])
+            scale = np.abs(o_vals[key][idx]).astype(np.float64)
+            assert np.all(d <= expl * (1 + 1e-5) + 4e-7 * scale + 1e-30), key
+    return out
+
+
 def compare(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, lr=0.7, mu=0.9,
             clip_sigmas=6.0, quantized=True, nan_ok=False):
     offsets = np.zeros(len(numels) + 1, dtype=np.int64)
@@ -141,15 +178,24 @@ def compare(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, l
         exc, moved = check_codes(o, gp, g, reps, offsets)
         check_codebook(o, gp, moved)
         report["boundary_exceptions"] = exc
-    for key in ("delta_bar", "theta_g", "momentum"):
-        a, b = gp[key], o[key]
-        if nan_ok:
-            nan = np.isnan(b)
-            assert np.array_equal(np.isnan(a), nan), key
-            a, b = a[~nan], b[~nan]
-        r = rel_l2(a, b)
-        report[key] = r
-        assert r <= TOL_REL_L2, (key, r)
+    if quantized and not nan_ok:
+        K = len(reps)
+        st_w, w_hat = oracle.merge_weights(weights, present, K, min_quorum)
+        pres = np.ones(K, bool) if present is None else np.asarray(present, bool)
+        t_of = np.searchsorted(offsets, np.arange(g.size), side="right") - 1
+        res = check_merge(gp, o, gp["codes"][pres], o["codes"][pres], gp["codebook"][pres],
+                          o["codebook"][pres], w_hat[pres], t_of)
+        report.update(res)
+    else:
+        for key in ("delta_bar", "theta_g", "momentum"):
+            a, b = gp[key], o[key]
+            if nan_ok:
+                nan = np.isnan(b)
+                assert np.array_equal(np.isnan(a), nan), key
+                a, b = a[~nan], b[~nan]
+            r = rel_l2(a, b)
+            report[key] = r
+            assert r <= TOL_REL_L2, (key, r)
     upd_o = (o["theta_g"].astype(np.float64) - g)
     upd_g = (gp["theta_g"].astype(np.float64) - g)
     if nan_ok:

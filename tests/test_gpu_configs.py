@@ -1,0 +1,245 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (one dl_pseudograd_stats / dl_quantize / dl_merge_outer_step sequence per
+fragment), on sampled tensors (needs a GPU; minutes).
+
+Statistics, codebooks and the merge are per tensor, so a sampled tensor can be
+checked against the oracle run on that tensor alone. Sampled tensors come from
+the seeded host generator (identical bits on both sides); the rest of each
+fragment is filled on the device with the same distributions from torch's
+generator, which only the GPU sees. Multi-step workloads rebuild the learner
+replicas from each side's own synced parameters (theta_k = theta_g - Delta,
+Delta drawn per step), so after the first step the two chains differ by
+rounding: later steps are checked on theta / momentum within the tolerance and
+on codes with the boundary band widened accordingly.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from parity import TOL_REL_L2, check_codebook, check_codes, check_merge, check_stats, rel_l2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import pseudo_grad_sync_gb300 as dl
+    dl.lib()
+
+
+def _delta_host(wl, t, k, step):
+    """Delta of learner k, tensor t, outer step `step` (fp32, host generator)."""
+    z = np.zeros(wl.numels[t], dtype=np.float32)
+    return -synthetic.replica_f32(synthetic.key(wl.seed, 2, step, t, k), 0, z, wl.tensor_scale(t),
+                                  wl.delta_dist)
+
+
+def _delta_device(wl, t, m, gen):
+    x = torch.randn(m, device="cuda", generator=gen)
+    if wl.delta_dist == 1:  # Student-t(3)
+        c = torch.randn(3, m, device="cuda", generator=gen).square_().sum(0).div_(3.0)
+        x.div_(c.sqrt_())
+    return x.mul_(wl.tensor_scale(t))
+
+
+class FragmentRun:
+    """Device state of one fragment and host copies of its sampled tensors."""
+
+    def __init__(self, wl, tensors, sampled, K=None, gen_seed=0):
+        import pseudo_grad_sync_gb300 as dl
+
+        self.dl, self.wl, self.tensors = dl, wl, tensors
+        self.K = wl.K if K is None else K
+        self.numels = [wl.numels[t] for t in tensors]
+        self.off = synthetic.offsets_of(self.numels)
+        self.n = int(self.off[-1])
+        self.frag = dl.Fragment(self.numels)
+        self.gen = torch.Generator(device="cuda")
+        self.gen.manual_seed(gen_seed)
+        self.g = torch.empty(self.n, device="cuda")
+        self.m = torch.zeros(self.n, device="cuda")
+        self.host = {}  # t -> dict(a, b, g, m) oracle chain of a sampled tensor
+        for i, t in enumerate(tensors):
+            a, b = int(self.off[i]), int(self.off[i + 1])
+            if t in sampled:
+                gh = wl.theta_global(t)
+                self.g[a:b].copy_(torch.from_numpy(gh))
+                self.host[t] = {"i": i, "a": a, "b": b, "g": gh, "m": np.zeros_like(gh)}
+            else:
+                self.g[a:b].normal_(0.0, wl.theta_std, generator=self.gen)
+        self.sync = dl.OuterSync(self.frag, self.K)
+
+    def replicas(self, step):
+        reps = []
+        for k in range(self.K):
+            r = torch.empty(self.n, device="cuda")
+            for i, t in enumerate(self.tensors):
+                a, b = int(self.off[i]), int(self.off[i + 1])
+                if t in self.host:
+                    d = torch.from_numpy(_delta_host(self.wl, t, k, step)).cuda()
+                else:
+                    d = _delta_device(self.wl, t, b - a, self.gen)
+                torch.sub(self.g[a:b], d, out=r[a:b])
+            reps.append(r)
+        return reps
+
+    def step(self, step, present=None, weights=None):
+        reps = self.replicas(step)
+        db = torch.empty_like(self.g)
+        counts = torch.empty((self.K, self.frag.T, 256), dtype=torch.int32, device="cuda")
+        idx = self.sync.step(self.g, self.m, reps, weights=weights, present=present, delta_bar=db,
+                             counts=counts)
+        torch.cuda.synchronize()
+        del reps
+        return idx, db, counts
+
+    def check(self, step, idx, db, counts, present=None, weights=None, band=1e-6):
+        """Oracle on every sampled tensor; returns the number of boundary exceptions."""
+        dl = self.dl
+        st_all = dl.stats_to_host(self.sync.stats[:len(idx)])
+        cb_all = self.sync.codebook[:len(idx)].cpu().numpy()
+        cnt_all = counts[:len(idx)].cpu().numpy().view(np.uint32)
+        exc = 0
+        for t, h in self.host.items():
+            i, a, b = h["i"], h["a"], h["b"]
+            # the oracle learners are the present ones, in order, with their weights
+            d = [_delta_host(self.wl, t, k, step) for k in idx]
+            reps = [(h["g"] - dk).astype(np.float32) for dk in d]
+            w = None if weights is None else np.asarray(weights, np.float32)[idx]
+            o = oracle.outer_step(h["g"], h["m"], reps, weights=w)
+            assert o["status"] == 0
+            gp = {
+                "stats": {key: v[:, i:i + 1] for key, v in st_all.items()},
+                "codes": np.stack([self.sync.codes[s][a:b].cpu().numpy() for s in range(len(idx))]),
+                "codebook": cb_all[:, i:i + 1], "counts": cnt_all[:, i:i + 1],
+            }
+            # stats with the sampled tensor as a one-tensor fragment
+            o1 = {"stats": o["stats"], "codes": o["codes"], "codebook": o["codebook"],
+                  "counts": o["counts"]}
+            # later steps: each chain's theta differs by ~1 ulp, so do its Delta
+            check_stats(o["stats"], gp["stats"], len(idx), 1, tol=5e-9 if band <= 1e-6 else 1e-7)
+            if band <= 1e-6:
+                n_exc, moved = check_codes(o1, gp, h["g"], reps, np.array([0, b - a]))
+                check_codebook(o1, gp, moved)
+            else:  # later steps: inputs differ by rounding between the chains
+                mism = (gp["codes"] != o["codes"]).sum()
+                n_exc = int(mism)
+                assert mism <= max(4, 1e-4 * gp["codes"].size), mism
+            exc += n_exc
+            w_hat = oracle.merge_weights(w, None, len(idx))[1]
+            gvals = {key: dev[a:b].cpu().numpy() for key, dev in
+                     (("delta_bar", db), ("theta_g", self.g), ("momentum", self.m))}
+            res = check_merge(gvals, o, gp["codes"], o["codes"], gp["codebook"], o["codebook"], w_hat)
+            print(f"step {step} tensor {t} n={b - a} K={len(idx)} {res}")
+            # the oracle chain carries on from its own outputs
+            h["g"], h["m"] = o["theta_g"], o["momentum"]
+        return exc
+
+
+def _plan(wl):
+    frag_of, load = oracle.plan_fragments(wl.numels, wl.n_frags)
+    return [[t for t in range(wl.n_tensors) if frag_of[t] == f] for f in range(wl.n_frags)], load
+
+
+def _smallest(wl, ts, kind="any"):
+    cand = [t for t in ts if kind == "any" or wl.numels[t] > 65536]
+    return min(cand, key=lambda t: wl.numels[t]) if cand else None
+
+
+def test_decoder_1b_every_fragment():
+    """1.1B set, K=4, P=24: every fragment synced; two tensors per fragment
+    checked against the oracle (its smallest and its smallest matrix)."""
+    wl = synthetic.decoder_1b()
+    frags, load = _plan(wl)
+    assert load.max() == 65536000 and load.sum() == wl.n_elems
+    total_exc = 0
+    for f, ts in enumerate(frags):
+        sampled = {_smallest(wl, ts), _smallest(wl, ts, "matrix")} - {None}
+        run = FragmentRun(wl, ts, sampled, gen_seed=f)
+        idx, db, counts = run.step(0)
+        assert torch.isfinite(run.g).all() and torch.isfinite(run.m).all()
+        total_exc += run.check(0, idx, db, counts)
+        del run
+        torch.cuda.empty_cache()
+    print("decoder_1b boundary exceptions:", total_exc)
+
+
+def test_decoder_10b_fragment_three_steps():
+    """10B set, K=14: the median (~415M-element) fragment over 3 outer steps
+    with momentum carried."""
+    wl = synthetic.decoder_10b()
+    frags, load = _plan(wl)
+    f = int(np.argsort(load)[len(load) // 2])
+    ts = frags[f]
+    sampled = {_smallest(wl, ts), _smallest(wl, ts, "matrix")} - {None}
+    run = FragmentRun(wl, ts, sampled, gen_seed=3)
+    assert 4e8 < run.n < 4.3e8
+    for step in range(wl.steps):
+        idx, db, counts = run.step(step)
+        run.check(step, idx, db, counts, band=1e-6 if step == 0 else 1e-4)
+    assert torch.isfinite(run.g).all()
+
+
+def test_ragged_heavy_single_batch():
+    """2000 ragged tensors (64..16Mi, every 10th a 4096 norm), K=8, Student-t(3)
+    pseudo-gradients, all in one launch per kernel."""
+    wl = synthetic.ragged_heavy()
+    ts = list(range(wl.n_tensors))
+    sizes = np.array(wl.numels)
+    order = np.argsort(sizes)
+    sampled = {int(order[0]), 9, int(order[len(order) // 2]), int(order[-200]), int(order[-1])}
+    run = FragmentRun(wl, ts, sampled, gen_seed=4)
+    idx, db, counts = run.step(0)
+    exc = run.check(0, idx, db, counts)
+    st = run.dl.stats_to_host(run.sync.stats)
+    assert (st["nonfinite"] == 0).all() and (st["count"] == sizes[None, :]).all()
+    # heavy tails: Student-t(3) puts ~1.9e-3 of the mass beyond 6 sigma
+    cnt = counts.cpu().numpy().view(np.uint32).astype(np.int64)
+    clipped = (cnt[:, :, 0] + cnt[:, :, 255]).sum() / (wl.K * wl.n_elems)
+    assert 5e-4 < clipped < 5e-3, clipped
+    print("ragged boundary exceptions:", exc, "edge-bucket fraction:", clipped)
+
+
+def test_quorum_10b_fragments_and_steps():
+    """10B shapes, K=16, random present subsets of size 1..16 and weights
+    U[0.5, 1.5] per (fragment, step), 4 outer steps with per-fragment momentum;
+    three multi-tensor fragments checked against the oracle at every step."""
+    wl = synthetic.quorum_10b()
+    frags, load = _plan(wl)
+    mixed = [f for f, ts in enumerate(frags) if len(ts) > 1]  # not the embedding / lm_head alone
+    for f in (mixed[0], mixed[len(mixed) // 2], mixed[-1]):
+        ts = frags[f]
+        sampled = {_smallest(wl, ts), _smallest(wl, ts, "matrix")} - {None}
+        run = FragmentRun(wl, ts, sampled, gen_seed=5 + f)
+        for step in range(wl.steps):
+            present = wl.present(f, step)
+            weights = wl.weights(f, step)
+            idx, db, counts = run.step(step, present=present, weights=weights)
+            assert idx == [k for k in range(wl.K) if present[k]]
+            run.check(step, idx, db, counts, present=present, weights=weights,
+                      band=1e-6 if step == 0 else 1e-4)
+        assert torch.isfinite(run.g).all()
+        del run
+        torch.cuda.empty_cache()
+
+
+def test_quorum_10b_embedding_fragment():
+    """The 525M-element embedding, a fragment of its own, first outer step:
+    the largest single tensor of the workloads (boundary exceptions appear
+    here and must be fully explained by their flipped codes)."""
+    wl = synthetic.quorum_10b()
+    frags, load = _plan(wl)
+    f = int(np.argmax(load))
+    ts = frags[f]
+    assert len(ts) == 1 and wl.numels[ts[0]] == 525336576
+    run = FragmentRun(wl, ts, {ts[0]}, gen_seed=7)
+    present, weights = wl.present(f, 0), wl.weights(f, 0)
+    idx, db, counts = run.step(0, present=present, weights=weights)
+    run.check(0, idx, db, counts, present=present, weights=weights)
