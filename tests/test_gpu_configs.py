@@ -10,7 +10,10 @@ generator, which only the GPU sees. Multi-step workloads rebuild the learner
 replicas from each side's own synced parameters (theta_k = theta_g - Delta,
 Delta drawn per step), so after the first step the two chains differ by
 rounding: later steps are checked on theta / momentum within the tolerance and
-on codes with the boundary band widened accordingly.
+on codes with the boundary band widened accordingly. An element moved by a
+counted boundary exception keeps that difference in its momentum and
+parameters; at later steps it is checked against the propagated difference
+instead of the relative-L2 bar.
 """
 import math
 
@@ -136,7 +139,12 @@ class FragmentRun:
             w_hat = oracle.merge_weights(w, None, len(idx))[1]
             gvals = {key: dev[a:b].cpu().numpy() for key, dev in
                      (("delta_bar", db), ("theta_g", self.g), ("momentum", self.m))}
-            res = check_merge(gvals, o, gp["codes"], o["codes"], gp["codebook"], o["codebook"], w_hat)
+            taint = h.setdefault("taint", np.zeros(b - a, dtype=bool))
+            res, diff, expl = check_merge(gvals, o, gp["codes"], o["codes"], gp["codebook"],
+                                          o["codebook"], w_hat, exclude=taint,
+                                          carried=h.get("carried", 0.0))
+            h["taint"] = taint | diff
+            h["carried"] = max(h.get("carried", 0.0), expl)
             print(f"step {step} tensor {t} n={b - a} K={len(idx)} {res}")
             # the oracle chain carries on from its own outputs
             h["g"], h["m"] = o["theta_g"], o["momentum"]
