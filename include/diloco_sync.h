@@ -9,6 +9,9 @@
  *   dl_quantize            (device)      uint8 codes + bucket-mean codebooks
  *   dl_merge_outer_step    (device)      decode, weighted fp32 mean, Nesterov
  *
+ * dl_outer_sync runs that sequence over every fragment of a model in one
+ * call, overlapping consecutive fragments on two streams.
+ *
  * Sources: the INTELLECT-1 paper notes ("INTELLECT-1: Training a 10B Model
  * Across 3 Continents", sections 3.2, 4.1 and 4.2) define the pseudo-gradient,
  * the 6-sigma / 256-bucket quantiser with a bucket-mean codebook, the fp32
@@ -34,7 +37,8 @@
  *    enqueued. Host-side validation happens before anything is enqueued, so
  *    an error return means nothing was launched (DL_ERR_CUDA excepted).
  *  - No call allocates device memory; scratch comes from the caller's
- *    workspace, sized by the matching *_workspace_bytes query.
+ *    workspace, sized by the matching *_workspace_bytes query. (dl_outer_sync
+ *    creates one stream and a few events per device on first use.)
  *  - n = 0 is a valid no-op. Outputs must not alias inputs, except that
  *    theta_g and momentum are updated in place by the merge.
  *  - No C++ exception crosses the ABI. Calls are thread-safe as long as
@@ -104,7 +108,9 @@ const char* dl_status_string(int status);
 int dl_plan_fragments(const int64_t* numel, int32_t n_tensors, int32_t n_frags,
                       int32_t* frag_of_tensor, int64_t* frag_load);
 
-/* Workspace bytes needed by dl_pseudograd_stats for this fragment and K. */
+/* Workspace bytes needed by dl_pseudograd_stats for this fragment and K.
+ * Never decreases with K, so a workspace sized for K serves any K' <= K
+ * (a subset of present learners); the same holds for dl_quantize. */
 size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K);
 
 /*
@@ -174,6 +180,61 @@ int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* c
                         const dl_fragment* frag, const float* weights, const uint8_t* present,
                         int32_t min_quorum, float lr, float mu, float* delta_bar_out,
                         void* stream);
+
+/* One fragment's share of a whole-model outer step (see dl_outer_sync). */
+typedef struct dl_fragment_job {
+    const dl_fragment* frag;      /* tensor layout of the fragment */
+    float* theta_g;               /* device [n] fp32, in/out */
+    float* momentum;              /* device [n] fp32, in/out */
+    const float* const* theta_k;  /* host [K] of device [n] fp32 learner replicas */
+    const float* weights;         /* host [K] fp32 >= 0, or NULL for all 1 */
+    const uint8_t* present;       /* host [K] 0/1, or NULL for all present */
+    float* delta_bar_out;         /* device [n] fp32, out (merged D); may be NULL */
+} dl_fragment_job;
+
+#define DL_SYNC_UNQUANTIZED 1 /* merge the fp32 Delta_k directly (no stats, no codes) */
+#define DL_SYNC_SERIAL 2      /* run every kernel on `stream`, one fragment after another */
+
+/* Workspace bytes needed by dl_outer_sync for these jobs and K (0 on a bad
+ * argument). Only the jobs' fragments are read. Covers every number of
+ * present learners from 1 to K, so one workspace serves any quorum. */
+size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K);
+
+/*
+ * A whole outer step over the fragments of a model (Decoupled DiLoCo note,
+ * architecture items 3-4: fragments synchronised one after another while
+ * other work goes on; INTELLECT-1 notes, sections 3.2 and 4.1-4.2 for each
+ * fragment's arithmetic). For each job in order it does exactly what
+ *   dl_pseudograd_stats -> dl_quantize -> dl_merge_outer_step
+ * do over that job's present learners (ascending; absent learners are never
+ * read), with codes, codebooks and statistics kept in the workspace, so the
+ * results are bitwise those of the three calls.
+ *
+ * Scheduling: the statistics of fragment j+1 run on a library-owned side
+ * stream beside the quantisation and merge of fragment j on `stream`
+ * (two statistics buffers). The side stream forks from `stream` at entry and
+ * joins it before return, so all effects are ordered on `stream`. The side
+ * stream and its events are created on the current device on first use and
+ * live until the process exits; enqueueing is serialised per device by a
+ * mutex. `stream` must belong to the current device. DL_SYNC_SERIAL keeps
+ * everything on `stream` and creates nothing.
+ *   jobs, n_jobs  host array of fragment jobs; fragments must not overlap
+ *                 each other's buffers
+ *   K             learners per job (1..DL_MAX_LEARNERS)
+ *   clip_sigmas   > 0 (6 in the pages); ignored with DL_SYNC_UNQUANTIZED
+ *   min_quorum    applied to every job; a job below it fails the whole call
+ *   lr, mu        outer Nesterov learning rate and momentum (0.7, 0.9)
+ *   flags         0 or a combination of DL_SYNC_UNQUANTIZED, DL_SYNC_SERIAL
+ *   d_workspace   device scratch of dl_outer_sync_workspace_bytes bytes
+ *                 (unused with DL_SYNC_UNQUANTIZED). Its first word is the
+ *                 device status word read by dl_read_device_status.
+ * Every job is validated before anything is enqueued (quorum, weights,
+ * pointers, alignment); a CUDA failure part way returns DL_ERR_CUDA with the
+ * earlier fragments enqueued.
+ */
+int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, double clip_sigmas,
+                  int32_t min_quorum, float lr, float mu, int32_t flags, void* d_workspace,
+                  size_t workspace_bytes, void* stream);
 
 /*
  * dl_quantize without a caller-provided workspace. The pages have no

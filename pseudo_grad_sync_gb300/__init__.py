@@ -8,9 +8,12 @@ C entry points (see include/diloco_sync.h) keep their names here:
     pseudograd_stats     per-(learner, tensor) mu / sigma / clip range
     quantize             uint8 codes + bucket-mean codebooks
     merge_outer_step     decode, weighted fp32 mean, outer Nesterov (in place)
+    outer_sync           the three calls over every fragment of a model, with
+                         consecutive fragments overlapped on two streams
 
 ``OuterSync`` bundles the three device calls of one fragment with their
-workspaces.
+workspaces; ``ModelSync`` holds the workspace of ``outer_sync`` for a fixed
+list of fragments.
 """
 from __future__ import annotations
 
@@ -25,6 +28,8 @@ from . import _build
 DL_OK = 0
 DL_NBUCKETS = 256
 DL_MAX_LEARNERS = 32
+DL_SYNC_UNQUANTIZED = 1
+DL_SYNC_SERIAL = 2
 STATS_FIELDS = ("count", "nonfinite", "mean", "std", "lo", "hi")
 
 _lib = None
@@ -33,6 +38,13 @@ _lib = None
 class _Fragment(ctypes.Structure):
     _fields_ = [("offsets", ctypes.c_void_p), ("d_offsets", ctypes.c_void_p),
                 ("n_tensors", ctypes.c_int32)]
+
+
+class _FragmentJob(ctypes.Structure):
+    _fields_ = [("frag", ctypes.POINTER(_Fragment)), ("theta_g", ctypes.c_void_p),
+                ("momentum", ctypes.c_void_p), ("theta_k", ctypes.c_void_p),
+                ("weights", ctypes.c_void_p), ("present", ctypes.c_void_p),
+                ("delta_bar_out", ctypes.c_void_p)]
 
 
 def lib():
@@ -62,6 +74,11 @@ def lib():
         L.dl_merge_outer_step.restype = ctypes.c_int
         L.dl_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, fr, vp, vp, i32, f32, f32, vp,
                                           vp]
+        jb = ctypes.POINTER(_FragmentJob)
+        L.dl_outer_sync_workspace_bytes.restype = sz
+        L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32]
+        L.dl_outer_sync.restype = ctypes.c_int
+        L.dl_outer_sync.argtypes = [jb, i32, i32, f64, i32, f32, f32, i32, vp, sz, vp]
         L.dl_read_device_status.restype = ctypes.c_int
         L.dl_read_device_status.argtypes = [vp, vp, vp]
         _lib = L
@@ -193,6 +210,58 @@ def merge_outer_step(theta_g, momentum, frag: Fragment, codes=None, codebook=Non
         int(min_quorum), float(lr), float(mu), _ptr(delta_bar), _stream(stream)))
 
 
+def _jobs(frags, theta_g=None, momentum=None, replicas=None, weights=None, present=None,
+          delta_bar=None):
+    """ctypes array of dl_fragment_job plus the host arrays it points into
+    (returned together so that they stay alive for the call)."""
+    P = len(frags)
+    arr = (_FragmentJob * max(P, 1))()
+    keep = []
+    for j, F in enumerate(frags):
+        job = arr[j]
+        job.frag = ctypes.pointer(F._c)
+        if theta_g is not None:
+            job.theta_g = theta_g[j].data_ptr()
+            job.momentum = momentum[j].data_ptr()
+        if replicas is not None:
+            ra = _ptr_array(replicas[j])
+            keep.append(ra)
+            job.theta_k = ctypes.cast(ra, ctypes.c_void_p)
+        if weights is not None and weights[j] is not None:
+            w = np.ascontiguousarray(weights[j], dtype=np.float32)
+            keep.append(w)
+            job.weights = w.ctypes.data
+        if present is not None and present[j] is not None:
+            pr = np.ascontiguousarray(present[j], dtype=np.uint8)
+            keep.append(pr)
+            job.present = pr.ctypes.data
+        if delta_bar is not None and delta_bar[j] is not None:
+            job.delta_bar_out = delta_bar[j].data_ptr()
+    return arr, keep
+
+
+def outer_sync_workspace_bytes(frags, K: int) -> int:
+    arr, _ = _jobs(frags)
+    return int(lib().dl_outer_sync_workspace_bytes(arr, len(frags), K))
+
+
+def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=None, present=None,
+               min_quorum=1, clip_sigmas=6.0, lr=0.7, mu=0.9, flags=0, delta_bar=None,
+               stream=None):
+    """One outer step over every fragment (dl_outer_sync). Per-fragment lists:
+    theta_g[j], momentum[j], replicas[j] (K tensors), and optionally
+    weights[j] / present[j] (length-K host arrays) and delta_bar[j]."""
+    arr, keep = _jobs(frags, theta_g, momentum, replicas, weights, present, delta_bar)
+    if workspace is None and not flags & DL_SYNC_UNQUANTIZED:
+        workspace = new_workspace(outer_sync_workspace_bytes(frags, K), theta_g[0].device)
+    nbytes = 0 if workspace is None else workspace.numel()
+    _check("dl_outer_sync", lib().dl_outer_sync(
+        arr, len(frags), K, float(clip_sigmas), int(min_quorum), float(lr), float(mu), int(flags),
+        _ptr(workspace), nbytes, _stream(stream)))
+    del keep
+    return workspace
+
+
 def read_device_status(workspace, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check("dl_read_device_status",
@@ -234,3 +303,17 @@ class OuterSync:
                          weights=w, min_quorum=min_quorum, lr=self.lr, mu=self.mu,
                          delta_bar=delta_bar, stream=stream)
         return idx
+
+
+class ModelSync:
+    """Whole-model outer step (dl_outer_sync) over a fixed list of fragments,
+    with its workspace allocated once."""
+
+    def __init__(self, frags, K: int, device="cuda", clip_sigmas=6.0, lr=0.7, mu=0.9):
+        self.frags, self.K, self.clip, self.lr, self.mu = list(frags), K, clip_sigmas, lr, mu
+        self.workspace = new_workspace(outer_sync_workspace_bytes(self.frags, K), device)
+
+    def step(self, theta_g, momentum, replicas, weights=None, present=None, min_quorum=1,
+             delta_bar=None, flags=0, stream=None):
+        outer_sync(self.frags, theta_g, momentum, replicas, self.K, self.workspace, weights,
+                   present, min_quorum, self.clip, self.lr, self.mu, flags, delta_bar, stream)

@@ -343,8 +343,10 @@ using namespace dl;
 extern "C" size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
+    // partials for K * T * J blocks, J <= kMaxBlocksTotal / K: sized as
+    // T * kMaxBlocksTotal so that the need never decreases with K
     return kWsHeader + shift_bytes(K, f.T) +
-           align256(sizeof(Partial) * static_cast<size_t>(K) * f.T * max_blocks_per_learner(K));
+           align256(sizeof(Partial) * static_cast<size_t>(f.T) * kMaxBlocksTotal);
 }
 
 extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* theta_k, int32_t K,

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(L):
             "dl_merge_outer_step"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
-    assert L.dl_version() == 100
+    assert L.dl_version() == 101
 
 
 def test_status_strings(L):
@@ -129,3 +129,102 @@ def test_merge_quorum_and_weight_rules_match_oracle(L):
         assert st_dl == expect, (w, p, q, st_or, st_dl)
     assert _merge(L, fb, 33) == -1
     assert _merge(L, fb, 0) == -1
+
+
+def _sync_jobs(frags, K, weights=None, present=None, theta_k=True):
+    """dl_fragment_job array with fake device pointers (never dereferenced)."""
+    arr = (dl._FragmentJob * len(frags))()
+    keep = []
+    for j, f in enumerate(frags):
+        arr[j].frag = ctypes.pointer(f)
+        arr[j].theta_g = FAKE
+        arr[j].momentum = FAKE
+        if theta_k:
+            ra = _ptrs(*([FAKE] * K))
+            keep.append(ra)
+            arr[j].theta_k = ctypes.cast(ra, ctypes.c_void_p)
+        if weights is not None and weights[j] is not None:
+            w = np.ascontiguousarray(weights[j], np.float32)
+            keep.append(w)
+            arr[j].weights = w.ctypes.data
+        if present is not None and present[j] is not None:
+            p = np.ascontiguousarray(present[j], np.uint8)
+            keep.append(p)
+            arr[j].present = p.ctypes.data
+    return arr, keep
+
+
+def _outer_sync(L, arr, n, K, min_quorum=1, flags=0, ws=FAKE, nbytes=0):
+    return L.dl_outer_sync(arr, n, K, 6.0, min_quorum, 0.7, 0.9, flags, ws, nbytes, None)
+
+
+def test_outer_sync_validates_every_job_before_any_launch(L):
+    fs = [_frag([0, 10, 30]), _frag([0, 5]), _frag([0, 0, 0])]
+    frags = [f for f, _ in fs]
+    K = 3
+    arr, keep = _sync_jobs(frags, K)
+    need = L.dl_outer_sync_workspace_bytes(arr, 3, K)
+    assert need > 0
+    # quantised mode: every job valid, so the short workspace is what fails
+    assert _outer_sync(L, arr, 3, K, nbytes=need - 1) == -6
+    assert _outer_sync(L, arr, 3, K, ws=FAKE + 16, nbytes=need) == -2
+    assert _outer_sync(L, arr, 3, K, flags=4) == -1
+    assert _outer_sync(L, arr, 3, 0) == -1 and _outer_sync(L, arr, 3, 33) == -1
+    assert L.dl_outer_sync(arr, 3, K, 0.0, 1, 0.7, 0.9, 0, FAKE, need, None) == -1
+    assert _outer_sync(L, arr, 3, K, min_quorum=4) == -3
+    # a later job's bad layout, missing replica array or misaligned buffer
+    bad, _ = _frag([0, 10, 5])
+    arr2, keep2 = _sync_jobs(frags[:2] + [bad], K)
+    assert _outer_sync(L, arr2, 3, K) == -5
+    arr3, keep3 = _sync_jobs(frags, K, theta_k=False)
+    assert _outer_sync(L, arr3, 3, K) == -1
+    arr[1].momentum = FAKE + 4
+    assert _outer_sync(L, arr, 3, K, nbytes=need) == -2
+    assert L.dl_outer_sync_workspace_bytes(arr, 3, 0) == 0
+
+
+def test_outer_sync_quorum_and_weights_per_job_match_oracle(L):
+    """Each job's present set and weights are checked like the merge's; the
+    first failing job (in order) decides the status. All-valid calls stop at
+    the (deliberately) short workspace, so nothing is launched."""
+    rng = np.random.default_rng(11)
+    f, _o = _frag([0, 40, 100])
+    for _ in range(150):
+        K = int(rng.integers(1, 9))
+        P = int(rng.integers(1, 5))
+        q = int(rng.integers(0, 4))
+        ws, ps, expect = [], [], 0
+        for _j in range(P):
+            w = rng.choice([0.0, 0.5, 1.0, 2.0, -1.0, np.inf], K, p=[.2, .3, .2, .2, .05, .05])
+            p = (rng.random(K) < 0.7).astype(np.uint8)
+            ws.append(w)
+            ps.append(p)
+            st_or, _ = oracle.merge_weights(w.astype(np.float32), p, K, q)
+            if expect == 0 and st_or < 0:
+                expect = st_or
+        arr, keep = _sync_jobs([f] * P, K, ws, ps)
+        st = _outer_sync(L, arr, P, K, min_quorum=q, nbytes=0)
+        assert st == (expect if expect < 0 else -6), (st, expect)
+
+
+def test_outer_sync_workspace_covers_every_quorum(L):
+    f, _o = _frag(np.cumsum([0, 4096, 77, 8192 * 9 + 3]))
+    for K in (1, 3, 4, 7, 16, 32):
+        arr, keep = _sync_jobs([f, f], K)
+        need = L.dl_outer_sync_workspace_bytes(arr, 2, K)
+        fb = ctypes.byref(f)
+        for np_ in range(1, K + 1):
+            parts = (L.dl_stats_workspace_bytes(fb, np_) + 2 * 48 * K * 3
+                     + L.dl_quantize_workspace_bytes(fb, np_) + 4 * K * 3 * 256 + K * (8192 * 9 + 4174))
+            assert need >= parts, (K, np_)
+
+
+def test_workspace_needs_never_decrease_with_K(L):
+    """A workspace sized for K must serve any subset of present learners."""
+    for offs in ([0, 10, 30], list(np.cumsum([0, 4096, 77, 8192 * 9 + 3])), [0] + [1] * 50):
+        f, _o = _frag(np.asarray(offs))
+        fb = ctypes.byref(f)
+        s = [L.dl_stats_workspace_bytes(fb, k) for k in range(1, 33)]
+        q = [L.dl_quantize_workspace_bytes(fb, k) for k in range(1, 33)]
+        assert all(a <= b for a, b in zip(s, s[1:])), s
+        assert all(a <= b for a, b in zip(q, q[1:])), q
