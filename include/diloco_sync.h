@@ -38,7 +38,10 @@
  *    an error return means nothing was launched (DL_ERR_CUDA excepted).
  *  - No call allocates device memory; scratch comes from the caller's
  *    workspace, sized by the matching *_workspace_bytes query. (dl_outer_sync
- *    creates one stream and a few events per device on first use.)
+ *    creates one stream and a few events per device on first use.) The first
+ *    4 bytes of a workspace are its device status word: zero them once when
+ *    the workspace is allocated; calls only ever set bits in it, and
+ *    dl_read_device_status clears it.
  *  - n = 0 is a valid no-op. Outputs must not alias inputs, except that
  *    theta_g and momentum are updated in place by the merge.
  *  - No C++ exception crosses the ABI. Calls are thread-safe as long as

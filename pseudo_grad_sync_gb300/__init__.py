@@ -149,8 +149,10 @@ def quantize_workspace_bytes(frag: Fragment, K: int) -> int:
 
 
 def new_workspace(nbytes: int, device="cuda"):
-    # torch's caching allocator returns 512-byte aligned blocks
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """A zeroed workspace (its first word is the device status word, which
+    must start at 0). torch's caching allocator returns 512-byte aligned
+    blocks."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def new_stats(K: int, T: int, device="cuda"):

@@ -235,23 +235,28 @@ struct SegQuant {
     float lo_f, w_f, s_f, guard;
     float c_f;        // fl32(-lo_f * s_f): u is evaluated as fmaf(d, s_f, c_f)
     float scale;      // 2^ks as fp32 (fast kind only)
+    float qoff;       // 2^23 + kResBias as fp32 (fast kind only)
     int ks;           // residual fixed-point exponent
     double ref0, refw; // slow kind: residual reference ref0 + b * refw (fp64)
 };
 
 constexpr int kSegFast = 0, kSegSlow = 1, kSegDegenerate = 2, kSegInvalid = 3;
-// residual fixed point: q = rint(r * 2^ks) with w * 2^ks in [2^22, 2^23),
-// biased by 2^14 so that the small negative residuals of elements at a bucket
-// edge stay positive; the biased value is below 2^24
-constexpr int kResBits = 22;
-constexpr int64_t kResBias = int64_t(1) << 14;
+// Residual fixed point: q = rint(r * 2^ks) + 2^19 with w * 2^ks in
+// [2^21, 2^22). For the fast kind the reference edge e_b = fmaf(b, w_f, lo_f)
+// misses the exact edge lo + b w by at most 2^-23 (|lo| + 256 w) + 2^-16 w,
+// which the fast-kind condition (|lo| / w < 2^19) keeps below w / 16 (up to
+// 2^-15 w): r lies in (-w/16, 17 w / 16), so q lies in (2^18, 2^23) and the
+// fp32 sum fmaf(r, 2^ks, 2^23 + 2^19) falls in [2^23, 2^24), where fp32 holds
+// every integer - its low 23 bits are q, rounded once to nearest even.
+constexpr int kResBits = 21;
+constexpr int64_t kResBias = int64_t(1) << 19;
 
 __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long nonfinite) {
     SegQuant q;
     q.lo = lo;
     q.hi = hi;
     q.s = 0.0;
-    q.lo_f = q.w_f = q.s_f = q.guard = q.scale = q.c_f = 0.f;
+    q.lo_f = q.w_f = q.s_f = q.guard = q.scale = q.qoff = q.c_f = 0.f;
     q.ks = 0;
     q.ref0 = q.refw = 0.0;
     if (nonfinite > 0) {
@@ -275,12 +280,13 @@ __device__ __forceinline__ SegQuant seg_quant(double lo, double hi, long long no
     q.guard = static_cast<float>(g);
     int e_w;
     frexp(static_cast<double>(q.w_f), &e_w);  // w_f = f * 2^e_w, f in [0.5, 1)
-    q.ks = kResBits + 1 - e_w;                  // w_f * 2^ks in [2^22, 2^23)
+    q.ks = kResBits + 1 - e_w;                  // w_f * 2^ks in [2^21, 2^22)
     const bool fast = isfinite(q.lo_f) && isfinite(q.s_f) && q.w_f > 0.f && g < 0.25 &&
                       q.ks >= -126 && q.ks <= 127 && fabs(hi) < 1e37 && fabs(lo) < 1e37;
     if (fast) {
         q.kind = kSegFast;
         q.scale = ldexpf(1.0f, q.ks);
+        q.qoff = static_cast<float>((int64_t(1) << 23) + kResBias);
     } else {
         q.kind = kSegSlow;
         q.ref0 = lo;

@@ -14,10 +14,15 @@
 //                * codebook sum: the residual r = clamp(Delta) - e_b, e_b the
 //                  fp32 bucket edge fmaf(b, w_f, lo_f), is exact or within
 //                  2^-24 bucket widths; it becomes a biased fixed-point
-//                  integer q (2^22 steps per bucket width, below 2^24) that is
-//                  added with two 32-bit shared-memory atomics: word A gets
-//                  (1 << 18) + (q >> 19) (count in bits 18..31), word B gets
-//                  q & (2^19 - 1). Both stay exact for up to 8192 elements;
+//                  integer q (2^21 to 2^22 steps per bucket width, below
+//                  2^23) that is added with two 32-bit shared-memory atomics:
+//                  word A gets (1 << 18) + (q >> 19) (count in bits 18..31),
+//                  word B gets q & (2^19 - 1). Both stay exact for up to 8192
+//                  elements;
+//                * no float-to-integer conversions on this path: floor(u) is
+//                  read from the bits of u + 1.5 * 2^23 added rounding down,
+//                  and q from the bits of fmaf(r, 2^ks, 2^23 + bias), both
+//                  full-rate fp32 operations;
 //                * the code byte is written with 32-bit stores (4 per store).
 //              After each piece (chunk x tensor; one block barrier) thread b
 //              folds bin b of the histogram into 64-bit per-bin sums it owns
@@ -60,7 +65,9 @@ struct QuantArgs {
 
 constexpr uint32_t kLoMask = (1u << 19) - 1;
 constexpr uint32_t kCountOne = 1u << 18;
-constexpr uint32_t kQMax = (1u << 24) - 1;
+constexpr uint32_t kQMax = (1u << 23) - 1;
+constexpr float kFloorMagic = 12582912.0f;    // 1.5 * 2^23
+constexpr int kFloorMagicBits = 0x4B400000;  // its fp32 bit pattern
 
 __global__ void __launch_bounds__(kThreads) k_qparams(QuantArgs a) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -90,13 +97,16 @@ __device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, ui
 // bucket of one value and its histogram update; returns the code
 __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_t* __restrict__ hA) {
     const float uf = __fmaf_rn(d, p.q.s_f, p.q.c_f);
-    const float bf = floorf(uf);
+    // floor(uf) for |uf| < 2^22: adding 1.5 * 2^23 rounding down lands on the
+    // integer grid of [2^23, 2^24); any other uf gives b far outside [0, 256)
+    const float tf = __fadd_rd(uf, kFloorMagic);
+    int b = __float_as_int(tf) - kFloorMagicBits;
+    const float bf = __fsub_rn(tf, kFloorMagic);
     const float fr = __fsub_rn(uf, bf);
-    int b = static_cast<int>(bf);
     uint32_t qv;
     if (static_cast<unsigned>(b) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
         const float r = __fsub_rn(d, __fmaf_rn(bf, p.q.w_f, p.q.lo_f));
-        qv = __float2uint_rn(__fmaf_rn(r, p.q.scale, static_cast<float>(kResBias)));
+        qv = __float_as_uint(__fmaf_rn(r, p.q.scale, p.q.qoff)) & 0x7FFFFFu;
     } else {
         rare_code(d, p.q, b, qv);
     }

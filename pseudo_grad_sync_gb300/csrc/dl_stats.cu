@@ -19,7 +19,9 @@
 //              with bulk copies (TMA engine), 8 consumer warps compute from
 //              shared memory. Per thread: fp32
 //              sums over groups of four, folded into float-float (hi + lo)
-//              sums that persist across all chunks of a tensor; the block
+//              sums that persist across all chunks of a tensor (squares on
+//              a power-of-two offset with exact error terms, so no rounding
+//              of a square biases the sum); the block
 //              reduces them (float-float butterfly, fp64 over the 8 warps)
 //              only when it moves to another tensor, into partial slot
 //              (k, t, j). Tensors shorter than 4096 elements and groups of
@@ -97,13 +99,20 @@ __device__ __forceinline__ void side_add(float d, float c, double& s1, double& s
     s2 = fma(y, y, s2);
 }
 
+// Per-thread sums. y^2 is summed on an offset: (s2h, s2l) holds H0 + the
+// squares since the last rebase, with H0 = yt^2 and yt a power of two at
+// least as large as every |y| this thread has summed since then; (c2h, c2l)
+// holds the squares summed before it (see sq_add and rebase).
 struct Acc {
-    float s1h, s1l, s2h, s2l;  // float-float sums of y and y^2
-    double s1d, s2d;           // fp64 side sums
+    float s1h, s1l;  // float-float sum of y
+    float s2h, s2l;  // float-float H0 + sum of y^2 since the last rebase
+    float c2h, c2l;  // float-float sum of y^2 before it
+    float yt, h0;    // current bound on |y| and H0 = yt^2
+    double s1d, s2d; // fp64 side sums
     int bad;
     bool side;
     __device__ __forceinline__ void reset() {
-        s1h = s1l = s2h = s2l = 0.f;
+        s1h = s1l = s2h = s2l = c2h = c2l = yt = h0 = 0.f;
         s1d = s2d = 0.0;
         bad = 0;
         side = false;
@@ -116,6 +125,11 @@ struct Acc {
 __device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
                               float (*red_ff)[4], double (*red_side)[2], int* red_bad) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // remove the offset (s2h >= H0, a power of two on its ulp grid, so the
+    // difference is exact) and join the squares summed before the last rebase
+    ff_add_ff(acc.c2h, acc.c2l, __fsub_rn(acc.s2h, acc.h0), acc.s2l);
+    acc.s2h = acc.c2h;
+    acc.s2l = acc.c2l;
 #pragma unroll
     for (int sh = 16; sh; sh >>= 1) {
         const float o1h = __shfl_xor_sync(kFull, acc.s1h, sh);
@@ -163,24 +177,98 @@ __device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
     consumer_sync();
 }
 
-__device__ __forceinline__ void add_group(Acc& acc, float4 gv, float4 rv, float csh) {
-    const float d0 = __fsub_rn(gv.x, rv.x), d1 = __fsub_rn(gv.y, rv.y);
-    const float d2 = __fsub_rn(gv.z, rv.z), d3 = __fsub_rn(gv.w, rv.w);
-    const float y0 = __fsub_rn(d0, csh), y1 = __fsub_rn(d1, csh);
-    const float y2 = __fsub_rn(d2, csh), y3 = __fsub_rn(d3, csh);
-    const float mx = fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3)));
-    // fp32 squares stay normal and finite for 2^-60 <= |y| <= 2^48
-    if (mx <= 0x1p48f && (mx >= 0x1p-60f || mx == 0.0f)) {  // false for NaN
-        const float b1 = __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3));
-        const float b2 = __fmaf_rn(y3, y3, __fmaf_rn(y2, y2, __fmaf_rn(y1, y1, __fmul_rn(y0, y0))));
-        ff_add(acc.s1h, acc.s1l, b1);
-        ff_add(acc.s2h, acc.s2l, b2);
+// y^2 added to the float-float sum (hi, lo) = H0 + squares, for |y| <= yt:
+// then y^2 <= H0 <= hi, the sum s = fl(hi + y^2) stays within [hi, 2 hi],
+// hi - s is exact, and fma(y, y, hi - s) is the rounding error of s, itself
+// rounded once (within 2^-25 ulp(s)). The error goes to lo. Plain fp32
+// squares are not enough: when Delta carries few significant bits relative to
+// sigma (|mu| >> sigma), y is a short integer times a power of two, and the
+// bits that rounding drops from its square follow the pattern of squares (an
+// odd square ends in ...001), so every rounding goes the same way; the error
+// terms keep those bits. As H0 <= 4 max y^2, the ulps involved stay within a
+// factor 2^-21 of the squares themselves.
+__device__ __forceinline__ void sq_add(float& hi, float& lo, float y) {
+    const float s = __fmaf_rn(y, y, hi);
+    const float err = __fmaf_rn(y, y, __fsub_rn(hi, s));
+    hi = s;
+    lo = __fadd_rn(lo, err);
+}
+
+// |y| up to mx (positive, normal) is about to be summed and exceeds yt: move
+// the offset sum into (c2h, c2l) and restart on yt = the power of two >= mx.
+// Taken at a thread's first non-zero group of a tensor and then only when a
+// value exceeds every earlier one by enough to cross a power of two.
+__device__ __forceinline__ void rebase(float& s2h, float& s2l, float& c2h, float& c2l, float& yt,
+                                    float& h0, float mx) {
+    ff_add_ff(c2h, c2l, __fsub_rn(s2h, h0), s2l);
+    yt = __int_as_float((__float_as_int(mx) + 0x7FFFFF) & static_cast<int>(0xFF800000u));
+    h0 = __fmul_rn(yt, yt);
+    s2h = h0;
+    s2l = 0.f;
+}
+
+// fold lo into hi (|lo| <= ulp(hi) afterwards), so that the roundings of
+// later additions to lo stay below 2^-24 ulp(hi)
+__device__ __forceinline__ void renorm(float& hi, float& lo) {
+    const float s = __fadd_rn(hi, lo);
+    lo = __fsub_rn(lo, __fsub_rn(s, hi));
+    hi = s;
+}
+
+constexpr int kTile = 4096;  // elements per pipeline tile
+
+// One thread's share of a full tile: kGroupsPerTile groups of four values.
+// All y are formed first so that one range check and at most one rebase
+// cover the whole share; a share with a value outside the fast range (or a
+// non-finite one) goes to the fp64 path as a whole.
+constexpr int kGroupsPerTile = kTile / 4 / kThreads;
+
+// max(|a|, b) that returns NaN if either input is NaN (fmaxf would drop it)
+__device__ __forceinline__ float absmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float* tr, int tid,
+                                         float csh) {
+    float y[kGroupsPerTile][4];
+    float mx = 0.f;
+#pragma unroll
+    for (int q = 0; q < kGroupsPerTile; ++q) {
+        const float4 gv = reinterpret_cast<const float4*>(tg)[tid + q * kThreads];
+        const float4 rv = reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
+        y[q][0] = __fsub_rn(__fsub_rn(gv.x, rv.x), csh);
+        y[q][1] = __fsub_rn(__fsub_rn(gv.y, rv.y), csh);
+        y[q][2] = __fsub_rn(__fsub_rn(gv.z, rv.z), csh);
+        y[q][3] = __fsub_rn(__fsub_rn(gv.w, rv.w), csh);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx = absmax_nan(y[q][e], mx);
+    }
+    // squares, their error terms and H0 stay normal and finite for
+    // 2^-50 <= |y| <= 2^48 (smaller values lose at most 2^-149); mx is NaN if
+    // any y is, so the fp64 path (which counts it) takes that share
+    if (mx <= 0x1p48f && (mx >= 0x1p-50f || mx == 0.0f)) {
+        if (mx > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, mx);
+#pragma unroll
+        for (int q = 0; q < kGroupsPerTile; ++q) {
+            const float b1 = __fadd_rn(__fadd_rn(y[q][0], y[q][1]), __fadd_rn(y[q][2], y[q][3]));
+            ff_add(acc.s1h, acc.s1l, b1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sq_add(acc.s2h, acc.s2l, y[q][e]);
+        }
+        renorm(acc.s2h, acc.s2l);
     } else {
         acc.side = true;
-        side_add(d0, csh, acc.s1d, acc.s2d, acc.bad);
-        side_add(d1, csh, acc.s1d, acc.s2d, acc.bad);
-        side_add(d2, csh, acc.s1d, acc.s2d, acc.bad);
-        side_add(d3, csh, acc.s1d, acc.s2d, acc.bad);
+#pragma unroll 1
+        for (int q = 0; q < kGroupsPerTile; ++q) {
+            const float4 gv = reinterpret_cast<const float4*>(tg)[tid + q * kThreads];
+            const float4 rv = reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
+            side_add(__fsub_rn(gv.x, rv.x), csh, acc.s1d, acc.s2d, acc.bad);
+            side_add(__fsub_rn(gv.y, rv.y), csh, acc.s1d, acc.s2d, acc.bad);
+            side_add(__fsub_rn(gv.z, rv.z), csh, acc.s1d, acc.s2d, acc.bad);
+            side_add(__fsub_rn(gv.w, rv.w), csh, acc.s1d, acc.s2d, acc.bad);
+        }
     }
 }
 
@@ -188,14 +276,16 @@ __device__ __forceinline__ void add_group(Acc& acc, float4 gv, float4 rv, float 
 // j, j + J, j + 2J, ... with j = b / K. The K blocks that read the same chunk
 // of theta_g run side by side, so theta_g crosses HBM once and is served to
 // the other K - 1 from L2. A producer warp streams the (theta_g, theta_k)
-// tiles of those chunks into a 3-stage shared-memory ring with bulk copies;
-// 8 consumer warps compute from shared memory. Each consumer thread keeps its
-// sums across every tile of a tensor; the consumers reduce them only when
-// they move to another tensor.
-constexpr int kTile = 4096;   // elements per pipeline tile
-constexpr int kStages = 3;    // tiles in flight per block
-
-__global__ void __launch_bounds__(kPipeThreads, 2) k_stats(StatsArgs a) {
+// tiles of those chunks into a STAGES-deep shared-memory ring with bulk
+// copies; 8 consumer warps compute from shared memory. Each consumer thread
+// keeps its sums across every tile of a tensor; the consumers reduce them
+// only when they move to another tensor. Two shapes: 3 stages with 2 blocks
+// per SM, and 2 stages with 3 blocks per SM (the same bytes in flight, more
+// consumer warps; faster when K is small and every element-learner brings
+// a theta_g value from HBM).
+template <int STAGES, int MINB>
+__global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
+    constexpr int kStages = STAGES;
     extern __shared__ __align__(128) float smem[];  // [kStages][kTile] theta_g, then theta_k
     float* sg = smem;
     float* sr = smem + kStages * kTile;
@@ -257,12 +347,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_stats(StatsArgs a) {
                     acc.reset();
                 }
                 if (pa == tb && pe == tb + kTile && !small) {
-#pragma unroll
-                    for (int q = 0; q < kTile / 4 / kThreads; ++q) {
-                        const int v = tid + q * kThreads;
-                        add_group(acc, reinterpret_cast<const float4*>(tg)[v],
-                                  reinterpret_cast<const float4*>(tr)[v], csh);
-                    }
+                    add_tile(acc, tg, tr, tid, csh);
                 } else {
                     for (int64_t e = pa + tid; e < pe; e += kThreads) {
                         const int l = static_cast<int>(e - tb);
@@ -271,14 +356,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_stats(StatsArgs a) {
                         const float d = __fsub_rn(gv, rv);
                         const float y = __fsub_rn(d, csh);
                         const float ay = fabsf(y);
-                        if (!small && ay <= 0x1p48f && (ay >= 0x1p-60f || ay == 0.0f)) {
+                        if (!small && ay <= 0x1p48f && (ay >= 0x1p-50f || ay == 0.0f)) {
+                            if (ay > acc.yt)
+                                rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
                             ff_add(acc.s1h, acc.s1l, y);
-                            ff_add(acc.s2h, acc.s2l, __fmul_rn(y, y));
+                            sq_add(acc.s2h, acc.s2l, y);
                         } else {
                             acc.side = true;
                             side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
                         }
                     }
+                    renorm(acc.s2h, acc.s2l);
                 }
             }
             __syncwarp();
@@ -389,12 +477,15 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     a.K = K;
     a.clip = clip_sigmas;
     a.J = 1;
-    const size_t smem = sizeof(float) * 2 * kStages * kTile;
+    const bool shallow = K <= 2;
+    const void* kern = shallow ? reinterpret_cast<const void*>(k_stats<2, 3>)
+                               : reinterpret_cast<const void*>(k_stats<3, 2>);
+    const size_t smem = sizeof(float) * 2 * (shallow ? 2 : 3) * kTile;
     if (a.n_chunks > 0) {
-        if ((st = cuda_status(cudaFuncSetAttribute(k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem)))) != DL_OK)
             return st;
-        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_stats), kPipeThreads, smem, K, a.n_chunks);
+        a.J = blocks_per_learner(kern, kPipeThreads, smem, K, a.n_chunks);
         if (a.J > max_blocks_per_learner(K)) a.J = max_blocks_per_learner(K);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -406,7 +497,10 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     k_shift<<<small_grid, kThreads, 0, s>>>(a);
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        k_stats<<<K * a.J, kPipeThreads, smem, s>>>(a);
+        if (shallow)
+            k_stats<2, 3><<<K * a.J, kPipeThreads, smem, s>>>(a);
+        else
+            k_stats<3, 2><<<K * a.J, kPipeThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     k_stats_fin<<<small_grid, kThreads, 0, s>>>(a);

@@ -132,8 +132,9 @@ def test_nonfinite_segment_is_invalid():
     sizes = [5000, 9000]
     g, reps = _make(sizes, 2, seed=3)
     reps[1][6000] = np.float32(np.inf)
+    reps[0][9321] = np.float32(np.nan)  # NaN must be counted like Inf
     rep, o, gp = compare(g, reps, sizes, nan_ok=True)
-    assert gp["stats"]["nonfinite"][1, 1] == 1
+    assert gp["stats"]["nonfinite"][1, 1] == 1 and gp["stats"]["nonfinite"][0, 1] == 1
     assert (gp["codes"][1, 5000:] == 0).all()
     assert np.isnan(gp["theta_g"][5000:]).all() and np.isfinite(gp["theta_g"][:5000]).all()
 
@@ -163,3 +164,50 @@ def test_tail_not_multiple_of_four():
 def test_empty_fragment_and_empty_tensors():
     g, reps = _make([0, 0, 10, 0], 2, seed=1)
     compare(g, reps, [0, 0, 10, 0])
+
+
+def test_large_mean_offset():
+    """Pseudo-gradients with |mu| thousands of sigma (a shared drift plus
+    small noise): the fp32 bucket edges then carry rounding errors of several
+    hundredths of a bucket width, and the fixed-point residuals must still be
+    in range. |mu|/sigma of 1e4 and 2e4 take the fp32 path, 1e5 the fp64 path."""
+    sizes = [60000, 4096, 20000, 9000]
+    g, reps = _make(sizes, 3, seed=31, scales=[1e-7, 1e-7, 3e-8, 1e-8],
+                    mean_shift=[1e-3, -2e-3, 5e-4, 1e-3])
+    rep, o, gp = compare(g, reps, sizes)
+    st = o["stats"]
+    ratio = np.abs(st.mean) / st.std
+    assert ratio.min() > 5e3 and ratio.max() > 5e4, ratio
+
+
+@pytest.mark.parametrize("seed,K", [(60, 2), (63, 2), (63, 4)])
+def test_mean_offset_straddling_a_power_of_two(seed, K):
+    """mu just inside -2^-10 (and -2^-8, -2^-12) with sigma ~1e-7 and theta
+    near 0, so Delta sits on the fine fp32 grid of the bucket edges: lo lies
+    one binade above most edges, its fp32 rounding is a whole ulp of an edge,
+    and an element can sit up to ~w/30 below its fp32 edge. Its residual must
+    still be carried exactly into the bucket mean."""
+    sizes = [60000, 60000, 60000]
+    mu = [-2.0**-10, -2.0**-8 + 2e-7, -2.0**-12]
+    g, reps = _make(sizes, K, seed=seed, scales=[1e-7, 1e-7, 1e-8], theta_std=1e-6,
+                    mean_shift=mu)
+    compare(g, reps, sizes)
+
+
+def test_unrepresentative_leading_values():
+    """Tensors whose first values differ from the rest: a large-spread head
+    (1000x sigma) followed by small values, a constant head, and a head of
+    exact zeros. Neither the shift nor the square offsets may depend on the
+    head being typical."""
+    sizes = [70000, 50000, 30000]
+    K = 3
+    g, reps = _make(sizes, K, seed=41, scales=[1e-6, 1e-4, 3e-5])
+    rng = np.random.default_rng(42)
+    off = np.concatenate([[0], np.cumsum(sizes)])
+    for k in range(K):
+        d = (g - reps[k]).astype(np.float64)
+        d[off[0]:off[0] + 64] = rng.standard_normal(64) * 1e-3      # 1000x spread head
+        d[off[1]:off[1] + 100] = 2.5e-4                            # constant head
+        d[off[2]:off[2] + 200] = 0.0                               # zero head
+        reps[k] = (g - d).astype(np.float32)
+    compare(g, reps, sizes)

@@ -76,7 +76,7 @@ def test_noalloc_matches_quantize_on_two_calls(noalloc, reverse):
         s = dl.stats_to_host(stats)
         width = (s["hi"] - s["lo"]) / 256
         a, b = cb_a.cpu().numpy(), cb_b.cpu().numpy()
-        tol = 2 * np.spacing(np.abs(a)).astype(np.float64) + width[..., None] * 2.0**-22
+        tol = 2 * np.spacing(np.abs(a)).astype(np.float64) + width[..., None] * 2.0**-21
         assert np.all(np.abs(a.astype(np.float64) - b) <= tol)
 
 
