@@ -43,6 +43,7 @@ import synthetic  # noqa: E402
 
 METRIC = "outer-step params/s & achieved HBM GB/s (quantise+merge+Nesterov, K learners)"
 UNIT = "params/s"
+LEARNER_METRIC = "learner-side quantiser params/s (stats + quantise, K=1, whole model)"
 
 
 def algo_bytes(K):
@@ -223,6 +224,115 @@ def traffic_record(name):
     return rec if h.hexdigest() == rec["sha256"] else None
 
 
+def learner_device_data(wl, dev, gen_seed=0):
+    """theta_g and the learner's replica of the whole model, filled on the
+    device with the workload's distributions (theta_g ~ N(0, theta_std),
+    Delta ~ N(0, sigma_t) per tensor)."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(gen_seed)
+    n = wl.n_elems
+    g = torch.empty(n, dtype=torch.float32, device=dev).normal_(0.0, wl.theta_std, generator=gen)
+    r = torch.empty_like(g)
+    o = 0
+    for t, m in enumerate(wl.numels):
+        d = torch.empty(m, dtype=torch.float32, device=dev).normal_(0.0, wl.tensor_scale(t),
+                                                                   generator=gen)
+        torch.sub(g[o:o + m], d, out=r[o:o + m])
+        o += m
+    return g, r
+
+
+def run_learner(args, rank, world, local):
+    """Learner-side quantiser: one learner's whole model, every tensor in one
+    ragged batch, dl_pseudograd_stats + dl_quantize with K=1 per step (codes
+    and codebooks are what the learner would send)."""
+    import torch
+
+    import pseudo_grad_sync_gb300 as dl
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = synthetic.WORKLOADS[args.workload]()
+    F = dl.Fragment(wl.numels, dev)
+    g, r = learner_device_data(wl, dev, gen_seed=rank)
+    stats = dl.new_stats(1, F.T, dev)
+    codes = [torch.empty(F.n, dtype=torch.uint8, device=dev)]
+    cb = torch.empty((1, F.T, 256), dtype=torch.float32, device=dev)
+    ws_s = dl.new_workspace(dl.stats_workspace_bytes(F, 1), dev)
+    ws_q = dl.new_workspace(dl.quantize_workspace_bytes(F, 1), dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dl.pseudograd_stats(g, [r], F, 6.0, stats, ws_s, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        dl.quantize(g, [r], F, stats, codes, cb, None, ws_q, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    peak, peak_kind = load_peaks()
+    ab = {"stats": 8, "quantize": 9}
+    calls = {}
+    for i, name in enumerate(("stats", "quantize")):
+        tot = sum(e[i].elapsed_time(e[i + 1]) for e in ev)
+        avg_s = tot / args.steps / 1e3
+        gbs = ab[name] * wl.n_elems / avg_s / 1e9
+        calls[name] = {"ms_per_step": tot / args.steps, "algo_bytes_per_elem": ab[name],
+                       "achieved_gbs": gbs, "frac": gbs / peak}
+    dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
+    full_gbs = 17 * wl.n_elems / (ms_per_step / 1e3) / 1e9
+    out = {
+        "metric": LEARNER_METRIC,
+        "value": world * wl.n_elems / (ms_per_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (device-filled)",
+        "config": {"workload": wl.name + ": " + wl.description, "K": 1, "params": wl.n_elems,
+                   "l2": "no flush: every call streams >= 8.8 GB, inputs larger than L2"},
+        "full_step_gbs": full_gbs, "full_step_frac": full_gbs / peak, "calls": calls,
+        "roofline": {"bound": "hbm", "achieved": round(calls[dominant]["achieved_gbs"], 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(calls[dominant]["frac"], 4),
+                     "traffic": None, "kernel": {"stats": "k_stats",
+                                                 "quantize": "k_quantize"}[dominant],
+                     "note": f"peak = {peak_kind} copy bandwidth"},
+        "clocks": clk, "gpu_launches": args.steps * 6, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -346,28 +456,31 @@ def run_ours(args, rank, world, local):
         "e2e": e2e, "setup_generate_s": gen_s,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl, frags, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline(wl, frags, host, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
 def run_e2e(run, host, args, world, dev):
     """Same step through the public API with host buffers: each fragment's K
-    replicas are copied from pinned host memory (double-buffered on a copy
-    stream) and the updated theta_g is copied back, all inside the timed
-    region."""
+    replicas are copied from pinned host memory on an upload stream (double-
+    buffered), the fragment is synced with dl_outer_sync as soon as they land,
+    and the updated theta_g goes back on a download stream, all inside the
+    timed region. Uploads never wait for downloads, so the upload link stays
+    busy for the whole step."""
     import torch
 
     K = run.wl.K
     max_n = max(f.n for f in run.F)
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     stage = [[torch.empty(max_n, dtype=torch.float32, device=dev) for _ in range(K)]
              for _ in range(2)]
     g_out = [torch.empty_like(h[0], pin_memory=True) for h in host]
     nF = len(run.F)
     bi = sum(K * f.n * 4 for f in run.F)
     bo = sum(f.n * 4 for f in run.F)
+    ws = run.msync.workspace  # sized for the largest fragment
 
     def one_step():
         ready = [torch.cuda.Event() for _ in range(nF)]
@@ -375,25 +488,21 @@ def run_e2e(run, host, args, world, dev):
         for f in range(nF):
             buf = stage[f % 2]
             n = run.F[f].n
-            with torch.cuda.stream(copy):
+            with torch.cuda.stream(up):
                 if f >= 2:
-                    copy.wait_event(done[f - 2])
+                    up.wait_event(done[f - 2])
                 for k in range(K):
                     buf[k][:n].copy_(host[f][1][k], non_blocking=True)
-                ready[f].record(copy)
+                ready[f].record(up)
             comp.wait_event(ready[f])
-            reps = [b[:n] for b in buf]
-            F = run.F[f]
-            run.dl.pseudograd_stats(run.g[f], reps, F, 6.0, run.stats, run.ws_s, comp)
-            run.dl.quantize(run.g[f], reps, F, run.stats, run.codes, run.codebook, None,
-                            run.ws_q, comp)
-            run.dl.merge_outer_step(run.g[f], run.m[f], F, run.codes, run.codebook, K=K,
-                                    lr=0.7, mu=0.9, stream=comp)
+            run.dl.outer_sync([run.F[f]], [run.g[f]], [run.m[f]], [[b[:n] for b in buf]], K,
+                              workspace=ws, stream=comp)
             done[f].record(comp)
-            with torch.cuda.stream(copy):
-                copy.wait_event(done[f])
+            with torch.cuda.stream(down):
+                down.wait_event(done[f])
                 g_out[f].copy_(run.g[f], non_blocking=True)
-        comp.wait_stream(copy)
+        comp.wait_stream(up)
+        comp.wait_stream(down)
 
     steps = max(2, min(args.steps, 5))
     for _ in range(2):
@@ -412,86 +521,79 @@ def run_e2e(run, host, args, world, dev):
         dt = float(t.item())
     return {"value": world * run.wl.n_elems * steps / dt, "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
-            "ms_per_step": dt / steps * 1e3,
-            "note": "replicas H2D from pinned memory on a copy stream (double-buffered), "
-                    "updated theta_g D2H; momentum and theta_g state stay on the device"}
+            "ms_per_step": dt / steps * 1e3, "h2d_gbs": bi * steps / dt / 1e9,
+            "note": "replicas H2D from pinned memory on an upload stream (double-buffered), "
+                    "dl_outer_sync per fragment as it lands, updated theta_g D2H on a "
+                    "download stream; momentum and theta_g state stay on the device; "
+                    "bound by the host-to-device link"}
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timings
 
 
-def oracle_sample(wl, frags, target_elems):
-    """A bounded sample of the workload: whole tensors, in fragment order,
-    skipping any that would overshoot target_elems."""
-    chosen = []
-    tot = 0
+def oracle_pass(wl, host, offsets):
+    """One whole-model step of the oracle, fragment by fragment, on the host
+    copy of the workload (the outer step; for a learner workload, stats and
+    quantisation only); returns the seconds it took."""
+    import oracle
+
+    t0 = time.perf_counter()
+    for (g, reps), off in zip(host, offsets):
+        gn = g.numpy()
+        rn = [r.numpy() for r in reps]
+        if wl.role == "learner":
+            oracle.quantize(gn, rn, oracle.stats(gn, rn, off), off)
+            continue
+        o = oracle.outer_step(gn, np.zeros_like(gn), rn, offsets=off)
+        assert o["status"] == 0
+    return time.perf_counter() - t0
+
+
+def fragment_offsets(wl, frags):
+    out = []
     for ts in frags:
-        for t in ts:
-            if tot + wl.numels[t] <= target_elems:
-                chosen.append(t)
-                tot += wl.numels[t]
-    if not chosen:
-        chosen = [min(range(wl.n_tensors), key=lambda t: wl.numels[t])]
-    numels = [wl.numels[t] for t in chosen]
-    n = sum(numels)
-    g = np.empty(n, dtype=np.float32)
-    reps = [np.empty(n, dtype=np.float32) for _ in range(wl.K)]
-    o = 0
-    for t in chosen:
-        m = wl.numels[t]
-        wl.theta_global(t, out=g[o:o + m])
-        for k in range(wl.K):
-            wl.replica(k, t, g[o:o + m], out=reps[k][o:o + m])
-        o += m
-    off = np.zeros(len(numels) + 1, dtype=np.int64)
-    np.cumsum(numels, out=off[1:])
-    return g, reps, off, chosen
+        off = np.zeros(len(ts) + 1, dtype=np.int64)
+        np.cumsum([wl.numels[t] for t in ts], out=off[1:])
+        out.append(off)
+    return out
 
 
-def time_oracle(g, reps, off, reps_min=1, budget_s=10.0):
+def cpu_baseline(wl, frags, host, budget_s=10.0):
+    """The oracle on the host cores over the same workload (the same host
+    arrays the GPU run uploads): whole-model passes until budget_s elapsed."""
     import oracle
 
-    m = np.zeros_like(g)
-    times = []
-    t_start = time.perf_counter()
-    while len(times) < reps_min or (time.perf_counter() - t_start < budget_s and len(times) < 5):
-        t0 = time.perf_counter()
-        oracle.outer_step(g, m, reps, offsets=off)
-        times.append(time.perf_counter() - t0)
-    return statistics.median(times), len(times)
-
-
-def cpu_baseline(wl, frags, budget_s=10.0):
-    import oracle
-
-    g, reps, off, chosen = oracle_sample(wl, frags, target_elems=24_000_000)
-    t, nrep = time_oracle(g, reps, off, budget_s=budget_s)
-    return {"value": g.size / t, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{len(chosen)} whole tensors, {g.size} elements x K={wl.K} of the "
-                      f"workload, full outer step (stats+quantise+merge+Nesterov), median "
-                      f"of {nrep} runs of {t:.2f} s"}
+    offsets = fragment_offsets(wl, frags)
+    total, passes = 0.0, 0
+    while passes == 0 or total < budget_s:
+        total += oracle_pass(wl, host, offsets)
+        passes += 1
+    return {"value": wl.n_elems * passes / total, "unit": UNIT, "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"the whole workload ({wl.n_elems} elements x K={wl.K}, "
+                      f"{len(frags)} fragments), full outer step (stats+quantise+merge+"
+                      f"Nesterov) per fragment, {passes} pass(es) in {total:.1f} s"}
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one whole-model outer step
+    of the workload on the host cores."""
     import oracle
 
     if rank != 0:
         return
     wl = synthetic.WORKLOADS[args.workload]()
-    import pseudo_grad_sync_gb300  # noqa: F401  (planner only: host code, no GPU work)
     frag_of, _ = oracle.plan_fragments(wl.numels, wl.n_frags)
     frags = fragment_tensors(wl, frag_of)
-    g, reps, off, chosen = oracle_sample(wl, frags, target_elems=8_000_000)
-    m = np.zeros_like(g)
+    host = generate_host(wl, frags, pin=False)
+    offsets = fragment_offsets(wl, frags)
     for _ in range(args.warmup):
-        oracle.outer_step(g, m, reps, offsets=off)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.outer_step(g, m, reps, offsets=off)
-    dt = time.perf_counter() - t0
-    value = g.size * args.steps / dt
-    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        oracle_pass(wl, host, offsets)
+    dt = sum(oracle_pass(wl, host, offsets) for _ in range(args.steps))
+    value = wl.n_elems * args.steps / dt
+    metric = LEARNER_METRIC if wl.role == "learner" else METRIC
+    out = {"impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic",
@@ -499,8 +601,8 @@ def run_reference(args, rank, world):
                       "fragments": wl.n_frags, "params": wl.n_elems},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
                             "kind": "oracle",
-                            "sample": f"each step: {len(chosen)} whole tensors, {g.size} "
-                                      f"elements x K={wl.K}, full outer step on the host"},
+                            "sample": f"each step: the whole workload ({wl.n_elems} elements "
+                                      f"x K={wl.K}), full outer step on the host"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -528,8 +630,11 @@ def main():
             dist.init_process_group("nccl")
         else:
             dist.init_process_group("gloo")
+    learner = synthetic.WORKLOADS[args.workload]().role == "learner"
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif learner:
+        run_learner(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -20,6 +20,10 @@ outer-step benchmark; sizes are computed from the model dimensions):
   (every 10th forced to 4096), K=8, Delta = 1e-3 * Student-t(3).
 * ``quorum_10b`` - the 10B shapes, K=16 learners, a seeded random present
   subset of size 1..16 and weights ~ U[0.5, 1.5] per (fragment, outer step).
+* ``learner_1b`` / ``learner_10b`` - one learner (K=1) quantising its whole
+  1.1B / 10B model for transmission: every tensor in one ragged batch, no
+  merge (the INTELLECT-1 notes' worked example, section 3.2 steps 4-5, at
+  full-model scale).
 """
 from __future__ import annotations
 
@@ -150,6 +154,7 @@ class Workload:
     n_frags: int = 1
     steps: int = 1
     quorum: bool = False            # random present subsets and weights
+    role: str = "syncer"            # "learner": stats + quantise only, K=1
     description: str = ""
     _sigmas: list = field(default=None, repr=False)
 
@@ -233,12 +238,27 @@ def quorum_10b(K=16, steps=4):
                     description="10B shapes, K=16, random quorum 1..16, weights U[0.5,1.5]")
 
 
+def learner_1b():
+    return Workload("learner_1b", decoder_1b_numels(), 1, SEED + 6, per_tensor_sigma=True,
+                    role="learner",
+                    description="one learner quantises its whole 1.1B decoder set "
+                                "(201 tensors) as one ragged batch, K=1")
+
+
+def learner_10b():
+    return Workload("learner_10b", decoder_10b_numels(), 1, SEED + 7, role="learner",
+                    description="one learner quantises its whole 10B decoder set "
+                                "(381 tensors) as one ragged batch, K=1")
+
+
 WORKLOADS = {
     "worked_example": worked_example,
     "decoder_1b": decoder_1b,
     "decoder_10b": decoder_10b,
     "ragged_heavy": ragged_heavy,
     "quorum_10b": quorum_10b,
+    "learner_1b": learner_1b,
+    "learner_10b": learner_10b,
 }
 
 

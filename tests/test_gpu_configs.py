@@ -251,3 +251,60 @@ def test_quorum_10b_embedding_fragment():
     present, weights = wl.present(f, 0), wl.weights(f, 0)
     idx, db, counts = run.step(0, present=present, weights=weights)
     run.check(0, idx, db, counts, present=present, weights=weights)
+
+
+def _learner_whole_model(wl, sampled):
+    """Stats + quantise of one learner's whole model as one ragged batch (the
+    learner-side quantiser); sampled tensors checked against the oracle."""
+    run = FragmentRun(wl, list(range(wl.n_tensors)), sampled, K=1, gen_seed=11)
+    dl = run.dl
+    reps = run.replicas(0)
+    counts = torch.empty((1, run.frag.T, 256), dtype=torch.int32, device="cuda")
+    dl.pseudograd_stats(run.g, reps, run.frag, 6.0, run.sync.stats, run.sync.ws_stats)
+    dl.quantize(run.g, reps, run.frag, run.sync.stats, run.sync.codes, run.sync.codebook, counts,
+                run.sync.ws_quant)
+    torch.cuda.synchronize()
+    del reps
+    st_all = dl.stats_to_host(run.sync.stats)
+    cb_all = run.sync.codebook.cpu().numpy()
+    cnt_all = counts.cpu().numpy().view(np.uint32)
+    assert (st_all["count"][0] == np.asarray(wl.numels)).all()
+    assert (st_all["nonfinite"] == 0).all()
+    exc = 0
+    for t, h in run.host.items():
+        i, a, b = h["i"], h["a"], h["b"]
+        rep = (h["g"] - _delta_host(wl, t, 0, 0)).astype(np.float32)
+        st = oracle.stats(h["g"], [rep])
+        codes_o, cb_o, cnt_o = oracle.quantize(h["g"], [rep], st)
+        o = {"stats": st, "codes": codes_o, "codebook": cb_o, "counts": cnt_o}
+        gp = {"stats": {key: v[:, i:i + 1] for key, v in st_all.items()},
+              "codes": run.sync.codes[0][a:b].cpu().numpy()[None, :],
+              "codebook": cb_all[:, i:i + 1], "counts": cnt_all[:, i:i + 1]}
+        check_stats(st, gp["stats"], 1, 1)
+        n_exc, moved = check_codes(o, gp, h["g"], [rep], np.array([0, b - a]))
+        check_codebook(o, gp, moved)
+        exc += n_exc
+        print(f"learner tensor {t} n={b - a} boundary exceptions {n_exc}")
+    return exc
+
+
+def test_learner_1b_whole_model():
+    """One learner, the whole 1.1B set (201 tensors, 1.1G elements) in one
+    launch per kernel: smallest tensor, a norm vector, a 2048x2048 and the
+    embedding checked against the oracle."""
+    wl = synthetic.learner_1b()
+    sizes = np.asarray(wl.numels)
+    sampled = {int(np.argmin(sizes)), int(np.nonzero(sizes == 2048)[0][0]),
+               int(np.nonzero(sizes == 2048 * 2048)[0][0]), 0}
+    _learner_whole_model(wl, sampled)
+
+
+def test_learner_10b_whole_model():
+    """One learner, the whole 10B set (381 tensors, 10.2G elements: element
+    indices far past 2^32) in one launch per kernel; the lm_head, the final
+    norm and the last layer's down projection (all starting past 9.6G) and
+    the first layer's q projection are checked against the oracle."""
+    wl = synthetic.learner_10b()
+    T = wl.n_tensors
+    assert wl.numels[T - 5] == 4096 * 14336 and wl.numels[T - 2] == 4096
+    _learner_whole_model(wl, {T - 1, T - 2, T - 5, 1})
