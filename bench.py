@@ -630,7 +630,19 @@ def main():
             dist.init_process_group("nccl")
         else:
             dist.init_process_group("gloo")
-    learner = synthetic.WORKLOADS[args.workload]().role == "learner"
+    wl = synthetic.WORKLOADS[args.workload]()
+    learner = wl.role == "learner"
+    # resident footprint: the whole model with every replica in HBM (and, for
+    # the syncer, a host copy of the inputs); refuse before allocating
+    dev_gb = (2 * 4 + 1 if learner else (wl.K + 2) * 4 + wl.K) * wl.n_elems / 1e9
+    host_gb = 0.0 if learner else (wl.K + 2) * 4 * wl.n_elems / 1e9
+    if dev_gb > 200 or host_gb > 64:
+        if rank == 0:
+            print(json.dumps({"error": f"workload {wl.name} needs ~{dev_gb:.0f} GB on the device "
+                                       f"and ~{host_gb:.0f} GB on the host as one resident "
+                                       "model; the benchmark runs whole models that fit "
+                                       "(its fragments are covered by the parity tests)"}))
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif learner:
