@@ -8,7 +8,9 @@ follows and for the readings taken where the pages are silent.
 Every function here is pinned by tests that do not retype its formulas:
 closed forms, the INTELLECT-1 worked example (section 3.2), brute force on
 tiny inputs, the bucket-mean optimality property (section 4.1 step 4), the
-code-space counterexample (section 4.2) and the planner's LPT bound.
+code-space counterexample (section 4.2), the planner's LPT bound, and for the
+ring accumulation its reductions to the plain merge and its per-hop error
+bound.
 """
 from __future__ import annotations
 
@@ -61,6 +63,9 @@ def lib():
         L.oracle_merge_outer_step.restype = ctypes.c_int
         L.oracle_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
                                               f32, f32, vp]
+        L.oracle_ring_outer_step.restype = ctypes.c_int
+        L.oracle_ring_outer_step.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f64, f32,
+                                             f32, vp]
         _lib = L
     return _lib
 
@@ -210,3 +215,23 @@ def outer_step(theta_g, momentum, replicas, offsets=None, weights=None, present=
                                             want_delta_bar=True)
     out.update(status=status, theta_g=g, momentum=m, delta_bar=db)
     return out
+
+
+def ring_outer_step(theta_g, momentum, replicas, offsets=None, weights=None, present=None,
+                    min_quorum=1, lr=0.7, mu=0.9, clip_sigmas=6.0):
+    """Ring accumulation with re-quantisation at every hop (INTELLECT-1 notes,
+    section 4.2), then the outer Nesterov step. Returns (status, theta_g',
+    momentum', delta_bar); inputs untouched."""
+    g = np.array(theta_g, dtype=np.float32, copy=True)
+    m = np.array(momentum, dtype=np.float32, copy=True)
+    off = _offsets(offsets, g.size)
+    T = len(off) - 1
+    reps = [_f32(r) for r in replicas]
+    w = None if weights is None else _f32(weights)
+    p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    db = np.empty_like(g)
+    st = lib().oracle_ring_outer_step(
+        g.ctypes.data, m.ctypes.data, _ptrs(reps), len(reps), off.ctypes.data, T,
+        None if w is None else w.ctypes.data, None if p is None else p.ctypes.data, min_quorum,
+        clip_sigmas, lr, mu, db.ctypes.data)
+    return st, g, m, db

@@ -318,3 +318,78 @@ int oracle_merge_outer_step(float* theta_g, float* momentum, const uint8_t* cons
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Ring accumulation with re-quantisation at every hop (INTELLECT-1 notes,  */
+/* sec. 4.2: what a node receives is dequantised, added to in fp32, and     */
+/* quantised again before it is sent on).                                   */
+
+/*
+ * The present learners, in increasing order, form the ring s = 0 .. S-1; the
+ * partial sum P travels along it:
+ *   P_0 = w_0 * Delta_0                                   (fp32 product)
+ *   P_s = fmaf(w_s, Delta_s, dec(Q(P_{s-1})))            s = 1 .. S-1
+ * where Q is the per-tensor quantiser of sec. 4.1 (oracle_stats and
+ * oracle_quantize applied to P itself) and dec its codebook lookup. The
+ * last holder keeps its fp32 sum: D = P_{S-1} feeds the outer Nesterov step
+ * exactly as in oracle_merge_outer_step. A present learner of weight 0 is
+ * still a hop (it re-quantises what passes through). delta_bar_out may be
+ * NULL. Returns the merge-weight status.
+ */
+int oracle_ring_outer_step(float* theta_g, float* momentum, const float* const* theta_k,
+                           int32_t K, const int64_t* offsets, int32_t T, const float* weights,
+                           const uint8_t* present, int32_t min_quorum, double clip_sigmas,
+                           float lr, float mu, float* delta_bar_out) {
+    float w_hat[256];
+    if (K > 256) return OR_ERR_ARG;
+    int np = oracle_merge_weights(weights, present, K, min_quorum, w_hat);
+    if (np < 0) return np;
+    const int64_t n = T > 0 ? offsets[T] : 0;
+    const size_t nn = (size_t)(n > 0 ? n : 1);
+    float* P = (float*)malloc(sizeof(float) * nn);
+    float* zero = (float*)calloc(nn, sizeof(float));
+    uint8_t* code = (uint8_t*)malloc(nn);
+    float* cb = (float*)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1) * NB);
+    const size_t tt = (size_t)(T > 0 ? T : 1);
+    int64_t* cnt = (int64_t*)malloc(sizeof(int64_t) * tt);
+    int64_t* bad = (int64_t*)malloc(sizeof(int64_t) * tt);
+    double* mean = (double*)malloc(sizeof(double) * tt);
+    double* sd = (double*)malloc(sizeof(double) * tt);
+    double* lo = (double*)malloc(sizeof(double) * tt);
+    double* hi = (double*)malloc(sizeof(double) * tt);
+    if (!P || !zero || !code || !cb || !cnt || !bad || !mean || !sd || !lo || !hi) {
+        free(P); free(zero); free(code); free(cb); free(cnt); free(bad);
+        free(mean); free(sd); free(lo); free(hi);
+        return OR_ERR_ARG;
+    }
+    const float* zp[1] = {zero};
+    uint8_t* cp[1] = {code};
+    int first = 1;
+    for (int32_t k = 0; k < K; ++k) {
+        if (present && !present[k]) continue; /* absent: never read */
+        if (first) {
+            for (int64_t i = 0; i < n; ++i) P[i] = w_hat[k] * pseudo_grad(theta_g[i], theta_k[k][i]);
+            first = 0;
+            continue;
+        }
+        /* the partial sum is quantised for sending, then decoded on arrival;
+           P - 0 is P exactly, so the quantiser sees P itself */
+        oracle_stats(P, zp, 1, offsets, T, clip_sigmas, cnt, bad, mean, sd, lo, hi);
+        oracle_quantize(P, zp, 1, offsets, T, mean, lo, hi, bad, cp, cb, NULL);
+        for (int32_t t = 0; t < T; ++t)
+            for (int64_t i = offsets[t]; i < offsets[t + 1]; ++i)
+                P[i] = fmaf(w_hat[k], pseudo_grad(theta_g[i], theta_k[k][i]),
+                            cb[(int64_t)t * NB + code[i]]);
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const float acc = P[i];
+        const float m_new = fmaf(mu, momentum[i], acc);
+        const float g = fmaf(mu, m_new, acc);
+        if (delta_bar_out) delta_bar_out[i] = acc;
+        momentum[i] = m_new;
+        theta_g[i] = fmaf(-lr, g, theta_g[i]);
+    }
+    free(P); free(zero); free(code); free(cb); free(cnt); free(bad);
+    free(mean); free(sd); free(lo); free(hi);
+    return OR_OK;
+}
