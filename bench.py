@@ -333,6 +333,79 @@ def run_learner(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def ring_algo_bytes(S):
+    """Algorithmic bytes per element of one ring step over S learners: hop 0
+    reads theta_g and a replica and writes P (12); each later hop quantises P
+    (stats 4, quantise 4 + 1) and then reads the codes, theta_g and a replica
+    and writes P (13), the last one instead reading momentum and writing
+    theta and momentum (21)."""
+    if S == 1:
+        return 24
+    return 12 + 9 * (S - 1) + 13 * (S - 2) + 21
+
+
+def run_ring(args, rank, world, local):
+    """Ring accumulation with re-quantisation at every hop (dl_ring_outer_step)
+    over every fragment of the workload, one call per fragment."""
+    import torch
+
+    import pseudo_grad_sync_gb300 as dl
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = synthetic.WORKLOADS[args.workload]()
+    frag_of, load = dl.plan_fragments(wl.numels, wl.n_frags)
+    frags = fragment_tensors(wl, frag_of)
+    host = generate_host(wl, frags, pin=False)
+    run = DeviceRun(wl, frags, host, dev)
+    del host
+    ws = dl.new_workspace(max(dl.ring_workspace_bytes(F) for F in run.F), dev)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in run.F]
+
+    def step(timed=False):
+        for f, F in enumerate(run.F):
+            if timed:
+                ev[f][0].record(stream)
+            dl.ring_outer_step(run.g[f], run.m[f], F, run.reps[f], workspace=ws, stream=stream)
+            if timed:
+                ev[f][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(None)
+    clocks.start()
+    time.sleep(0.3)
+    tot_call = 0.0
+    for _ in range(args.steps):
+        step(timed=True)
+        torch.cuda.synchronize()
+        tot_call += sum(e[0].elapsed_time(e[1]) for e in ev)
+    clk = clocks.stop()
+    ms_per_step = tot_call / args.steps  # the calls run back to back within a step
+    peak, peak_kind = load_peaks()
+    ab = ring_algo_bytes(wl.K)
+    gbs = ab * wl.n_elems / (tot_call / args.steps / 1e3) / 1e9
+    out = {
+        "metric": "ring outer-step params/s (re-quantised at every hop, K learners)",
+        "value": world * wl.n_elems / (ms_per_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name + ": " + wl.description, "K": wl.K,
+                   "fragments": wl.n_frags, "params": wl.n_elems, "mode": "ring"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "note": f"{ab} algorithmic B/elem per ring step; calls timed with CUDA "
+                             f"events; peak = {peak_kind} copy bandwidth"},
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * (1 + 7 * (wl.K - 1)),
+        "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -618,6 +691,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--mode", choices=["outer", "ring"], default="outer",
+                    help="ring: accumulate along a ring, re-quantising at every hop")
     args = ap.parse_args()
     rank, world, local = env_rank()
     if world > 1:
@@ -647,6 +722,8 @@ def main():
         run_reference(args, rank, world)
     elif learner:
         run_learner(args, rank, world, local)
+    elif args.mode == "ring":
+        run_ring(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -124,7 +124,9 @@ size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K);
  * clip_sigmas * std, hi = mean + clip_sigmas * std, computed to fp64
  * accuracy, plus the element and non-finite counts.
  *   theta_g      device [n] fp32, global parameters at the start of the round
- *   theta_k      host [K] of device [n] fp32, learner replicas
+ *   theta_k      host [K] of device [n] fp32, learner replicas; or NULL with
+ *                K = 1 for values mode: Delta is theta_g itself (statistics of
+ *                any fp32 vector, e.g. a partial sum to be re-quantised)
  *   clip_sigmas  > 0, 6 in the pages
  *   d_stats      device [K*T] dl_stats, out (8-byte aligned)
  *   d_workspace  device scratch of dl_stats_workspace_bytes(frag, K) bytes
@@ -146,6 +148,8 @@ size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K);
  * A segment whose range is below 256 * FLT_MIN (sigma = 0 included) gets
  * code 0 everywhere and cb[b] = (float)mean; a segment with non-finite
  * elements gets code 0 everywhere and a NaN codebook.
+ *   theta_g, theta_k  as for dl_pseudograd_stats (theta_k NULL with K = 1:
+ *               values mode, the vector quantised is theta_g itself)
  *   d_stats     device [K*T], as written by dl_pseudograd_stats
  *   codes       host [K] of device [n] uint8, out
  *   d_codebook  device [K*T*256] fp32, out, index (k*T + t)*256 + b
@@ -238,6 +242,38 @@ size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs
 int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, double clip_sigmas,
                   int32_t min_quorum, float lr, float mu, int32_t flags, void* d_workspace,
                   size_t workspace_bytes, void* stream);
+
+/* Workspace bytes needed by dl_ring_outer_step for this fragment (0 on a bad
+ * fragment); independent of K. */
+size_t dl_ring_workspace_bytes(const dl_fragment* frag);
+
+/*
+ * Ring accumulation with re-quantisation at every hop, then the outer
+ * Nesterov step (INTELLECT-1 notes, section 4.2: a node dequantises what it
+ * receives, adds in fp32, and quantises again before sending on; section 4.1
+ * for the quantiser). The present learners, in increasing order, form the
+ * ring s = 0 .. S-1 and the partial sum P passes along it:
+ *   P_0 = w_0 * Delta_0                         (fp32)
+ *   P_s = fmaf(w_s, Delta_s, dec(Q(P_{s-1})))   s = 1 .. S-1
+ *   D = P_{S-1}; then the outer step of dl_merge_outer_step.
+ * Q is the per-tensor quantiser of dl_quantize applied to P itself, with
+ * clip_sigmas; w_s are the weights normalised over the present learners as
+ * for the merge. A present learner of weight 0 is still a hop. Compared with
+ * dl_merge_outer_step (one quantisation per learner), the error of D grows
+ * with the number of hops: this call measures that.
+ *   theta_g, momentum  device [n] fp32, in/out
+ *   theta_k     host [K] of device [n] fp32 (absent learners never read)
+ *   weights, present, min_quorum, lr, mu, delta_bar_out  as for
+ *               dl_merge_outer_step
+ *   d_workspace device scratch of dl_ring_workspace_bytes(frag) bytes (holds
+ *               P, its codes and codebooks; its first word is the device
+ *               status word)
+ */
+int dl_ring_outer_step(float* theta_g, float* momentum, const float* const* theta_k, int32_t K,
+                       const dl_fragment* frag, const float* weights, const uint8_t* present,
+                       int32_t min_quorum, double clip_sigmas, float lr, float mu,
+                       float* delta_bar_out, void* d_workspace, size_t workspace_bytes,
+                       void* stream);
 
 /*
  * dl_quantize without a caller-provided workspace. The pages have no

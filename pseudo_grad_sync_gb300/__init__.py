@@ -8,6 +8,8 @@ C entry points (see include/diloco_sync.h) keep their names here:
     pseudograd_stats     per-(learner, tensor) mu / sigma / clip range
     quantize             uint8 codes + bucket-mean codebooks
     merge_outer_step     decode, weighted fp32 mean, outer Nesterov (in place)
+    ring_outer_step      ring accumulation re-quantised at every hop, then the
+                         outer step (measures the error growth of a ring)
     outer_sync           the three calls over every fragment of a model, with
                          consecutive fragments overlapped on two streams
 
@@ -79,6 +81,11 @@ def lib():
         L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32]
         L.dl_outer_sync.restype = ctypes.c_int
         L.dl_outer_sync.argtypes = [jb, i32, i32, f64, i32, f32, f32, i32, vp, sz, vp]
+        L.dl_ring_workspace_bytes.restype = sz
+        L.dl_ring_workspace_bytes.argtypes = [fr]
+        L.dl_ring_outer_step.restype = ctypes.c_int
+        L.dl_ring_outer_step.argtypes = [vp, vp, vp, i32, fr, vp, vp, i32, f64, f32, f32, vp, vp,
+                                         sz, vp]
         L.dl_read_device_status.restype = ctypes.c_int
         L.dl_read_device_status.argtypes = [vp, vp, vp]
         _lib = L
@@ -170,21 +177,24 @@ def stats_to_host(stats: torch.Tensor) -> dict:
 
 def pseudograd_stats(theta_g, replicas, frag: Fragment, clip_sigmas=6.0, stats=None,
                      workspace=None, stream=None):
-    K = len(replicas)
+    """replicas=None: values mode (statistics of theta_g itself, K = 1)."""
+    K = 1 if replicas is None else len(replicas)
     if stats is None:
         stats = new_stats(K, frag.T, theta_g.device)
     need = stats_workspace_bytes(frag, K)
     if workspace is None:
         workspace = new_workspace(need, theta_g.device)
     _check("dl_pseudograd_stats", lib().dl_pseudograd_stats(
-        _ptr(theta_g), _ptr_array(replicas), K, frag.c, float(clip_sigmas), _ptr(stats),
+        _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
+        float(clip_sigmas), _ptr(stats),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return stats
 
 
 def quantize(theta_g, replicas, frag: Fragment, stats, codes=None, codebook=None, counts=None,
              workspace=None, stream=None):
-    K = len(replicas)
+    """replicas=None: values mode (quantise theta_g itself, K = 1)."""
+    K = 1 if replicas is None else len(replicas)
     dev = theta_g.device
     if codes is None:
         codes = [torch.empty(frag.n, dtype=torch.uint8, device=dev) for _ in range(K)]
@@ -193,7 +203,8 @@ def quantize(theta_g, replicas, frag: Fragment, stats, codes=None, codebook=None
     if workspace is None:
         workspace = new_workspace(quantize_workspace_bytes(frag, K), dev)
     _check("dl_quantize", lib().dl_quantize(
-        _ptr(theta_g), _ptr_array(replicas), K, frag.c, _ptr(stats), _ptr_array(codes),
+        _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
+        _ptr(stats), _ptr_array(codes),
         _ptr(codebook), _ptr(counts), _ptr(workspace), workspace.numel(), _stream(stream)))
     return codes, codebook
 
@@ -261,6 +272,27 @@ def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=No
         arr, len(frags), K, float(clip_sigmas), int(min_quorum), float(lr), float(mu), int(flags),
         _ptr(workspace), nbytes, _stream(stream)))
     del keep
+    return workspace
+
+
+def ring_workspace_bytes(frag: Fragment) -> int:
+    return int(lib().dl_ring_workspace_bytes(frag.c))
+
+
+def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, present=None,
+                    min_quorum=1, clip_sigmas=6.0, lr=0.7, mu=0.9, delta_bar=None,
+                    workspace=None, stream=None):
+    """Ring accumulation with re-quantisation at every hop, then the outer
+    step (dl_ring_outer_step); theta_g and momentum are updated in place."""
+    if workspace is None:
+        workspace = new_workspace(ring_workspace_bytes(frag), theta_g.device)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
+    p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    _check("dl_ring_outer_step", lib().dl_ring_outer_step(
+        _ptr(theta_g), _ptr(momentum), _ptr_array(replicas), len(replicas), frag.c,
+        None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
+        int(min_quorum), float(clip_sigmas), float(lr), float(mu), _ptr(delta_bar),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
 
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdiloco_sync.so")
-SOURCES = ["dl_host.cu", "dl_stats.cu", "dl_quantize.cu", "dl_merge.cu", "dl_sync.cu"]
+SOURCES = ["dl_host.cu", "dl_stats.cu", "dl_quantize.cu", "dl_merge.cu", "dl_sync.cu", "dl_ring.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

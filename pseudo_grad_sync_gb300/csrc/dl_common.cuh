@@ -175,7 +175,8 @@ __device__ __forceinline__ void consumer_sync() {
 }
 
 // Producer side: lane 0 of the producer warp issues the bulk copies of tile
-// number `it` (its stage is it % STAGES) covering [tb, tb + tn) of two arrays.
+// number `it` (its stage is it % STAGES) covering [tb, tb + tn) of two arrays
+// (of one when gb is null: values mode, the second array is never staged).
 template <int TILE, int STAGES>
 __device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float* sb, const float* ga,
                                              const float* gb, int64_t tb, int tn, uint32_t it,
@@ -184,10 +185,10 @@ __device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float*
     if (it >= STAGES) wait_or_flag(&pb->empty[s], ((it / STAGES) - 1) & 1u, status);
     const uint32_t bytes = static_cast<uint32_t>(tn >> 2) * 16u;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&pb->full[s], 2u * bytes);
+    mbar_arrive_expect_tx(&pb->full[s], gb ? 2u * bytes : bytes);
     if (bytes) {
         bulk_copy_g2s(sa + s * TILE, ga + tb, bytes, &pb->full[s]);
-        bulk_copy_g2s(sb + s * TILE, gb + tb, bytes, &pb->full[s]);
+        if (gb) bulk_copy_g2s(sb + s * TILE, gb + tb, bytes, &pb->full[s]);
     }
 }
 

@@ -136,6 +136,8 @@ __device__ __forceinline__ void flush_bin(const QuantArgs& a, int k, int t, int 
     l2[kNB + b] = 0ull;
 }
 
+// VALUES: values mode (no replica; Delta is theta_g itself, K = 1)
+template <bool VALUES>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     __shared__ uint32_t l1[2][2 * kNB];             // [parity][word A bins | word B bins]
     __shared__ unsigned long long l2[2 * kNB];       // [count bins | residual-sum bins]
@@ -188,7 +190,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
 #pragma unroll
                     for (int q = 0; q < kGroups / 2; ++q) gv[q] = __ldg(g4 + tid + (h + q) * kThreads);
 #pragma unroll
-                    for (int q = 0; q < kGroups / 2; ++q) rv[q] = __ldcs(r4 + tid + (h + q) * kThreads);
+                    for (int q = 0; q < kGroups / 2; ++q)
+                        rv[q] = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : __ldcs(r4 + tid + (h + q) * kThreads);
                     if (p.q.kind == kSegFast) {
 #pragma unroll
                         for (int q = 0; q < kGroups / 2; ++q) {
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                 }
             } else {
                 for (int64_t e = pa + tid; e < pb; e += kThreads) {
-                    const float d = __fsub_rn(__ldg(g + e), __ldcs(rk + e));
+                    const float d = __fsub_rn(__ldg(g + e), VALUES ? 0.f : __ldcs(rk + e));
                     ck[e] = static_cast<uint8_t>(encode_one(d, p, hA));
                 }
             }
@@ -287,7 +291,8 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     HostFrag f;
     int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
-    if (K <= 0 || K > DL_MAX_LEARNERS || !theta_k || !codes) return DL_ERR_ARG;
+    const bool values = theta_k == nullptr;  // Delta is theta_g itself
+    if (K <= 0 || K > DL_MAX_LEARNERS || (values && K != 1) || !codes) return DL_ERR_ARG;
     if (f.T == 0) return DL_OK;
     if (!d_stats || !d_codebook) return DL_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(d_stats) & 7u) != 0 || !aligned16(d_codebook) ||
@@ -297,8 +302,8 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
         if (!theta_g) return DL_ERR_ARG;
         if (!aligned16(theta_g)) return DL_ERR_ALIGN;
         for (int k = 0; k < K; ++k) {
-            if (!theta_k[k] || !codes[k]) return DL_ERR_ARG;
-            if (!aligned16(theta_k[k]) || !aligned16(codes[k])) return DL_ERR_ALIGN;
+            if ((!values && !theta_k[k]) || !codes[k]) return DL_ERR_ARG;
+            if ((!values && !aligned16(theta_k[k])) || !aligned16(codes[k])) return DL_ERR_ALIGN;
         }
     }
     const size_t need = dl_quantize_workspace_bytes(frag, K);
@@ -309,7 +314,7 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     memset(&a, 0, sizeof(a));
     a.g = theta_g;
     for (int k = 0; k < K; ++k) {
-        a.r[k] = theta_k[k];
+        a.r[k] = values ? nullptr : theta_k[k];
         a.codes[k] = codes[k];
     }
     a.off = f.d_offsets;
@@ -331,8 +336,13 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     k_qparams<<<(segs + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        a.J = blocks_per_learner(reinterpret_cast<const void*>(k_quantize), kThreads, 0, K, a.n_chunks);
-        k_quantize<<<K * a.J, kThreads, 0, s>>>(a);
+        const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true>)
+                                  : reinterpret_cast<const void*>(k_quantize<false>);
+        a.J = blocks_per_learner(kern, kThreads, 0, K, a.n_chunks);
+        if (values)
+            k_quantize<true><<<K * a.J, kThreads, 0, s>>>(a);
+        else
+            k_quantize<false><<<K * a.J, kThreads, 0, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     const int64_t cells = static_cast<int64_t>(K) * f.T * kNB;

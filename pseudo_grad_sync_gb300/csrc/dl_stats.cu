@@ -66,8 +66,11 @@ __global__ void __launch_bounds__(kThreads) k_shift(StatsArgs a) {
     const int64_t N = a.off[t + 1] - o;
     const int m = N < 64 ? static_cast<int>(N) : 64;
     const bool h0 = lane < m, h1 = lane + 32 < m;
-    const double v0 = h0 ? static_cast<double>(__fsub_rn(a.g[o + lane], a.r[k][o + lane])) : 0.0;
-    const double v1 = h1 ? static_cast<double>(__fsub_rn(a.g[o + lane + 32], a.r[k][o + lane + 32])) : 0.0;
+    const float* rk = a.r[k];  // null: values mode, Delta = theta_g itself
+    const double v0 =
+        h0 ? static_cast<double>(__fsub_rn(a.g[o + lane], rk ? rk[o + lane] : 0.f)) : 0.0;
+    const double v1 =
+        h1 ? static_cast<double>(__fsub_rn(a.g[o + lane + 32], rk ? rk[o + lane + 32] : 0.f)) : 0.0;
     double s = v0 + v1;
     for (int sh = 16; sh; sh >>= 1) s += __shfl_xor_sync(kFull, s, sh);
     const double mean = m > 0 ? s / m : 0.0;
@@ -230,6 +233,7 @@ __device__ __forceinline__ float absmax_nan(float a, float b) {
     return r;
 }
 
+template <bool VALUES>
 __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float* tr, int tid,
                                          float csh) {
     float y[kGroupsPerTile][4];
@@ -237,7 +241,8 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
 #pragma unroll
     for (int q = 0; q < kGroupsPerTile; ++q) {
         const float4 gv = reinterpret_cast<const float4*>(tg)[tid + q * kThreads];
-        const float4 rv = reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
+        const float4 rv = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                 : reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
         y[q][0] = __fsub_rn(__fsub_rn(gv.x, rv.x), csh);
         y[q][1] = __fsub_rn(__fsub_rn(gv.y, rv.y), csh);
         y[q][2] = __fsub_rn(__fsub_rn(gv.z, rv.z), csh);
@@ -263,7 +268,8 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
 #pragma unroll 1
         for (int q = 0; q < kGroupsPerTile; ++q) {
             const float4 gv = reinterpret_cast<const float4*>(tg)[tid + q * kThreads];
-            const float4 rv = reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
+            const float4 rv = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                     : reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
             side_add(__fsub_rn(gv.x, rv.x), csh, acc.s1d, acc.s2d, acc.bad);
             side_add(__fsub_rn(gv.y, rv.y), csh, acc.s1d, acc.s2d, acc.bad);
             side_add(__fsub_rn(gv.z, rv.z), csh, acc.s1d, acc.s2d, acc.bad);
@@ -283,7 +289,8 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
 // per SM, and 2 stages with 3 blocks per SM (the same bytes in flight, more
 // consumer warps; faster when K is small and every element-learner brings
 // a theta_g value from HBM).
-template <int STAGES, int MINB>
+// VALUES: values mode (no replica; Delta is theta_g itself, K = 1)
+template <int STAGES, int MINB, bool VALUES>
 __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     constexpr int kStages = STAGES;
     extern __shared__ __align__(128) float smem[];  // [kStages][kTile] theta_g, then theta_k
@@ -347,12 +354,12 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                     acc.reset();
                 }
                 if (pa == tb && pe == tb + kTile && !small) {
-                    add_tile(acc, tg, tr, tid, csh);
+                    add_tile<VALUES>(acc, tg, tr, tid, csh);
                 } else {
                     for (int64_t e = pa + tid; e < pe; e += kThreads) {
                         const int l = static_cast<int>(e - tb);
                         const float gv = l < tvec ? tg[l] : __ldg(g + e);
-                        const float rv = l < tvec ? tr[l] : __ldg(rk + e);
+                        const float rv = VALUES ? 0.f : (l < tvec ? tr[l] : __ldg(rk + e));
                         const float d = __fsub_rn(gv, rv);
                         const float y = __fsub_rn(d, csh);
                         const float ay = fabsf(y);
@@ -443,7 +450,8 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     HostFrag f;
     int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
-    if (K <= 0 || K > DL_MAX_LEARNERS || !theta_k || !(clip_sigmas > 0.0) ||
+    const bool values = theta_k == nullptr;  // Delta is theta_g itself
+    if (K <= 0 || K > DL_MAX_LEARNERS || (values && K != 1) || !(clip_sigmas > 0.0) ||
         !(clip_sigmas < 1e300))
         return DL_ERR_ARG;
     if (f.T == 0) return DL_OK;
@@ -452,7 +460,7 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     if (f.n > 0) {
         if (!theta_g) return DL_ERR_ARG;
         if (!aligned16(theta_g)) return DL_ERR_ALIGN;
-        for (int k = 0; k < K; ++k) {
+        for (int k = 0; k < K && !values; ++k) {
             if (!theta_k[k]) return DL_ERR_ARG;
             if (!aligned16(theta_k[k])) return DL_ERR_ALIGN;
         }
@@ -464,7 +472,7 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     StatsArgs a;
     memset(&a, 0, sizeof(a));
     a.g = theta_g;
-    for (int k = 0; k < K; ++k) a.r[k] = theta_k[k];
+    for (int k = 0; k < K; ++k) a.r[k] = values ? nullptr : theta_k[k];
     a.off = f.d_offsets;
     char* ws = static_cast<char*>(d_workspace);
     a.status = reinterpret_cast<uint32_t*>(ws);
@@ -478,8 +486,10 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     a.clip = clip_sigmas;
     a.J = 1;
     const bool shallow = K <= 2;
-    const void* kern = shallow ? reinterpret_cast<const void*>(k_stats<2, 3>)
-                               : reinterpret_cast<const void*>(k_stats<3, 2>);
+    const void* kern =
+        shallow ? (values ? reinterpret_cast<const void*>(k_stats<2, 3, true>)
+                          : reinterpret_cast<const void*>(k_stats<2, 3, false>))
+                : reinterpret_cast<const void*>(k_stats<3, 2, false>);
     const size_t smem = sizeof(float) * 2 * (shallow ? 2 : 3) * kTile;
     if (a.n_chunks > 0) {
         if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -498,9 +508,10 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
         if (shallow)
-            k_stats<2, 3><<<K * a.J, kPipeThreads, smem, s>>>(a);
+            values ? k_stats<2, 3, true><<<K * a.J, kPipeThreads, smem, s>>>(a)
+                   : k_stats<2, 3, false><<<K * a.J, kPipeThreads, smem, s>>>(a);
         else
-            k_stats<3, 2><<<K * a.J, kPipeThreads, smem, s>>>(a);
+            k_stats<3, 2, false><<<K * a.J, kPipeThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     k_stats_fin<<<small_grid, kThreads, 0, s>>>(a);

@@ -228,3 +228,44 @@ def test_workspace_needs_never_decrease_with_K(L):
         q = [L.dl_quantize_workspace_bytes(fb, k) for k in range(1, 33)]
         assert all(a <= b for a, b in zip(s, s[1:])), s
         assert all(a <= b for a, b in zip(q, q[1:])), q
+
+
+def test_values_mode_needs_one_learner(L):
+    f, _o = _frag([0, 10, 30])
+    fb = ctypes.byref(f)
+    ws = L.dl_stats_workspace_bytes(fb, 2)
+    # theta_k NULL selects values mode, which is defined for K = 1 only
+    assert L.dl_pseudograd_stats(FAKE, None, 2, fb, 6.0, FAKE, FAKE, ws, None) == -1
+    wq = L.dl_quantize_workspace_bytes(fb, 2)
+    assert L.dl_quantize(FAKE, None, 2, fb, FAKE, _ptrs(FAKE, FAKE), FAKE, None, FAKE, wq,
+                         None) == -1
+    # K = 1 in values mode passes validation and stops at the short workspace
+    assert L.dl_pseudograd_stats(FAKE, None, 1, fb, 6.0, FAKE, FAKE, 0, None) == -6
+
+
+def _ring(L, fb, K, weights=None, present=None, min_quorum=1, ws=FAKE, nbytes=0):
+    w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+    p = None if present is None else np.ascontiguousarray(present, np.uint8)
+    return L.dl_ring_outer_step(FAKE, FAKE, _ptrs(*([FAKE] * K)), K, fb,
+                                None if w is None else w.ctypes.data,
+                                None if p is None else p.ctypes.data, min_quorum, 6.0, 0.7, 0.9,
+                                None, ws, nbytes, None)
+
+
+def test_ring_validation_and_quorum_rules(L):
+    f, _o = _frag([0, 100, 4000])
+    fb = ctypes.byref(f)
+    need = L.dl_ring_workspace_bytes(fb)
+    assert need >= 4000 * 5
+    assert _ring(L, fb, 0) == -1 and _ring(L, fb, 33) == -1
+    assert _ring(L, fb, 3, nbytes=need - 1) == -6       # valid otherwise: short workspace
+    assert _ring(L, fb, 3, ws=FAKE + 16, nbytes=need) == -2
+    rng = np.random.default_rng(8)
+    for _ in range(150):
+        K = int(rng.integers(1, 9))
+        w = rng.choice([0.0, 0.5, 1.0, 2.0, -1.0, np.inf], K, p=[.2, .3, .2, .2, .05, .05])
+        p = (rng.random(K) < 0.6).astype(np.uint8)
+        q = int(rng.integers(0, 5))
+        st_or, _ = oracle.merge_weights(w.astype(np.float32), p, K, q)
+        st = _ring(L, fb, K, w, p, q)
+        assert st == (st_or if st_or < 0 else -6), (w, p, q, st_or, st)
