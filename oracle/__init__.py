@@ -10,7 +10,9 @@ closed forms, the INTELLECT-1 worked example (section 3.2), brute force on
 tiny inputs, the bucket-mean optimality property (section 4.1 step 4), the
 code-space counterexample (section 4.2), the planner's LPT bound, and for the
 ring accumulation its reductions to the plain merge and its per-hop error
-bound.
+bound. One exception: ``rda_merge_outer_step`` is PARITY UNPINNED - the page
+names Radial-Directional Averaging without a formula, so its reading is
+checked only against the properties that define that reading.
 """
 from __future__ import annotations
 
@@ -63,6 +65,9 @@ def lib():
         L.oracle_merge_outer_step.restype = ctypes.c_int
         L.oracle_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
                                               f32, f32, vp]
+        L.oracle_rda_merge_outer_step.restype = ctypes.c_int
+        L.oracle_rda_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
+                                                  f32, f32, vp]
         L.oracle_ring_outer_step.restype = ctypes.c_int
         L.oracle_ring_outer_step.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f64, f32,
                                              f32, vp]
@@ -234,4 +239,28 @@ def ring_outer_step(theta_g, momentum, replicas, offsets=None, weights=None, pre
         g.ctypes.data, m.ctypes.data, _ptrs(reps), len(reps), off.ctypes.data, T,
         None if w is None else w.ctypes.data, None if p is None else p.ctypes.data, min_quorum,
         clip_sigmas, lr, mu, db.ctypes.data)
+    return st, g, m, db
+
+
+def rda_merge_outer_step(theta_g, momentum, codes, codebook, counts, offsets=None, weights=None,
+                         present=None, min_quorum=1, lr=0.7, mu=0.9):
+    """Radial-Directional Averaging merge of decoded values, then the outer
+    step (see oracle.c for the reading: no formula on the page; parity
+    unpinned). Returns (status, theta_g', momentum', delta_bar)."""
+    g = np.array(theta_g, dtype=np.float32, copy=True)
+    m = np.array(momentum, dtype=np.float32, copy=True)
+    off = _offsets(offsets, g.size)
+    T = len(off) - 1
+    codes = [np.ascontiguousarray(c, dtype=np.uint8) for c in codes]
+    K = len(codes)
+    cb = np.ascontiguousarray(codebook, dtype=np.float32)
+    cnt = np.ascontiguousarray(counts, dtype=np.uint32)
+    assert cb.size == K * T * NB and cnt.size == K * T * NB
+    w = None if weights is None else _f32(weights)
+    p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    db = np.empty_like(g)
+    st = lib().oracle_rda_merge_outer_step(
+        g.ctypes.data, m.ctypes.data, _ptrs(codes), cb.ctypes.data, cnt.ctypes.data, K,
+        off.ctypes.data, T, None if w is None else w.ctypes.data,
+        None if p is None else p.ctypes.data, min_quorum, lr, mu, db.ctypes.data)
     return st, g, m, db

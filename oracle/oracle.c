@@ -393,3 +393,71 @@ int oracle_ring_outer_step(float* theta_g, float* momentum, const float* const* 
     free(mean); free(sd); free(lo); free(hi);
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Radial-Directional Averaging merge (Decoupled DiLoCo note, architecture */
+/* item 4: the outer gradients' norms and directions are averaged apart).  */
+/* PARITY UNPINNED: the page gives no formula; the reading taken, per      */
+/* tensor t:                                                               */
+/*   n_k = ||v_k|| over t (v_k the decoded values of learner k),            */
+/*   r   = sum_k w_k n_k                  (radial: mean norm)               */
+/*   u   = sum_k (w_k / n_k) v_k          (directional: mean unit vector)   */
+/*   D   = r u / ||u||                                                      */
+/* Norms from the codebook and the bucket counts, sum_b count_b cb_b^2,    */
+/* in fp64; ||u||^2 summed over the tensor's elements in fp64. D is formed */
+/* in fp32 from scaled codebooks: c_k = (float)((w_k / n_k) r / ||u||),    */
+/* acc = acc + (float)(c_k * cb_k[code]) over present k ascending. A      */
+/* learner with n_k = 0 has no direction (c_k = 0); ||u|| = 0 gives D = 0. */
+
+int oracle_rda_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
+                                const float* codebook, const uint32_t* counts, int32_t K,
+                                const int64_t* offsets, int32_t T, const float* weights,
+                                const uint8_t* present, int32_t min_quorum, float lr, float mu,
+                                float* delta_bar_out) {
+    float w_hat[256];
+    if (K > 256) return OR_ERR_ARG;
+    int np = oracle_merge_weights(weights, present, K, min_quorum, w_hat);
+    if (np < 0) return np;
+    for (int32_t t = 0; t < T; ++t) {
+        const int64_t a = offsets[t], b = offsets[t + 1];
+        double nrm[256], coef[256];
+        double r = 0.0;
+        for (int32_t k = 0; k < K; ++k) {
+            nrm[k] = coef[k] = 0.0;
+            if (present && !present[k]) continue;
+            const float* cb = codebook + ((int64_t)k * T + t) * NB;
+            const uint32_t* cnt = counts + ((int64_t)k * T + t) * NB;
+            double ss = 0.0;
+            for (int j = 0; j < NB; ++j) ss += (double)cnt[j] * (double)cb[j] * (double)cb[j];
+            nrm[k] = sqrt(ss);
+            r += (double)w_hat[k] * nrm[k];
+            coef[k] = nrm[k] > 0.0 ? (double)w_hat[k] / nrm[k] : 0.0;
+        }
+        double uu = 0.0;
+        for (int64_t i = a; i < b; ++i) {
+            double x = 0.0;
+            for (int32_t k = 0; k < K; ++k) {
+                if (present && !present[k]) continue;
+                x += coef[k] * (double)codebook[((int64_t)k * T + t) * NB + codes[k][i]];
+            }
+            uu += x * x;
+        }
+        const double scale = uu > 0.0 ? r / sqrt(uu) : 0.0;
+        float c[256];
+        for (int32_t k = 0; k < K; ++k) c[k] = (float)(coef[k] * scale);
+        for (int64_t i = a; i < b; ++i) {
+            float acc = 0.0f;
+            for (int32_t k = 0; k < K; ++k) {
+                if (present && !present[k]) continue;
+                const float v = codebook[((int64_t)k * T + t) * NB + codes[k][i]];
+                acc = acc + c[k] * v;
+            }
+            const float m_new = fmaf(mu, momentum[i], acc);
+            const float g = fmaf(mu, m_new, acc);
+            if (delta_bar_out) delta_bar_out[i] = acc;
+            momentum[i] = m_new;
+            theta_g[i] = fmaf(-lr, g, theta_g[i]);
+        }
+    }
+    return OR_OK;
+}
