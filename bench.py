@@ -406,6 +406,75 @@ def run_ring(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def run_rda(args, rank, world, local):
+    """The outer step with the Radial-Directional Averaging merge: per fragment
+    dl_pseudograd_stats, dl_quantize (with bucket counts) and
+    dl_rda_merge_outer_step."""
+    import torch
+
+    import pseudo_grad_sync_gb300 as dl
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = synthetic.WORKLOADS[args.workload]()
+    K = wl.K
+    frag_of, load = dl.plan_fragments(wl.numels, wl.n_frags)
+    frags = fragment_tensors(wl, frag_of)
+    host = generate_host(wl, frags, pin=False)
+    run = DeviceRun(wl, frags, host, dev)
+    del host
+    max_t = max(F.T for F in run.F)
+    counts = torch.empty((K, max_t, 256), dtype=torch.int32, device=dev)
+    ws_r = dl.new_workspace(max(dl.rda_workspace_bytes(F, K) for F in run.F), dev)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in run.F]
+
+    def step(timed=False):
+        for f, F in enumerate(run.F):
+            if timed:
+                ev[f][0].record(stream)
+            dl.pseudograd_stats(run.g[f], run.reps[f], F, 6.0, run.stats, run.ws_s, stream)
+            dl.quantize(run.g[f], run.reps[f], F, run.stats, run.codes, run.codebook, counts,
+                        run.ws_q, stream)
+            dl.rda_merge_outer_step(run.g[f], run.m[f], F, run.codes, run.codebook, counts,
+                                    workspace=ws_r, stream=stream, K=K)
+            if timed:
+                ev[f][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(None)
+    clocks.start()
+    time.sleep(0.3)
+    tot = 0.0
+    for _ in range(args.steps):
+        step(timed=True)
+        torch.cuda.synchronize()
+        tot += sum(e[0].elapsed_time(e[1]) for e in ev)
+    clk = clocks.stop()
+    ms_per_step = tot / args.steps
+    peak, peak_kind = load_peaks()
+    ab = 11 * K + 24  # stats 4(K+1), quantise 4(K+1)+K, ||u|| pass K, merge K+16
+    gbs = ab * wl.n_elems / (ms_per_step / 1e3) / 1e9
+    out = {
+        "metric": "RDA outer-step params/s (stats + quantise + RDA merge + Nesterov)",
+        "value": world * wl.n_elems / (ms_per_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name + ": " + wl.description, "K": K,
+                   "fragments": wl.n_frags, "params": wl.n_elems, "mode": "rda"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "note": f"{ab} algorithmic B/elem per step; peak = {peak_kind} copy "
+                             "bandwidth"},
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * 10, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -691,8 +760,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--mode", choices=["outer", "ring"], default="outer",
-                    help="ring: accumulate along a ring, re-quantising at every hop")
+    ap.add_argument("--mode", choices=["outer", "ring", "rda"], default="outer",
+                    help="ring: accumulate along a ring, re-quantising at every hop; "
+                         "rda: Radial-Directional Averaging merge")
     args = ap.parse_args()
     rank, world, local = env_rank()
     if world > 1:
@@ -724,6 +794,8 @@ def main():
         run_learner(args, rank, world, local)
     elif args.mode == "ring":
         run_ring(args, rank, world, local)
+    elif args.mode == "rda":
+        run_rda(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

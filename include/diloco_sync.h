@@ -243,6 +243,36 @@ int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, double
                   int32_t min_quorum, float lr, float mu, int32_t flags, void* d_workspace,
                   size_t workspace_bytes, void* stream);
 
+/* Workspace bytes needed by dl_rda_merge_outer_step for this fragment and K
+ * (0 on a bad argument). */
+size_t dl_rda_workspace_bytes(const dl_fragment* frag, int32_t K);
+
+/*
+ * Radial-Directional Averaging merge, then the outer Nesterov step (Decoupled
+ * DiLoCo note, architecture item 4: the outer gradients' norms and directions
+ * are averaged apart instead of averaging the vectors). The page gives no
+ * formula; the reading implemented, per tensor t over the present learners
+ * k with normalised weights w_k (as for the merge) and decoded values v_k:
+ *   n_k = ||v_k||  (from the codebook and the bucket counts, fp64)
+ *   r   = sum_k w_k n_k                         radial: mean norm
+ *   u   = sum_k (w_k / n_k) v_k                 directional: mean unit vector
+ *   D   = r u / ||u||   formed in fp32 as sum_k fl(c_k * v_k), ascending k,
+ *         with c_k = (float)((w_k / n_k) r / ||u||); c_k = 0 when n_k = 0,
+ *         D = 0 when ||u|| = 0
+ * then m' = fmaf(mu, m, D); g = fmaf(mu, m', D); theta' = fmaf(-lr, g, theta).
+ *   codes, d_codebook  as for dl_merge_outer_step (quantised mode only)
+ *   d_counts    device [K*T*256] uint32 bucket populations from dl_quantize
+ *   d_workspace device scratch of dl_rda_workspace_bytes(frag, K) bytes
+ * Weights, present, min_quorum, lr, mu, delta_bar_out and the errors are as
+ * for dl_merge_outer_step.
+ */
+int dl_rda_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
+                            const float* d_codebook, const uint32_t* d_counts, int32_t K,
+                            const dl_fragment* frag, const float* weights,
+                            const uint8_t* present, int32_t min_quorum, float lr, float mu,
+                            float* delta_bar_out, void* d_workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Workspace bytes needed by dl_ring_outer_step for this fragment (0 on a bad
  * fragment); independent of K. */
 size_t dl_ring_workspace_bytes(const dl_fragment* frag);

@@ -8,6 +8,7 @@ C entry points (see include/diloco_sync.h) keep their names here:
     pseudograd_stats     per-(learner, tensor) mu / sigma / clip range
     quantize             uint8 codes + bucket-mean codebooks
     merge_outer_step     decode, weighted fp32 mean, outer Nesterov (in place)
+    rda_merge_outer_step Radial-Directional Averaging merge, then the outer step
     ring_outer_step      ring accumulation re-quantised at every hop, then the
                          outer step (measures the error growth of a ring)
     outer_sync           the three calls over every fragment of a model, with
@@ -81,6 +82,11 @@ def lib():
         L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32]
         L.dl_outer_sync.restype = ctypes.c_int
         L.dl_outer_sync.argtypes = [jb, i32, i32, f64, i32, f32, f32, i32, vp, sz, vp]
+        L.dl_rda_workspace_bytes.restype = sz
+        L.dl_rda_workspace_bytes.argtypes = [fr, i32]
+        L.dl_rda_merge_outer_step.restype = ctypes.c_int
+        L.dl_rda_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, fr, vp, vp, i32, f32, f32,
+                                              vp, vp, sz, vp]
         L.dl_ring_workspace_bytes.restype = sz
         L.dl_ring_workspace_bytes.argtypes = [fr]
         L.dl_ring_outer_step.restype = ctypes.c_int
@@ -272,6 +278,29 @@ def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=No
         arr, len(frags), K, float(clip_sigmas), int(min_quorum), float(lr), float(mu), int(flags),
         _ptr(workspace), nbytes, _stream(stream)))
     del keep
+    return workspace
+
+
+def rda_workspace_bytes(frag: Fragment, K: int) -> int:
+    return int(lib().dl_rda_workspace_bytes(frag.c, K))
+
+
+def rda_merge_outer_step(theta_g, momentum, frag: Fragment, codes, codebook, counts, weights=None,
+                         present=None, min_quorum=1, lr=0.7, mu=0.9, delta_bar=None,
+                         workspace=None, stream=None, K=None):
+    """Radial-Directional Averaging merge of decoded values, then the outer
+    step (dl_rda_merge_outer_step); counts as written by quantize()."""
+    if K is None:
+        K = len(codes)
+    if workspace is None:
+        workspace = new_workspace(rda_workspace_bytes(frag, K), theta_g.device)
+    w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
+    p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    _check("dl_rda_merge_outer_step", lib().dl_rda_merge_outer_step(
+        _ptr(theta_g), _ptr(momentum), _ptr_array(codes), _ptr(codebook), _ptr(counts), K,
+        frag.c, None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
+        int(min_quorum), float(lr), float(mu), _ptr(delta_bar), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return workspace
 
 

@@ -2,7 +2,7 @@
 // Nesterov step in place (INTELLECT-1 notes, section 3.2 steps 6-7 and
 // section 4.2; Decoupled DiLoCo note, fault-tolerance items 1 and 3).
 //
-// k_merge_q<NPM>  persistent blocks over 8192-element chunks. The codebooks
+// k_merge_q<NPM, RDA> persistent blocks over 8192-element chunks. The codebooks
 //                 of the present learners for the current tensor sit in
 //                 shared memory (NPM x 1 KB at most); per 4-element group a
 //                 thread issues one 32-bit code load per present learner plus
@@ -13,6 +13,21 @@
 //                 once.
 // k_merge_u       the unquantised variant: values are the fp32 Delta_k read
 //                 from the learner replicas.
+//
+// Radial-Directional Averaging (Decoupled DiLoCo note, architecture item 4:
+// the outer gradients' norms and directions are averaged apart; the page has
+// no formula, the reading is stated with dl_rda_merge_outer_step). Per tensor:
+// k_rda_norms     one warp per tensor: each present learner's norm from its
+//                 codebook and bucket counts (fp64), the weighted mean norm r
+//                 and the direction coefficients w_k / n_k;
+// k_rda_u         one pass over the codes: ||u||^2 of u = sum_k (w_k/n_k) v_k,
+//                 one fp64 partial per warp and (chunk, tensor) piece, in
+//                 slots (chunk + tensor) * 8 + warp (unique, so no clearing
+//                 and a fixed order);
+// k_rda_coef      one block per tensor: fixed-order sum of its partials, then
+//                 c_k = (w_k / n_k) r / ||u|| per learner;
+// k_merge_q<NPM, true> then decodes through codebooks scaled by c_k and adds
+//                 the values in fp32 in ascending k.
 #include <math.h>
 
 #include "dl_common.cuh"
@@ -36,6 +51,7 @@ struct MergeArgs {
     int T;
     float lr;
     float mu;
+    const float* rda_c;  // RDA: [np][T] codebook scales (else unused)
 };
 
 __device__ __forceinline__ void outer_update(float acc, float& th, float& mm, float lr, float mu) {
@@ -45,7 +61,7 @@ __device__ __forceinline__ void outer_update(float acc, float& th, float& mm, fl
     mm = m1;
 }
 
-template <int NPM>
+template <int NPM, bool RDA>
 __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
     extern __shared__ float scb[];  // [np][256]
     const int tid = threadIdx.x;
@@ -63,8 +79,11 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
             if (pa >= pb) continue;
             if (t != cur_t) {
                 __syncthreads();
-                for (int i = tid; i < np * kNB; i += kThreads)
-                    scb[i] = __ldg(a.cb + (static_cast<int64_t>(a.kidx[i >> 8]) * a.T + t) * kNB + (i & (kNB - 1)));
+                for (int i = tid; i < np * kNB; i += kThreads) {
+                    float v = __ldg(a.cb + (static_cast<int64_t>(a.kidx[i >> 8]) * a.T + t) * kNB + (i & (kNB - 1)));
+                    if (RDA) v = __fmul_rn(__ldg(a.rda_c + (i >> 8) * a.T + t), v);
+                    scb[i] = v;
+                }
                 __syncthreads();
                 cur_t = t;
             }
@@ -94,10 +113,17 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
                                 const float* cbs = scb + s * kNB;
                                 const uint32_t w4 = cw[u][s];
                                 const float ws = a.w[s];
-                                a0 = __fmaf_rn(ws, cbs[w4 & 255u], a0);
-                                a1 = __fmaf_rn(ws, cbs[(w4 >> 8) & 255u], a1);
-                                a2 = __fmaf_rn(ws, cbs[(w4 >> 16) & 255u], a2);
-                                a3 = __fmaf_rn(ws, cbs[w4 >> 24], a3);
+                                if (RDA) {  // values already scaled
+                                    a0 = __fadd_rn(a0, cbs[w4 & 255u]);
+                                    a1 = __fadd_rn(a1, cbs[(w4 >> 8) & 255u]);
+                                    a2 = __fadd_rn(a2, cbs[(w4 >> 16) & 255u]);
+                                    a3 = __fadd_rn(a3, cbs[w4 >> 24]);
+                                } else {
+                                    a0 = __fmaf_rn(ws, cbs[w4 & 255u], a0);
+                                    a1 = __fmaf_rn(ws, cbs[(w4 >> 8) & 255u], a1);
+                                    a2 = __fmaf_rn(ws, cbs[(w4 >> 16) & 255u], a2);
+                                    a3 = __fmaf_rn(ws, cbs[w4 >> 24], a3);
+                                }
                             }
                         }
                         const int gi = tid + (j + u) * kThreads;
@@ -114,8 +140,10 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
             } else {
                 for (int64_t i = pa + tid; i < pb; i += kThreads) {
                     float acc = 0.f;
-                    for (int s = 0; s < np; ++s)
-                        acc = __fmaf_rn(a.w[s], scb[s * kNB + a.cp[s][i]], acc);
+                    for (int s = 0; s < np; ++s) {
+                        const float v = scb[s * kNB + a.cp[s][i]];
+                        acc = RDA ? __fadd_rn(acc, v) : __fmaf_rn(a.w[s], v, acc);
+                    }
                     float th = a.g[i], mm = a.m[i];
                     outer_update(acc, th, mm, a.lr, a.mu);
                     a.g[i] = th;
@@ -165,12 +193,141 @@ __global__ void __launch_bounds__(kThreads) k_merge_u(MergeArgs a) {
     }
 }
 
-template <int NPM>
+template <int NPM, bool RDA>
 int launch_q(const MergeArgs& a, cudaStream_t s) {
     const size_t smem = sizeof(float) * kNB * a.np;
-    const int grid = grid_for(reinterpret_cast<const void*>(k_merge_q<NPM>), kThreads, smem, a.n_chunks);
-    k_merge_q<NPM><<<grid, kThreads, smem, s>>>(a);
+    const int grid =
+        grid_for(reinterpret_cast<const void*>(k_merge_q<NPM, RDA>), kThreads, smem, a.n_chunks);
+    k_merge_q<NPM, RDA><<<grid, kThreads, smem, s>>>(a);
     return launch_status();
+}
+
+template <bool RDA>
+int launch_quantised(const MergeArgs& a, cudaStream_t s) {
+    if (a.np <= 4) return launch_q<4, RDA>(a, s);
+    if (a.np <= 8) return launch_q<8, RDA>(a, s);
+    if (a.np <= 16) return launch_q<16, RDA>(a, s);
+    return launch_q<32, RDA>(a, s);
+}
+
+// ---------------------------------------------------------------------------
+// RDA kernels
+
+struct RdaArgs {
+    const float* cb;          // [K][T][256]
+    const uint32_t* counts;   // [K][T][256]
+    const uint8_t* cp[DL_MAX_LEARNERS];
+    int kidx[DL_MAX_LEARNERS];
+    float w[DL_MAX_LEARNERS];
+    int np;
+    int T;
+    const int64_t* off;
+    int64_t n;
+    int64_t n_chunks;
+    double* coef;  // [np][T]  w_k / n_k
+    double* r;     // [T]      sum_k w_k n_k
+    double* part;  // [(n_chunks + T) * 8] ||u||^2 per piece and warp
+    float* c;      // [np][T]  final codebook scales
+};
+
+__global__ void __launch_bounds__(kThreads) k_rda_norms(RdaArgs a) {
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    double rr = 0.0;
+    for (int s = 0; s < a.np; ++s) {
+        const int64_t base = (static_cast<int64_t>(a.kidx[s]) * a.T + t) * kNB;
+        double ss = 0.0;
+#pragma unroll
+        for (int j = 0; j < kNB / 32; ++j) {
+            const int b = lane * (kNB / 32) + j;
+            const double v = static_cast<double>(__ldg(a.cb + base + b));
+            ss = fma(static_cast<double>(__ldg(a.counts + base + b)) * v, v, ss);
+        }
+        for (int sh = 16; sh; sh >>= 1) ss += __shfl_xor_sync(kFull, ss, sh);
+        const double nrm = sqrt(ss);
+        rr = fma(static_cast<double>(a.w[s]), nrm, rr);
+        if (lane == 0) a.coef[s * a.T + t] = nrm > 0.0 ? static_cast<double>(a.w[s]) / nrm : 0.0;
+    }
+    if (lane == 0) a.r[t] = rr;
+}
+
+__global__ void __launch_bounds__(kThreads) k_rda_u(RdaArgs a) {
+    extern __shared__ float scu[];  // [np][256] codebooks scaled by w_k / n_k
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int np = a.np;
+    int cur_t = -1;
+    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+        const int64_t base = c * kChunk;
+        const int64_t cend = min(base + static_cast<int64_t>(kChunk), a.n);
+        for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
+            const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+            if (o0 >= cend) break;
+            const int64_t pa = o0 > base ? o0 : base;
+            const int64_t pb = o1 < cend ? o1 : cend;
+            if (pa >= pb) continue;
+            if (t != cur_t) {
+                __syncthreads();
+                for (int i = tid; i < np * kNB; i += kThreads) {
+                    const int s = i >> 8;
+                    const float v = __ldg(a.cb + (static_cast<int64_t>(a.kidx[s]) * a.T + t) * kNB + (i & (kNB - 1)));
+                    scu[i] = __fmul_rn(static_cast<float>(a.coef[s * a.T + t]), v);
+                }
+                __syncthreads();
+                cur_t = t;
+            }
+            // squares of x = sum_k coef_k v_k, four at a time in fp32, then fp64
+            double acc = 0.0;
+            if (pa == base && pb == base + kChunk) {  // 32-bit code words, 4 elements each
+#pragma unroll 2
+                for (int j = 0; j < kGroups; ++j) {
+                    const int gi = tid + j * kThreads;
+                    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+                    for (int s = 0; s < np; ++s) {
+                        const uint32_t w4 =
+                            __ldcs(reinterpret_cast<const unsigned int*>(a.cp[s] + base) + gi);
+                        const float* cs = scu + s * kNB;
+                        x0 = __fadd_rn(x0, cs[w4 & 255u]);
+                        x1 = __fadd_rn(x1, cs[(w4 >> 8) & 255u]);
+                        x2 = __fadd_rn(x2, cs[(w4 >> 16) & 255u]);
+                        x3 = __fadd_rn(x3, cs[w4 >> 24]);
+                    }
+                    const float q = __fmaf_rn(x3, x3, __fmaf_rn(x2, x2, __fmaf_rn(x1, x1, __fmul_rn(x0, x0))));
+                    acc += static_cast<double>(q);
+                }
+            } else {
+                for (int64_t i = pa + tid; i < pb; i += kThreads) {
+                    float x = 0.f;
+                    for (int s = 0; s < np; ++s) x = __fadd_rn(x, scu[s * kNB + a.cp[s][i]]);
+                    acc += static_cast<double>(__fmul_rn(x, x));
+                }
+            }
+            for (int sh = 16; sh; sh >>= 1) acc += __shfl_xor_sync(kFull, acc, sh);
+            if (lane == 0) a.part[(c + t) * kWarps + warp] = acc;
+        }
+    }
+}
+
+// one block per tensor: its pieces' per-warp partials summed in a fixed order
+__global__ void __launch_bounds__(kThreads) k_rda_coef(RdaArgs a) {
+    __shared__ double red[kThreads];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const int64_t o0 = a.off[t], o1 = a.off[t + 1];
+    double uu = 0.0;
+    if (o1 > o0) {
+        const int64_t s0 = (o0 / kChunk + t) * kWarps, s1 = ((o1 - 1) / kChunk + t + 1) * kWarps;
+        for (int64_t i = s0 + tid; i < s1; i += kThreads) uu += a.part[i];
+    }
+    red[tid] = uu;
+    __syncthreads();
+    for (int h = kThreads / 2; h > 0; h >>= 1) {
+        if (tid < h) red[tid] += red[tid + h];
+        __syncthreads();
+    }
+    uu = red[0];
+    const double scale = uu > 0.0 ? a.r[t] / sqrt(uu) : 0.0;
+    for (int s = tid; s < a.np; s += kThreads)
+        a.c[s * a.T + t] = static_cast<float>(a.coef[s * a.T + t] * scale);
 }
 
 }  // namespace
@@ -178,11 +335,16 @@ int launch_q(const MergeArgs& a, cudaStream_t s) {
 
 using namespace dl;
 
-extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
-                                   const float* d_codebook, const float* const* theta_k, int32_t K,
-                                   const dl_fragment* frag, const float* weights,
-                                   const uint8_t* present, int32_t min_quorum, float lr, float mu,
-                                   float* delta_bar_out, void* stream) {
+namespace dl {
+namespace {
+
+// Validation shared by the merges: quorum and weight normalisation over the
+// present learners (fp64, then fp32), pointers and alignment; fills `a`.
+// Returns DL_OK with a.n == 0 for an empty fragment (nothing to launch).
+int prepare_merge(MergeArgs& a, float* theta_g, float* momentum, const uint8_t* const* codes,
+                  const float* d_codebook, const float* const* theta_k, int32_t K,
+                  const dl_fragment* frag, const float* weights, const uint8_t* present,
+                  int32_t min_quorum, float lr, float mu, float* delta_bar_out) {
     HostFrag f;
     int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
@@ -190,8 +352,6 @@ extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_
     const bool quant = codes != nullptr;
     if (!quant && !theta_k) return DL_ERR_ARG;
 
-    // quorum and weight normalisation over the present learners (fp64, then fp32)
-    MergeArgs a;
     memset(&a, 0, sizeof(a));
     double total = 0.0;
     int np = 0;
@@ -210,6 +370,7 @@ extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_
         a.w[s] = static_cast<float>(w / total);
     }
     a.np = np;
+    a.T = f.T;
     if (f.n == 0) return DL_OK;
 
     if (!theta_g || !momentum) return DL_ERR_ARG;
@@ -238,18 +399,103 @@ extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_
     a.dbar = delta_bar_out;
     a.n = f.n;
     a.n_chunks = n_chunks_of(f.n);
-    a.T = f.T;
     a.lr = lr;
     a.mu = mu;
+    return DL_OK;
+}
+
+struct RdaLayout {
+    size_t coef, r, part, c, total;
+};
+
+RdaLayout rda_layout(const HostFrag& f, int K) {
+    RdaLayout L;
+    L.coef = kWsHeader;
+    L.r = L.coef + align256(sizeof(double) * static_cast<size_t>(K) * f.T);
+    L.part = L.r + align256(sizeof(double) * static_cast<size_t>(f.T));
+    L.c = L.part + align256(sizeof(double) * kWarps * static_cast<size_t>(n_chunks_of(f.n) + f.T));
+    L.total = L.c + align256(sizeof(float) * static_cast<size_t>(K) * f.T);
+    return L;
+}
+
+}  // namespace
+}  // namespace dl
+
+extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
+                                   const float* d_codebook, const float* const* theta_k, int32_t K,
+                                   const dl_fragment* frag, const float* weights,
+                                   const uint8_t* present, int32_t min_quorum, float lr, float mu,
+                                   float* delta_bar_out, void* stream) {
+    MergeArgs a;
+    const int st = prepare_merge(a, theta_g, momentum, codes, d_codebook, theta_k, K, frag,
+                                 weights, present, min_quorum, lr, mu, delta_bar_out);
+    if (st != DL_OK || a.n == 0) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (!quant) {
+    if (codes == nullptr) {
         const int grid = grid_for(reinterpret_cast<const void*>(k_merge_u), kThreads, 0,
-                                  ((f.n >> 2) + kThreads - 1) / kThreads + 1);
+                                  ((a.n >> 2) + kThreads - 1) / kThreads + 1);
         k_merge_u<<<grid, kThreads, 0, s>>>(a);
         return launch_status();
     }
-    if (np <= 4) return launch_q<4>(a, s);
-    if (np <= 8) return launch_q<8>(a, s);
-    if (np <= 16) return launch_q<16>(a, s);
-    return launch_q<32>(a, s);
+    return launch_quantised<false>(a, s);
+}
+
+extern "C" size_t dl_rda_workspace_bytes(const dl_fragment* frag, int32_t K) {
+    HostFrag f;
+    if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
+    return rda_layout(f, K).total;
+}
+
+extern "C" int dl_rda_merge_outer_step(float* theta_g, float* momentum,
+                                       const uint8_t* const* codes, const float* d_codebook,
+                                       const uint32_t* d_counts, int32_t K,
+                                       const dl_fragment* frag, const float* weights,
+                                       const uint8_t* present, int32_t min_quorum, float lr,
+                                       float mu, float* delta_bar_out, void* d_workspace,
+                                       size_t workspace_bytes, void* stream) {
+    if (!codes) return DL_ERR_ARG;
+    MergeArgs a;
+    int st = prepare_merge(a, theta_g, momentum, codes, d_codebook, nullptr, K, frag, weights,
+                           present, min_quorum, lr, mu, delta_bar_out);
+    if (st != DL_OK) return st;
+    HostFrag f;
+    check_fragment(frag, &f);
+    const RdaLayout L = rda_layout(f, K);
+    if (a.n == 0) return DL_OK;
+    if (!d_counts) return DL_ERR_ARG;
+    if (!aligned16(d_counts)) return DL_ERR_ALIGN;
+    if (!d_workspace || workspace_bytes < L.total) return DL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0) return DL_ERR_ALIGN;
+
+    char* ws = static_cast<char*>(d_workspace);
+    RdaArgs r;
+    memset(&r, 0, sizeof(r));
+    r.cb = d_codebook;
+    r.counts = d_counts;
+    r.np = a.np;
+    for (int s = 0; s < a.np; ++s) {
+        r.cp[s] = a.cp[s];
+        r.kidx[s] = a.kidx[s];
+        r.w[s] = a.w[s];
+    }
+    r.T = f.T;
+    r.off = f.d_offsets;
+    r.n = f.n;
+    r.n_chunks = a.n_chunks;
+    r.coef = reinterpret_cast<double*>(ws + L.coef);
+    r.r = reinterpret_cast<double*>(ws + L.r);
+    r.part = reinterpret_cast<double*>(ws + L.part);
+    r.c = reinterpret_cast<float*>(ws + L.c);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    k_rda_norms<<<(f.T * 32 + kThreads - 1) / kThreads, kThreads, 0, s>>>(r);
+    if ((st = launch_status()) != DL_OK) return st;
+    const size_t smem = sizeof(float) * kNB * a.np;
+    const int grid = grid_for(reinterpret_cast<const void*>(k_rda_u), kThreads, smem, a.n_chunks);
+    k_rda_u<<<grid, kThreads, smem, s>>>(r);
+    if ((st = launch_status()) != DL_OK) return st;
+    k_rda_coef<<<f.T, kThreads, 0, s>>>(r);
+    if ((st = launch_status()) != DL_OK) return st;
+    a.rda_c = r.c;
+    return launch_quantised<true>(a, s);
 }

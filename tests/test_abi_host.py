@@ -269,3 +269,33 @@ def test_ring_validation_and_quorum_rules(L):
         st_or, _ = oracle.merge_weights(w.astype(np.float32), p, K, q)
         st = _ring(L, fb, K, w, p, q)
         assert st == (st_or if st_or < 0 else -6), (w, p, q, st_or, st)
+
+
+def test_rda_validation_and_quorum_rules(L):
+    f, _o = _frag([0, 100, 4000])
+    fb = ctypes.byref(f)
+    K = 3
+    need = L.dl_rda_workspace_bytes(fb, K)
+    assert need > 0 and L.dl_rda_workspace_bytes(fb, 0) == 0
+
+    def rda(K, weights=None, present=None, q=1, counts=FAKE, ws=FAKE, nbytes=0, codes=True):
+        w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+        p = None if present is None else np.ascontiguousarray(present, np.uint8)
+        return L.dl_rda_merge_outer_step(FAKE, FAKE, _ptrs(*([FAKE] * K)) if codes else None,
+                                         FAKE, counts, K, fb,
+                                         None if w is None else w.ctypes.data,
+                                         None if p is None else p.ctypes.data, q, 0.7, 0.9,
+                                         None, ws, nbytes, None)
+
+    assert rda(K, codes=False) == -1           # quantised mode only
+    assert rda(K, counts=None, nbytes=need) == -1
+    assert rda(K, counts=FAKE + 4, nbytes=need) == -2
+    assert rda(K, nbytes=need - 1) == -6
+    rng = np.random.default_rng(9)
+    for _ in range(100):
+        Kr = int(rng.integers(1, 9))
+        w = rng.choice([0.0, 0.5, 1.0, -1.0], Kr, p=[.2, .5, .25, .05])
+        p = (rng.random(Kr) < 0.6).astype(np.uint8)
+        q = int(rng.integers(0, 4))
+        st_or, _ = oracle.merge_weights(w.astype(np.float32), p, Kr, q)
+        assert rda(Kr, w, p, q) == (st_or if st_or < 0 else -6)
