@@ -52,6 +52,18 @@ def algo_bytes(K):
     return {"stats": 4 * (K + 1), "quantize": 4 * (K + 1) + K, "merge": K + 16}
 
 
+def max_over_ranks(value, world, device):
+    """The largest value over all ranks (timings: the job is as slow as its
+    slowest rank); the value itself on one rank."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def env_rank():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -298,9 +310,7 @@ def run_learner(args, rank, world, local):
     clk = clocks.stop()
     ms = start.elapsed_time(end)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
     peak, peak_kind = load_peaks()
     ab = {"stats": 8, "quantize": 9}
@@ -523,11 +533,7 @@ def run_ours(args, rank, world, local):
             body(s)
         end.record(stream)
         barrier()
-        ms = start.elapsed_time(end)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(start.elapsed_time(end), world, dev)
         return ms / args.steps
 
     # headline: the whole step through dl_outer_sync (consecutive fragments
@@ -658,9 +664,7 @@ def run_e2e(run, host, args, world, dev):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+        dt = max_over_ranks(dt, world, dev)
     return {"value": world * run.wl.n_elems * steps / dt, "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps,
             "ms_per_step": dt / steps * 1e3, "h2d_gbs": bi * steps / dt / 1e9,
