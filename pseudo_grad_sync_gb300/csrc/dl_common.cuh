@@ -193,6 +193,16 @@ __device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float*
 }
 
 // ---------------------------------------------------------------------------
+// Contiguous chunk range [c0, c1) of this block: the chunks split as evenly as
+// possible over the grid. A block then meets few tensors, so per-tensor
+// set-up (codebooks staged in shared memory) is rarely repeated.
+__device__ __forceinline__ void block_chunks(int64_t n_chunks, int64_t& c0, int64_t& c1) {
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    c0 = n_chunks * b / G;
+    c1 = n_chunks * (b + 1) / G;
+}
+
+// ---------------------------------------------------------------------------
 // Tensor lookup: smallest t with off[t+1] > pos (empty tensors are skipped).
 __device__ __forceinline__ int tensor_containing(const int64_t* __restrict__ off, int T,
                                                  int64_t pos) {

@@ -2,7 +2,10 @@
 // Nesterov step in place (INTELLECT-1 notes, section 3.2 steps 6-7 and
 // section 4.2; Decoupled DiLoCo note, fault-tolerance items 1 and 3).
 //
-// k_merge_q<NPM, RDA> persistent blocks over 8192-element chunks. The codebooks
+// k_merge_q<NPM, RDA> persistent blocks over 8192-element chunks (block b takes
+//                 chunks b, b + grid, ...: all blocks stay in one region of
+//                 the arrays, which measured faster than contiguous runs).
+//                 The codebooks
 //                 of the present learners for the current tensor sit in
 //                 shared memory (NPM x 1 KB at most); per 4-element group a
 //                 thread issues one 32-bit code load per present learner plus
@@ -17,10 +20,12 @@
 // Radial-Directional Averaging (Decoupled DiLoCo note, architecture item 4:
 // the outer gradients' norms and directions are averaged apart; the page has
 // no formula, the reading is stated with dl_rda_merge_outer_step). Per tensor:
-// k_rda_norms     one warp per tensor: each present learner's norm from its
+// k_rda_norms     one block per tensor: each present learner's norm from its
 //                 codebook and bucket counts (fp64), the weighted mean norm r
 //                 and the direction coefficients w_k / n_k;
-// k_rda_u         one pass over the codes: ||u||^2 of u = sum_k (w_k/n_k) v_k,
+// k_rda_u         one pass over the codes (each block over a contiguous run of
+//                 chunks, so it rescales codebooks rarely): ||u||^2 of
+//                 u = sum_k (w_k/n_k) v_k,
 //                 one fp64 partial per warp and (chunk, tensor) piece, in
 //                 slots (chunk + tensor) * 8 + warp (unique, so no clearing
 //                 and a fixed order);
@@ -230,12 +235,12 @@ struct RdaArgs {
     float* c;      // [np][T]  final codebook scales
 };
 
+// one block per tensor; warp w takes learners w, w + 8, ...
 __global__ void __launch_bounds__(kThreads) k_rda_norms(RdaArgs a) {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (t >= a.T) return;
-    double rr = 0.0;
-    for (int s = 0; s < a.np; ++s) {
+    __shared__ double nrm_s[DL_MAX_LEARNERS];
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int s = warp; s < a.np; s += kWarps) {
         const int64_t base = (static_cast<int64_t>(a.kidx[s]) * a.T + t) * kNB;
         double ss = 0.0;
 #pragma unroll
@@ -246,18 +251,28 @@ __global__ void __launch_bounds__(kThreads) k_rda_norms(RdaArgs a) {
         }
         for (int sh = 16; sh; sh >>= 1) ss += __shfl_xor_sync(kFull, ss, sh);
         const double nrm = sqrt(ss);
-        rr = fma(static_cast<double>(a.w[s]), nrm, rr);
-        if (lane == 0) a.coef[s * a.T + t] = nrm > 0.0 ? static_cast<double>(a.w[s]) / nrm : 0.0;
+        if (lane == 0) {
+            nrm_s[s] = nrm;
+            a.coef[s * a.T + t] = nrm > 0.0 ? static_cast<double>(a.w[s]) / nrm : 0.0;
+        }
     }
-    if (lane == 0) a.r[t] = rr;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double rr = 0.0;
+        for (int s = 0; s < a.np; ++s) rr = fma(static_cast<double>(a.w[s]), nrm_s[s], rr);
+        a.r[t] = rr;
+    }
 }
 
+template <int NPM>
 __global__ void __launch_bounds__(kThreads) k_rda_u(RdaArgs a) {
     extern __shared__ float scu[];  // [np][256] codebooks scaled by w_k / n_k
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int np = a.np;
     int cur_t = -1;
-    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    int64_t c0, c1;
+    block_chunks(a.n_chunks, c0, c1);
+    for (int64_t c = c0; c < c1; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + static_cast<int64_t>(kChunk), a.n);
         for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
@@ -276,36 +291,59 @@ __global__ void __launch_bounds__(kThreads) k_rda_u(RdaArgs a) {
                 __syncthreads();
                 cur_t = t;
             }
-            // squares of x = sum_k coef_k v_k, four at a time in fp32, then fp64
-            double acc = 0.0;
+            // squares of x = sum_k coef_k v_k, four at a time in fp32, summed per
+            // thread as a float-float pair (exact two-sums; fp64 is scarce on
+            // this part), then in fp64 once per piece
+            float ah = 0.f, al = 0.f;
             if (pa == base && pb == base + kChunk) {  // 32-bit code words, 4 elements each
-#pragma unroll 2
-                for (int j = 0; j < kGroups; ++j) {
-                    const int gi = tid + j * kThreads;
-                    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                    for (int s = 0; s < np; ++s) {
-                        const uint32_t w4 =
-                            __ldcs(reinterpret_cast<const unsigned int*>(a.cp[s] + base) + gi);
-                        const float* cs = scu + s * kNB;
-                        x0 = __fadd_rn(x0, cs[w4 & 255u]);
-                        x1 = __fadd_rn(x1, cs[(w4 >> 8) & 255u]);
-                        x2 = __fadd_rn(x2, cs[(w4 >> 16) & 255u]);
-                        x3 = __fadd_rn(x3, cs[w4 >> 24]);
+#pragma unroll 1
+                for (int j = 0; j < kGroups; j += 2) {
+                    uint32_t cw[2][NPM];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int s = 0; s < NPM; ++s)
+                            if (s < np)
+                                cw[u][s] = __ldcs(reinterpret_cast<const unsigned int*>(a.cp[s] + base) +
+                                                  tid + (j + u) * kThreads);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+                        for (int s = 0; s < NPM; ++s) {
+                            if (s < np) {
+                                const uint32_t w4 = cw[u][s];
+                                const float* cs = scu + s * kNB;
+                                x0 = __fadd_rn(x0, cs[w4 & 255u]);
+                                x1 = __fadd_rn(x1, cs[(w4 >> 8) & 255u]);
+                                x2 = __fadd_rn(x2, cs[(w4 >> 16) & 255u]);
+                                x3 = __fadd_rn(x3, cs[w4 >> 24]);
+                            }
+                        }
+                        ff_add(ah, al,
+                               __fmaf_rn(x3, x3, __fmaf_rn(x2, x2, __fmaf_rn(x1, x1, __fmul_rn(x0, x0)))));
                     }
-                    const float q = __fmaf_rn(x3, x3, __fmaf_rn(x2, x2, __fmaf_rn(x1, x1, __fmul_rn(x0, x0))));
-                    acc += static_cast<double>(q);
                 }
             } else {
                 for (int64_t i = pa + tid; i < pb; i += kThreads) {
                     float x = 0.f;
                     for (int s = 0; s < np; ++s) x = __fadd_rn(x, scu[s * kNB + a.cp[s][i]]);
-                    acc += static_cast<double>(__fmul_rn(x, x));
+                    ff_add(ah, al, __fmul_rn(x, x));
                 }
             }
+            double acc = static_cast<double>(ah) + static_cast<double>(al);
             for (int sh = 16; sh; sh >>= 1) acc += __shfl_xor_sync(kFull, acc, sh);
             if (lane == 0) a.part[(c + t) * kWarps + warp] = acc;
         }
     }
+}
+
+template <int NPM>
+int launch_rda_u(const RdaArgs& r, cudaStream_t s) {
+    const size_t smem = sizeof(float) * kNB * r.np;
+    const int grid = grid_for(reinterpret_cast<const void*>(k_rda_u<NPM>), kThreads, smem, r.n_chunks);
+    k_rda_u<NPM><<<grid, kThreads, smem, s>>>(r);
+    return launch_status();
 }
 
 // one block per tensor: its pieces' per-warp partials summed in a fixed order
@@ -488,12 +526,12 @@ extern "C" int dl_rda_merge_outer_step(float* theta_g, float* momentum,
     r.c = reinterpret_cast<float*>(ws + L.c);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    k_rda_norms<<<(f.T * 32 + kThreads - 1) / kThreads, kThreads, 0, s>>>(r);
+    k_rda_norms<<<f.T, kThreads, 0, s>>>(r);
     if ((st = launch_status()) != DL_OK) return st;
-    const size_t smem = sizeof(float) * kNB * a.np;
-    const int grid = grid_for(reinterpret_cast<const void*>(k_rda_u), kThreads, smem, a.n_chunks);
-    k_rda_u<<<grid, kThreads, smem, s>>>(r);
-    if ((st = launch_status()) != DL_OK) return st;
+    st = a.np <= 4 ? launch_rda_u<4>(r, s)
+         : a.np <= 8 ? launch_rda_u<8>(r, s)
+         : a.np <= 16 ? launch_rda_u<16>(r, s) : launch_rda_u<32>(r, s);
+    if (st != DL_OK) return st;
     k_rda_coef<<<f.T, kThreads, 0, s>>>(r);
     if ((st = launch_status()) != DL_OK) return st;
     a.rda_c = r.c;
