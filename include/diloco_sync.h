@@ -345,6 +345,17 @@ int dl_quantize_noalloc(const float* theta_g, const float* const* theta_k, int32
  */
 int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream);
 
+/*
+ * Self-test of the failure path of the bounded waits (a diagnostic; the pages
+ * have no counterpart). Launches one wait on a shared-memory barrier that
+ * nothing completes; after `polls` polls (1 .. 2^22) it gives up, sets the
+ * same bit in the workspace's status word that a stalled bulk copy would set,
+ * and returns - no trap, no hang, the context stays usable. Read the result
+ * with dl_read_device_status.
+ *   d_workspace  any workspace of this library (256-byte aligned)
+ */
+int dl_selftest_wait_timeout(void* d_workspace, int32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -92,6 +92,8 @@ def lib():
         L.dl_ring_outer_step.restype = ctypes.c_int
         L.dl_ring_outer_step.argtypes = [vp, vp, vp, i32, fr, vp, vp, i32, f64, f32, f32, vp, vp,
                                          sz, vp]
+        L.dl_selftest_wait_timeout.restype = ctypes.c_int
+        L.dl_selftest_wait_timeout.argtypes = [vp, i32, vp]
         L.dl_read_device_status.restype = ctypes.c_int
         L.dl_read_device_status.argtypes = [vp, vp, vp]
         _lib = L
@@ -323,6 +325,13 @@ def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, p
         int(min_quorum), float(clip_sigmas), float(lr), float(mu), _ptr(delta_bar),
         _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
+
+
+def selftest_wait_timeout(workspace, polls=1000, stream=None):
+    """Run one bounded wait that nothing completes (dl_selftest_wait_timeout);
+    the workspace's status word then reports it."""
+    _check("dl_selftest_wait_timeout",
+           lib().dl_selftest_wait_timeout(_ptr(workspace), int(polls), _stream(stream)))
 
 
 def read_device_status(workspace, stream=None) -> int:

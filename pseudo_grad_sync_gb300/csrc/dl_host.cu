@@ -137,3 +137,26 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? DL_OK : DL_ERR_CUDA; 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DL_OK : DL_ERR_CUDA; }
 
 }  // namespace dl
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded-wait failure path: one thread waits on a
+// shared-memory mbarrier that expects one arrival nobody makes, so the wait
+// runs out after `polls` polls; the kernel then records the failure in the
+// workspace status word, exactly as a stalled bulk copy would, and returns.
+namespace {
+__global__ void k_selftest_wait(uint32_t* status, long polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    dl::mbar_init(&bar, 1);
+    dl::fence_barrier_init();
+    if (!dl::mbar_wait_bounded(&bar, 0u, polls)) atomicOr(status, dl::kDevErrCopyTimeout);
+}
+}  // namespace
+
+extern "C" int dl_selftest_wait_timeout(void* d_workspace, int32_t polls, void* stream) {
+    if (!d_workspace || polls <= 0 || polls > dl::kSpinLimit) return DL_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0) return DL_ERR_ALIGN;
+    k_selftest_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint32_t*>(d_workspace), static_cast<long>(polls));
+    return dl::launch_status();
+}
