@@ -308,3 +308,63 @@ def test_learner_10b_whole_model():
     T = wl.n_tensors
     assert wl.numels[T - 5] == 4096 * 14336 and wl.numels[T - 2] == 4096
     _learner_whole_model(wl, {T - 1, T - 2, T - 5, 1})
+
+
+def test_ring_and_rda_on_a_full_decoder_1b_fragment():
+    """The largest multi-tensor 1.1B fragment (K=4) through the ring and the RDA
+    merge, as bench.py --mode ring / rda run it. Both work tensor by tensor,
+    so the sampled tensors are checked against the oracle on their own: the
+    ring end to end; RDA on the GPU's own codes, codebooks and counts (its
+    reading has no formula on the page, so it is held to the oracle's
+    reading on identical inputs)."""
+    import pseudo_grad_sync_gb300 as dl
+
+    wl = synthetic.decoder_1b()
+    frags, load = _plan(wl)
+    f = max((f for f, ts in enumerate(frags) if len(ts) > 1), key=lambda f: load[f])
+    ts = frags[f]
+    sampled = {_smallest(wl, ts), _smallest(wl, ts, "matrix")} - {None}
+    run = FragmentRun(wl, ts, sampled, gen_seed=9)
+    reps = run.replicas(0)
+    g0 = run.g.clone()
+    # ring
+    db = torch.empty_like(run.g)
+    dl.ring_outer_step(run.g, run.m, run.frag, reps, delta_bar=db)
+    torch.cuda.synchronize()
+    for t, h in run.host.items():
+        a, b = h["a"], h["b"]
+        rh = [(h["g"] - _delta_host(wl, t, k, 0)).astype(np.float32) for k in range(wl.K)]
+        st, g_o, m_o, d_o = oracle.ring_outer_step(h["g"], h["m"], rh)
+        d_g = db[a:b].cpu().numpy()
+        acc = np.zeros(b - a)
+        width = 0.0
+        for k in range(wl.K - 1):
+            acc = acc + 0.25 * (h["g"] - rh[k]).astype(np.float32).astype(np.float64)
+            width = max(width, 12.0 * acc.std() / 256.0)
+        diff = np.abs(d_g.astype(np.float64) - d_o)
+        far = diff > 1e-3 * width
+        assert far.mean() <= 1e-4 and np.all(diff[far] <= 1.1 * width), (t, far.sum())
+        assert rel_l2(d_g[~far], d_o[~far]) <= TOL_REL_L2, t
+        print(f"ring tensor {t} n={b - a} moved elements {int(far.sum())}")
+    # RDA from a fresh copy of theta_g, on the GPU's own quantisation
+    run.g.copy_(g0)
+    run.m.zero_()
+    counts = torch.empty((wl.K, run.frag.T, 256), dtype=torch.int32, device="cuda")
+    dl.pseudograd_stats(run.g, reps, run.frag, 6.0, run.sync.stats, run.sync.ws_stats)
+    dl.quantize(run.g, reps, run.frag, run.sync.stats, run.sync.codes, run.sync.codebook, counts,
+                run.sync.ws_quant)
+    db.fill_(float("nan"))
+    dl.rda_merge_outer_step(run.g, run.m, run.frag, run.sync.codes, run.sync.codebook, counts,
+                            delta_bar=db)
+    torch.cuda.synchronize()
+    cb_all = run.sync.codebook.cpu().numpy()
+    cnt_all = counts.cpu().numpy().view(np.uint32)
+    for t, h in run.host.items():
+        i, a, b = h["i"], h["a"], h["b"]
+        codes = [run.sync.codes[k][a:b].cpu().numpy() for k in range(wl.K)]
+        st, g_o, m_o, d_o = oracle.rda_merge_outer_step(
+            h["g"], h["m"], codes, np.ascontiguousarray(cb_all[:, i:i + 1]),
+            np.ascontiguousarray(cnt_all[:, i:i + 1]))
+        assert st == 0
+        assert rel_l2(db[a:b].cpu().numpy(), d_o) <= TOL_REL_L2, t
+        assert rel_l2(run.g[a:b].cpu().numpy(), g_o) <= TOL_REL_L2, t
