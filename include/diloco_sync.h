@@ -10,7 +10,8 @@
  *   dl_merge_outer_step    (device)      decode, weighted fp32 mean, Nesterov
  *
  * dl_outer_sync runs that sequence over every fragment of a model in one
- * call, overlapping consecutive fragments on two streams.
+ * call, overlapping consecutive fragments on two streams; flags select the
+ * RDA merge or the re-quantising ring in place of the mean merge.
  *
  * Sources: the INTELLECT-1 paper notes ("INTELLECT-1: Training a 10B Model
  * Across 3 Continents", sections 3.2, 4.1 and 4.2) define the pseudo-gradient,
@@ -201,11 +202,15 @@ typedef struct dl_fragment_job {
 
 #define DL_SYNC_UNQUANTIZED 1 /* merge the fp32 Delta_k directly (no stats, no codes) */
 #define DL_SYNC_SERIAL 2      /* run every kernel on `stream`, one fragment after another */
+#define DL_SYNC_RDA 4         /* merge with dl_rda_merge_outer_step instead of the mean */
+#define DL_SYNC_RING 8        /* each fragment through dl_ring_outer_step (on `stream`) */
 
-/* Workspace bytes needed by dl_outer_sync for these jobs and K (0 on a bad
- * argument). Only the jobs' fragments are read. Covers every number of
- * present learners from 1 to K, so one workspace serves any quorum. */
-size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K);
+/* Workspace bytes needed by dl_outer_sync for these jobs, K and flags (0 on a
+ * bad argument or an invalid flag combination). Only the jobs' fragments are
+ * read. Covers every number of present learners from 1 to K, so one
+ * workspace serves any quorum. */
+size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K,
+                                     int32_t flags);
 
 /*
  * A whole outer step over the fragments of a model (Decoupled DiLoCo note,
@@ -225,14 +230,23 @@ size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs
  * live until the process exits; enqueueing is serialised per device by a
  * mutex. `stream` must belong to the current device. DL_SYNC_SERIAL keeps
  * everything on `stream` and creates nothing.
+ *
+ * DL_SYNC_RDA: the merge of each job is dl_rda_merge_outer_step (the
+ * quantiser's bucket counts kept in the workspace), bitwise what the four
+ * calls stats -> quantize (with counts) -> dl_rda_merge_outer_step give.
+ * DL_SYNC_RING: each job is one dl_ring_outer_step call on `stream` (its
+ * hops are sequential by definition, so nothing overlaps); bitwise what
+ * that call gives. Neither combines with DL_SYNC_UNQUANTIZED, nor with each
+ * other (DL_ERR_ARG).
  *   jobs, n_jobs  host array of fragment jobs; fragments must not overlap
  *                 each other's buffers
  *   K             learners per job (1..DL_MAX_LEARNERS)
  *   clip_sigmas   > 0 (6 in the pages); ignored with DL_SYNC_UNQUANTIZED
  *   min_quorum    applied to every job; a job below it fails the whole call
  *   lr, mu        outer Nesterov learning rate and momentum (0.7, 0.9)
- *   flags         0 or a combination of DL_SYNC_UNQUANTIZED, DL_SYNC_SERIAL
- *   d_workspace   device scratch of dl_outer_sync_workspace_bytes bytes
+ *   flags         0 or DL_SYNC_UNQUANTIZED, DL_SYNC_RDA or DL_SYNC_RING,
+ *                 each optionally with DL_SYNC_SERIAL
+ *   d_workspace   device scratch of dl_outer_sync_workspace_bytes(..., flags)
  *                 (unused with DL_SYNC_UNQUANTIZED). Its first word is the
  *                 device status word read by dl_read_device_status.
  * Every job is validated before anything is enqueued (quorum, weights,

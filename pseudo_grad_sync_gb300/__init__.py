@@ -33,6 +33,8 @@ DL_NBUCKETS = 256
 DL_MAX_LEARNERS = 32
 DL_SYNC_UNQUANTIZED = 1
 DL_SYNC_SERIAL = 2
+DL_SYNC_RDA = 4
+DL_SYNC_RING = 8
 STATS_FIELDS = ("count", "nonfinite", "mean", "std", "lo", "hi")
 
 _lib = None
@@ -79,7 +81,7 @@ def lib():
                                           vp]
         jb = ctypes.POINTER(_FragmentJob)
         L.dl_outer_sync_workspace_bytes.restype = sz
-        L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32]
+        L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32, i32]
         L.dl_outer_sync.restype = ctypes.c_int
         L.dl_outer_sync.argtypes = [jb, i32, i32, f64, i32, f32, f32, i32, vp, sz, vp]
         L.dl_rda_workspace_bytes.restype = sz
@@ -261,9 +263,9 @@ def _jobs(frags, theta_g=None, momentum=None, replicas=None, weights=None, prese
     return arr, keep
 
 
-def outer_sync_workspace_bytes(frags, K: int) -> int:
+def outer_sync_workspace_bytes(frags, K: int, flags: int = 0) -> int:
     arr, _ = _jobs(frags)
-    return int(lib().dl_outer_sync_workspace_bytes(arr, len(frags), K))
+    return int(lib().dl_outer_sync_workspace_bytes(arr, len(frags), K, int(flags)))
 
 
 def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=None, present=None,
@@ -271,10 +273,12 @@ def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=No
                stream=None):
     """One outer step over every fragment (dl_outer_sync). Per-fragment lists:
     theta_g[j], momentum[j], replicas[j] (K tensors), and optionally
-    weights[j] / present[j] (length-K host arrays) and delta_bar[j]."""
+    weights[j] / present[j] (length-K host arrays) and delta_bar[j]. flags:
+    DL_SYNC_UNQUANTIZED, DL_SYNC_RDA or DL_SYNC_RING, each optionally with
+    DL_SYNC_SERIAL."""
     arr, keep = _jobs(frags, theta_g, momentum, replicas, weights, present, delta_bar)
     if workspace is None and not flags & DL_SYNC_UNQUANTIZED:
-        workspace = new_workspace(outer_sync_workspace_bytes(frags, K), theta_g[0].device)
+        workspace = new_workspace(outer_sync_workspace_bytes(frags, K, flags), theta_g[0].device)
     nbytes = 0 if workspace is None else workspace.numel()
     _check("dl_outer_sync", lib().dl_outer_sync(
         arr, len(frags), K, float(clip_sigmas), int(min_quorum), float(lr), float(mu), int(flags),
@@ -381,11 +385,17 @@ class ModelSync:
     """Whole-model outer step (dl_outer_sync) over a fixed list of fragments,
     with its workspace allocated once."""
 
-    def __init__(self, frags, K: int, device="cuda", clip_sigmas=6.0, lr=0.7, mu=0.9):
+    def __init__(self, frags, K: int, device="cuda", clip_sigmas=6.0, lr=0.7, mu=0.9, mode=0):
+        """mode: 0 (mean merge), DL_SYNC_RDA or DL_SYNC_RING; the workspace is
+        sized for it (and serves the unquantised and serial variants)."""
         self.frags, self.K, self.clip, self.lr, self.mu = list(frags), K, clip_sigmas, lr, mu
-        self.workspace = new_workspace(outer_sync_workspace_bytes(self.frags, K), device)
+        self.mode = int(mode)
+        self.workspace = new_workspace(outer_sync_workspace_bytes(self.frags, K, self.mode),
+                                       device)
 
     def step(self, theta_g, momentum, replicas, weights=None, present=None, min_quorum=1,
              delta_bar=None, flags=0, stream=None):
+        if not flags & DL_SYNC_UNQUANTIZED:
+            flags |= self.mode
         outer_sync(self.frags, theta_g, momentum, replicas, self.K, self.workspace, weights,
                    present, min_quorum, self.clip, self.lr, self.mu, flags, delta_bar, stream)

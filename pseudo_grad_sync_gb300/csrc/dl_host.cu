@@ -11,7 +11,7 @@
 
 #include "dl_common.cuh"
 
-extern "C" int dl_version(void) { return 101; }
+extern "C" int dl_version(void) { return 200; }
 
 extern "C" const char* dl_status_string(int status) {
     switch (status) {

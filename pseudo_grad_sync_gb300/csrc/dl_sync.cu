@@ -62,12 +62,26 @@ int create_side(SideResources& r) {
     return DL_OK;
 }
 
+constexpr int32_t kSyncFlags = DL_SYNC_UNQUANTIZED | DL_SYNC_SERIAL | DL_SYNC_RDA | DL_SYNC_RING;
+
+// Flags that make sense together: RDA and the ring are quantised modes, and
+// one excludes the other.
+bool flags_valid(int32_t flags) {
+    if ((flags & ~kSyncFlags) != 0) return false;
+    const bool unq = (flags & DL_SYNC_UNQUANTIZED) != 0;
+    const bool rda = (flags & DL_SYNC_RDA) != 0, ring = (flags & DL_SYNC_RING) != 0;
+    return !(rda && ring) && !(unq && (rda || ring));
+}
+
 // Workspace layout (every part 256-byte aligned). The statistics workspace
 // comes first, so its status word is the outer workspace's first word and
-// dl_read_device_status reads it.
+// dl_read_device_status reads it; in ring mode the ring's own workspace is
+// the whole layout (its status word first, too).
 struct SyncLayout {
     size_t stats_ws = 0, stats_arr = 0, quant_ws = 0, codebook = 0, codes_each = 0;
+    size_t counts = 0, rda_ws = 0, ring_ws = 0;
     size_t off_stats_arr[2] = {0, 0}, off_quant_ws = 0, off_codebook = 0, off_codes = 0;
+    size_t off_counts = 0, off_rda_ws = 0;
     size_t total = 0;
     int T_max = 0;
     int64_t n_max = 0;
@@ -75,9 +89,24 @@ struct SyncLayout {
 
 // Scratch sizes depend on the number of present learners, which may be any
 // value in 1..K; the layout takes the largest over all of them.
-int sync_layout(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, SyncLayout* L) {
-    if (n_jobs < 0 || K <= 0 || K > DL_MAX_LEARNERS || (n_jobs > 0 && !jobs)) return DL_ERR_ARG;
+int sync_layout(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, int32_t flags,
+                SyncLayout* L) {
+    if (n_jobs < 0 || K <= 0 || K > DL_MAX_LEARNERS || (n_jobs > 0 && !jobs) ||
+        !flags_valid(flags))
+        return DL_ERR_ARG;
     *L = SyncLayout();
+    if (flags & DL_SYNC_RING) {
+        for (int32_t j = 0; j < n_jobs; ++j) {
+            HostFrag f;
+            const int st = check_fragment(jobs[j].frag, &f);
+            if (st != DL_OK) return st;
+            const size_t r = dl_ring_workspace_bytes(jobs[j].frag);
+            if (r > L->ring_ws) L->ring_ws = r;
+        }
+        L->ring_ws = align256(L->ring_ws > kWsHeader ? L->ring_ws : kWsHeader);
+        L->total = L->ring_ws;
+        return DL_OK;
+    }
     for (int32_t j = 0; j < n_jobs; ++j) {
         HostFrag f;
         const int st = check_fragment(jobs[j].frag, &f);
@@ -90,6 +119,10 @@ int sync_layout(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, SyncLayo
             const size_t q = dl_quantize_workspace_bytes(jobs[j].frag, np);
             if (s > L->stats_ws) L->stats_ws = s;
             if (q > L->quant_ws) L->quant_ws = q;
+            if (flags & DL_SYNC_RDA) {
+                const size_t r = dl_rda_workspace_bytes(jobs[j].frag, np);
+                if (r > L->rda_ws) L->rda_ws = r;
+            }
         }
     }
     L->stats_ws = align256(L->stats_ws > kWsHeader ? L->stats_ws : kWsHeader);
@@ -108,6 +141,14 @@ int sync_layout(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, SyncLayo
     o += L->codebook;
     L->off_codes = o;
     o += L->codes_each * static_cast<size_t>(K);
+    if (flags & DL_SYNC_RDA) {
+        L->counts = align256(sizeof(uint32_t) * static_cast<size_t>(K) * L->T_max * kNB);
+        L->rda_ws = align256(L->rda_ws);
+        L->off_counts = o;
+        o += L->counts;
+        L->off_rda_ws = o;
+        o += L->rda_ws;
+    }
     L->total = o;
     return DL_OK;
 }
@@ -155,9 +196,9 @@ int gather_present(const dl_fragment_job& job, int32_t K, int32_t min_quorum, Pr
 using namespace dl;
 
 extern "C" size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs,
-                                                int32_t K) {
+                                                int32_t K, int32_t flags) {
     SyncLayout L;
-    if (sync_layout(jobs, n_jobs, K, &L) != DL_OK) return 0;
+    if (sync_layout(jobs, n_jobs, K, flags, &L) != DL_OK) return 0;
     return L.total;
 }
 
@@ -165,12 +206,13 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
                              double clip_sigmas, int32_t min_quorum, float lr, float mu,
                              int32_t flags, void* d_workspace, size_t workspace_bytes,
                              void* stream) {
-    if ((flags & ~(DL_SYNC_UNQUANTIZED | DL_SYNC_SERIAL)) != 0) return DL_ERR_ARG;
+    if (!flags_valid(flags)) return DL_ERR_ARG;
     const bool quantized = (flags & DL_SYNC_UNQUANTIZED) == 0;
     const bool serial = (flags & DL_SYNC_SERIAL) != 0;
+    const bool rda = (flags & DL_SYNC_RDA) != 0, ring = (flags & DL_SYNC_RING) != 0;
     if (quantized && (!(clip_sigmas > 0.0) || !(clip_sigmas < 1e300))) return DL_ERR_ARG;
     SyncLayout L;
-    int st = sync_layout(jobs, n_jobs, K, &L);
+    int st = sync_layout(jobs, n_jobs, K, flags, &L);
     if (st != DL_OK) return st;
     if (n_jobs == 0) return DL_OK;
     // every job is validated before anything is enqueued
@@ -195,6 +237,18 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
 
     if (!d_workspace || workspace_bytes < L.total) return DL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0) return DL_ERR_ALIGN;
+    if (ring) {  // each fragment's ring runs its hops in order on `stream`
+        for (int32_t j = 0; j < n_jobs; ++j) {
+            const dl_fragment_job& job = jobs[j];
+            Present p;
+            gather_present(job, K, min_quorum, &p);
+            st = dl_ring_outer_step(job.theta_g, job.momentum, p.rep, p.np, job.frag,
+                                    job.weights ? p.w : nullptr, nullptr, min_quorum, clip_sigmas,
+                                    lr, mu, job.delta_bar_out, d_workspace, L.ring_ws, main_s);
+            if (st != DL_OK) return st;
+        }
+        return DL_OK;
+    }
     char* ws = static_cast<char*>(d_workspace);
     void* stats_ws = ws;
     dl_stats* stats_arr[2] = {reinterpret_cast<dl_stats*>(ws + L.off_stats_arr[0]),
@@ -235,14 +289,21 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
                 break;
         }
         // main: quantise and merge fragment j
+        uint32_t* counts = rda ? reinterpret_cast<uint32_t*>(ws + L.off_counts) : nullptr;
         st = dl_quantize(job.theta_g, p.rep, p.np, job.frag, stats_arr[b], codes, codebook,
-                         nullptr, quant_ws, L.quant_ws, main_s);
+                         counts, quant_ws, L.quant_ws, main_s);
         if (st != DL_OK) break;
         if (!serial && (st = cuda_status(cudaEventRecord(R->quant_done[b], main_s))) != DL_OK)
             break;
-        st = dl_merge_outer_step(job.theta_g, job.momentum, codes, codebook, nullptr, p.np,
-                                 job.frag, job.weights ? p.w : nullptr, nullptr, min_quorum, lr,
-                                 mu, job.delta_bar_out, main_s);
+        if (rda)
+            st = dl_rda_merge_outer_step(job.theta_g, job.momentum, codes, codebook, counts,
+                                         p.np, job.frag, job.weights ? p.w : nullptr, nullptr,
+                                         min_quorum, lr, mu, job.delta_bar_out,
+                                         ws + L.off_rda_ws, L.rda_ws, main_s);
+        else
+            st = dl_merge_outer_step(job.theta_g, job.momentum, codes, codebook, nullptr, p.np,
+                                     job.frag, job.weights ? p.w : nullptr, nullptr, min_quorum,
+                                     lr, mu, job.delta_bar_out, main_s);
     }
     if (!serial) {
         // join even after a failure, so that the caller's stream stays ordered

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(L):
             "dl_merge_outer_step"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
-    assert L.dl_version() == 101
+    assert L.dl_version() == 200
 
 
 def test_status_strings(L):
@@ -163,12 +163,21 @@ def test_outer_sync_validates_every_job_before_any_launch(L):
     frags = [f for f, _ in fs]
     K = 3
     arr, keep = _sync_jobs(frags, K)
-    need = L.dl_outer_sync_workspace_bytes(arr, 3, K)
+    need = L.dl_outer_sync_workspace_bytes(arr, 3, K, 0)
     assert need > 0
     # quantised mode: every job valid, so the short workspace is what fails
     assert _outer_sync(L, arr, 3, K, nbytes=need - 1) == -6
     assert _outer_sync(L, arr, 3, K, ws=FAKE + 16, nbytes=need) == -2
-    assert _outer_sync(L, arr, 3, K, flags=4) == -1
+    # unknown flags and combinations that mean nothing
+    for fl in (16, 1 | 4, 1 | 8, 4 | 8, 1 | 4 | 8, -1):
+        assert _outer_sync(L, arr, 3, K, flags=fl) == -1, fl
+        assert L.dl_outer_sync_workspace_bytes(arr, 3, K, fl) == 0, fl
+    for fl in (4, 8, 4 | 2, 8 | 2):
+        need_m = L.dl_outer_sync_workspace_bytes(arr, 3, K, fl)
+        assert need_m > 0, fl
+        assert _outer_sync(L, arr, 3, K, flags=fl, nbytes=need_m - 1) == -6, fl
+        assert _outer_sync(L, arr, 3, K, flags=fl, ws=FAKE + 16, nbytes=need_m) == -2, fl
+        assert _outer_sync(L, arr, 3, K, flags=fl, min_quorum=4) == -3, fl
     assert _outer_sync(L, arr, 3, 0) == -1 and _outer_sync(L, arr, 3, 33) == -1
     assert L.dl_outer_sync(arr, 3, K, 0.0, 1, 0.7, 0.9, 0, FAKE, need, None) == -1
     assert _outer_sync(L, arr, 3, K, min_quorum=4) == -3
@@ -180,7 +189,7 @@ def test_outer_sync_validates_every_job_before_any_launch(L):
     assert _outer_sync(L, arr3, 3, K) == -1
     arr[1].momentum = FAKE + 4
     assert _outer_sync(L, arr, 3, K, nbytes=need) == -2
-    assert L.dl_outer_sync_workspace_bytes(arr, 3, 0) == 0
+    assert L.dl_outer_sync_workspace_bytes(arr, 3, 0, 0) == 0
 
 
 def test_outer_sync_quorum_and_weights_per_job_match_oracle(L):
@@ -211,12 +220,17 @@ def test_outer_sync_workspace_covers_every_quorum(L):
     f, _o = _frag(np.cumsum([0, 4096, 77, 8192 * 9 + 3]))
     for K in (1, 3, 4, 7, 16, 32):
         arr, keep = _sync_jobs([f, f], K)
-        need = L.dl_outer_sync_workspace_bytes(arr, 2, K)
+        need = L.dl_outer_sync_workspace_bytes(arr, 2, K, 0)
+        need_rda = L.dl_outer_sync_workspace_bytes(arr, 2, K, 4)
         fb = ctypes.byref(f)
         for np_ in range(1, K + 1):
             parts = (L.dl_stats_workspace_bytes(fb, np_) + 2 * 48 * K * 3
                      + L.dl_quantize_workspace_bytes(fb, np_) + 4 * K * 3 * 256 + K * (8192 * 9 + 4174))
             assert need >= parts, (K, np_)
+            # RDA adds the bucket counts and the RDA merge's own scratch
+            assert need_rda >= parts + 4 * K * 3 * 256 + L.dl_rda_workspace_bytes(fb, np_)
+        # the ring needs its own workspace, whatever K
+        assert L.dl_outer_sync_workspace_bytes(arr, 2, K, 8) >= L.dl_ring_workspace_bytes(fb)
 
 
 def test_workspace_needs_never_decrease_with_K(L):

@@ -130,16 +130,18 @@ def test_canaries_survive_every_entry_point(dl):
     assert not bad, bad
 
 
-def test_canaries_survive_outer_sync(dl):
+@pytest.mark.parametrize("mode", ["mean", "rda", "ring"])
+def test_canaries_survive_outer_sync(dl, mode):
     K = 4
+    flags = {"mean": 0, "rda": dl.DL_SYNC_RDA, "ring": dl.DL_SYNC_RING}[mode]
     layout = [[9001, 3, 0], [4095, 8193], [1], [16384 + 2, 77]]
     frags = [dl.Fragment(x) for x in layout]
     models = [_model(K, x, seed=i) for i, x in enumerate(layout)]
-    ws = Guarded((dl.outer_sync_workspace_bytes(frags, K),), torch.uint8, 0)
+    ws = Guarded((dl.outer_sync_workspace_bytes(frags, K, flags),), torch.uint8, 0)
     dbs = [Guarded((F.n,), torch.float32) for F in frags]
     dl.outer_sync(frags, [mm[0].t for mm in models], [mm[2].t for mm in models],
                   [[r.t for r in mm[1]] for mm in models], K, workspace=ws.t,
-                  delta_bar=[d.t for d in dbs])
+                  delta_bar=[d.t for d in dbs], flags=flags)
     torch.cuda.synchronize()
     guards = [ws] + dbs + [x for mm in models for x in [mm[0], mm[2]] + mm[1]]
     assert all(x.intact() for x in guards)

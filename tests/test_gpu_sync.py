@@ -5,7 +5,10 @@ Its results must be bitwise those of the per-fragment call sequence
 (dl_pseudograd_stats -> dl_quantize -> dl_merge_outer_step over the present
 learners), whichever schedule runs: the two-stream pipeline or
 DL_SYNC_SERIAL. The per-fragment sequence itself is checked against the
-oracle here on the first step and in the other GPU parity tests.
+oracle here on the first step and in the other GPU parity tests. The same
+holds for the RDA merge (DL_SYNC_RDA: stats -> quantize with counts ->
+dl_rda_merge_outer_step) and the ring (DL_SYNC_RING: dl_ring_outer_step per
+fragment), whose per-call results the RDA and ring tests check further.
 """
 import numpy as np
 import pytest
@@ -195,3 +198,54 @@ def test_many_fragments_single_learner(dl):
     _per_call(dl, b, reps_d, 1, [None] * len(layout), [None] * len(layout))
     torch.cuda.synchronize()
     _assert_same(a.host(), b.host())
+
+
+def _per_call_mode(dl, mode, run, reps_d, K, weights, present):
+    """The per-fragment calls that DL_SYNC_RDA / DL_SYNC_RING stand for, over
+    the present learners in ascending order."""
+    for j, F in enumerate(run.frags):
+        if mode == "ring":
+            dl.ring_outer_step(run.g[j], run.m[j], F, reps_d[j], weights=weights[j],
+                               present=present[j], delta_bar=run.db[j])
+            continue
+        idx = [k for k in range(K) if present[j][k]]
+        reps = [reps_d[j][k] for k in idx]
+        st = dl.pseudograd_stats(run.g[j], reps, F)
+        counts = torch.empty((len(idx), F.T, 256), dtype=torch.int32, device="cuda")
+        codes, cb = dl.quantize(run.g[j], reps, F, st, counts=counts)
+        dl.rda_merge_outer_step(run.g[j], run.m[j], F, codes, cb, counts,
+                                weights=weights[j][idx], delta_bar=run.db[j])
+
+
+@pytest.mark.parametrize("mode", ["rda", "ring"])
+def test_rda_and_ring_modes_bitwise_equal_per_call(dl, mode):
+    K, steps = 4, 2
+    flag = dl.DL_SYNC_RDA if mode == "rda" else dl.DL_SYNC_RING
+    rng, g, sig = _model(6 if mode == "rda" else 7, K)
+    P = len(LAYOUT)
+    runs = {name: Run(dl, g) for name in ("pipe", "serial", "calls")}
+    ms = dl.ModelSync(runs["pipe"].frags, K, mode=flag)
+    ms_serial = dl.ModelSync(runs["serial"].frags, K, mode=flag)
+    for _step in range(steps):
+        present = [(rng.random(K) < 0.75).astype(np.uint8) for _ in range(P)]
+        for p in present:
+            p[rng.integers(K)] = 1
+        weights = [rng.uniform(0.5, 1.5, K).astype(np.float32) for _ in range(P)]
+        deltas = [[(rng.standard_normal(gf.size) * sf).astype(np.float32) for _ in range(K)]
+                  for gf, sf in zip(g, sig)]
+
+        def reps_of(run):
+            return [[run.g[j] - torch.from_numpy(d).cuda() for d in deltas[j]] for j in range(P)]
+
+        ms.step(runs["pipe"].g, runs["pipe"].m, reps_of(runs["pipe"]), weights=weights,
+                present=present, delta_bar=runs["pipe"].db)
+        ms_serial.step(runs["serial"].g, runs["serial"].m, reps_of(runs["serial"]),
+                       weights=weights, present=present, delta_bar=runs["serial"].db,
+                       flags=dl.DL_SYNC_SERIAL)
+        _per_call_mode(dl, mode, runs["calls"], reps_of(runs["calls"]), K, weights, present)
+        torch.cuda.synchronize()
+        out = {k: r.host() for k, r in runs.items()}
+        _assert_same(out["pipe"], out["serial"])
+        _assert_same(out["pipe"], out["calls"])
+        assert dl.read_device_status(ms.workspace) == 0
+        assert all(np.isfinite(x).all() for x in out["pipe"][0])
