@@ -345,13 +345,22 @@ def run_learner(args, rank, world, local):
 
 def ring_algo_bytes(S):
     """Algorithmic bytes per element of one ring step over S learners: hop 0
-    reads theta_g and a replica and writes P (12); each later hop quantises P
-    (stats 4, quantise 4 + 1) and then reads the codes, theta_g and a replica
-    and writes P (13), the last one instead reading momentum and writing
-    theta and momentum (21)."""
+    reads theta_g and a replica and writes P (12), accumulating P's
+    statistics as it goes; each later hop quantises P (4 + 1) and then reads
+    the codes, theta_g and a replica and writes P (13), the last one instead
+    reading momentum and writing theta and momentum (21)."""
     if S == 1:
         return 24
-    return 12 + 9 * (S - 1) + 13 * (S - 2) + 21
+    return 12 + 5 * (S - 1) + 13 * (S - 2) + 21
+
+
+def ring_launches(S):
+    """Kernels of one ring step per fragment: hop 0 (shift + hop), then per
+    later hop the statistics finalisation and the quantiser's three kernels,
+    and the hop (shift + hop, the last one alone)."""
+    if S == 1:
+        return 1
+    return 2 + 4 * (S - 1) + 2 * (S - 2) + 1
 
 
 def run_ring(args, rank, world, local):
@@ -409,7 +418,7 @@ def run_ring(args, rank, world, local):
                      "frac": round(gbs / peak, 4), "traffic": None,
                      "note": f"{ab} algorithmic B/elem per ring step; calls timed with CUDA "
                              f"events; peak = {peak_kind} copy bandwidth"},
-        "clocks": clk, "gpu_launches": args.steps * len(frags) * (1 + 7 * (wl.K - 1)),
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * ring_launches(wl.K),
         "e2e": None,
     }
     if rank == 0:

@@ -227,8 +227,8 @@ size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs
  * (two statistics buffers). The side stream forks from `stream` at entry and
  * joins it before return, so all effects are ordered on `stream`. The side
  * stream and its events are created on the current device on first use and
- * live until the process exits; enqueueing is serialised per device by a
- * mutex. `stream` must belong to the current device. DL_SYNC_SERIAL keeps
+ * live until dl_shutdown (or process exit); enqueueing is serialised per
+ * device by a mutex. `stream` must belong to the current device. DL_SYNC_SERIAL keeps
  * everything on `stream` and creates nothing.
  *
  * DL_SYNC_RDA: the merge of each job is dl_rda_merge_outer_step (the
@@ -256,6 +256,14 @@ size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs
 int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_t K, double clip_sigmas,
                   int32_t min_quorum, float lr, float mu, int32_t flags, void* d_workspace,
                   size_t workspace_bytes, void* stream);
+
+/* Releases what the library created on its own: dl_outer_sync's side stream
+ * and events, on every device where they exist, after waiting for the work
+ * queued on the side stream. The next dl_outer_sync creates them again. Must not run
+ * concurrently with a dl_outer_sync call that is enqueueing (it waits for
+ * the per-device mutex). Returns DL_OK, or DL_ERR_CUDA if a destroy failed
+ * (the handles are dropped either way). */
+int dl_shutdown(void);
 
 /* Workspace bytes needed by dl_rda_merge_outer_step for this fragment and K
  * (0 on a bad argument). */
@@ -309,15 +317,20 @@ size_t dl_ring_workspace_bytes(const dl_fragment* frag);
  *   theta_k     host [K] of device [n] fp32 (absent learners never read)
  *   weights, present, min_quorum, lr, mu, delta_bar_out  as for
  *               dl_merge_outer_step
+ *   hop_stats_out  device [S-1][T] dl_stats (8-byte aligned), or NULL: row s
+ *               gets the statistics of P_s as quantised at hop s+1 (the
+ *               partial sum's range at each hop); untouched when S = 1
  *   d_workspace device scratch of dl_ring_workspace_bytes(frag) bytes (holds
  *               P, its codes and codebooks; its first word is the device
  *               status word)
+ * The statistics of each P_s are accumulated by the hop that writes it (no
+ * separate pass over P), with the arithmetic of dl_pseudograd_stats.
  */
 int dl_ring_outer_step(float* theta_g, float* momentum, const float* const* theta_k, int32_t K,
                        const dl_fragment* frag, const float* weights, const uint8_t* present,
                        int32_t min_quorum, double clip_sigmas, float lr, float mu,
-                       float* delta_bar_out, void* d_workspace, size_t workspace_bytes,
-                       void* stream);
+                       float* delta_bar_out, dl_stats* hop_stats_out, void* d_workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * dl_quantize without a caller-provided workspace. The pages have no

@@ -84,6 +84,8 @@ def lib():
         L.dl_outer_sync_workspace_bytes.argtypes = [jb, i32, i32, i32]
         L.dl_outer_sync.restype = ctypes.c_int
         L.dl_outer_sync.argtypes = [jb, i32, i32, f64, i32, f32, f32, i32, vp, sz, vp]
+        L.dl_shutdown.restype = ctypes.c_int
+        L.dl_shutdown.argtypes = []
         L.dl_rda_workspace_bytes.restype = sz
         L.dl_rda_workspace_bytes.argtypes = [fr, i32]
         L.dl_rda_merge_outer_step.restype = ctypes.c_int
@@ -93,7 +95,7 @@ def lib():
         L.dl_ring_workspace_bytes.argtypes = [fr]
         L.dl_ring_outer_step.restype = ctypes.c_int
         L.dl_ring_outer_step.argtypes = [vp, vp, vp, i32, fr, vp, vp, i32, f64, f32, f32, vp, vp,
-                                         sz, vp]
+                                         vp, sz, vp]
         L.dl_selftest_wait_timeout.restype = ctypes.c_int
         L.dl_selftest_wait_timeout.argtypes = [vp, i32, vp]
         L.dl_read_device_status.restype = ctypes.c_int
@@ -287,6 +289,11 @@ def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=No
     return workspace
 
 
+def shutdown():
+    """Release the side stream and events dl_outer_sync created (dl_shutdown)."""
+    _check("dl_shutdown", lib().dl_shutdown())
+
+
 def rda_workspace_bytes(frag: Fragment, K: int) -> int:
     return int(lib().dl_rda_workspace_bytes(frag.c, K))
 
@@ -316,9 +323,12 @@ def ring_workspace_bytes(frag: Fragment) -> int:
 
 def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, present=None,
                     min_quorum=1, clip_sigmas=6.0, lr=0.7, mu=0.9, delta_bar=None,
-                    workspace=None, stream=None):
+                    workspace=None, stream=None, hop_stats=None):
     """Ring accumulation with re-quantisation at every hop, then the outer
-    step (dl_ring_outer_step); theta_g and momentum are updated in place."""
+    step (dl_ring_outer_step); theta_g and momentum are updated in place.
+    hop_stats: optional device int64 tensor of (S-1) * T * 6 words (as
+    new_stats(S - 1, T)) that receives the statistics of each quantised
+    partial sum."""
     if workspace is None:
         workspace = new_workspace(ring_workspace_bytes(frag), theta_g.device)
     w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
@@ -327,7 +337,7 @@ def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, p
         _ptr(theta_g), _ptr(momentum), _ptr_array(replicas), len(replicas), frag.c,
         None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
         int(min_quorum), float(clip_sigmas), float(lr), float(mu), _ptr(delta_bar),
-        _ptr(workspace), workspace.numel(), _stream(stream)))
+        _ptr(hop_stats), _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
 
 

@@ -6,18 +6,25 @@
 // On one GPU the ring's S present learners, in increasing order, are visited
 // one after another; the partial sum P lives in the workspace:
 //   hop 0:        P = w_0 * Delta_0
-//   hop s >= 1:   quantise P (dl_pseudograd_stats + dl_quantize in values
-//                 mode: the vector quantised is P itself), then
-//                 P = fmaf(w_s, Delta_s, cb[code])
+//   hop s >= 1:   quantise P (dl_quantize in values mode: the vector
+//                 quantised is P itself), then P = fmaf(w_s, Delta_s, cb[code])
 //   last hop:     instead of storing P, apply the outer Nesterov step with
 //                 D = P (and write D out if asked).
-// k_ring_hop<DECODE, FINAL> does one hop's element work: persistent blocks
-// over 8192-element chunks, the previous codebook of the current tensor in
-// shared memory, 128-bit loads and stores, 32-bit code loads.
+// k_ring_hop<DECODE, FINAL, STATS> does one hop's element work: persistent
+// blocks over 8192-element chunks, the previous codebook of the current
+// tensor in shared memory, 128-bit loads and stores, 32-bit code loads. A
+// hop whose P is quantised next (STATS) also accumulates P's per-tensor
+// statistics as it writes P, with the exact scheme of the statistics kernel
+// (float-float sums of y = P - c and of y^2 on a power-of-two offset, fp64
+// for values outside the fast range): the quantiser's statistics then cost
+// no extra pass over P. k_ring_shift computes each tensor's shift c first,
+// from the hop's own formula at the tensor's first 64 elements, with the
+// statistics kernel's rule, and stats_finish turns the partials into
+// mu, sigma, lo, hi.
 #include <math.h>
 #include <string.h>
 
-#include "dl_common.cuh"
+#include "dl_stats_acc.cuh"
 
 namespace dl {
 namespace {
@@ -33,6 +40,8 @@ struct RingArgs {
     const float* cb;        // its codebook [T][256] (DECODE)
     const int64_t* off;
     float* dbar;            // optional D (FINAL)
+    float* shift;           // [T] shifts of the new P (STATS)
+    Partial* part;          // [T][gridDim.x] partial sums of the new P (STATS)
     int64_t n;
     int64_t n_chunks;
     int T;
@@ -54,11 +63,66 @@ __device__ __forceinline__ void nesterov(float acc, float& th, float& mm, float 
     mm = m1;
 }
 
-template <bool DECODE, bool FINAL>
+// One warp per tensor: the shift of the P this hop writes, from P at the
+// tensor's first min(N, 64) elements (the hop's formula, bit for bit).
+template <bool DECODE>
+__global__ void __launch_bounds__(kThreads) k_ring_shift(RingArgs a) {
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    const int64_t o = a.off[t];
+    const int64_t N = a.off[t + 1] - o;
+    const int m = N < 64 ? static_cast<int>(N) : 64;
+    const bool h0 = lane < m, h1 = lane + 32 < m;
+    const float* cbt = a.cb + static_cast<int64_t>(t) * kNB;
+    double v[2] = {0.0, 0.0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (!(h ? h1 : h0)) continue;
+        const int64_t i = o + lane + 32 * h;
+        const float dec = DECODE ? cbt[a.codes[i]] : 0.f;
+        v[h] = static_cast<double>(hop_value<DECODE>(a.g[i], a.r[i], dec, a.w));
+    }
+    const float c = warp_shift(v[0], v[1], h0, h1, m);
+    if (lane == 0) a.shift[t] = c;
+}
+
+// Statistics of four P values of one group (the fast path when all four are
+// in range, else fp64 for the four)
+__device__ __forceinline__ void acc_group(Acc& acc, float v0, float v1, float v2, float v3,
+                                          float csh, bool small) {
+    const float y0 = __fsub_rn(v0, csh), y1 = __fsub_rn(v1, csh);
+    const float y2 = __fsub_rn(v2, csh), y3 = __fsub_rn(v3, csh);
+    const float mx = absmax_nan(y3, absmax_nan(y2, absmax_nan(y1, absmax_nan(y0, 0.f))));
+    if (!small && fast_range(mx)) {
+        if (mx > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, mx);
+        ff_add(acc.s1h, acc.s1l, __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3)));
+        sq_add(acc.s2h, acc.s2l, y0);
+        sq_add(acc.s2h, acc.s2l, y1);
+        sq_add(acc.s2h, acc.s2l, y2);
+        sq_add(acc.s2h, acc.s2l, y3);
+    } else {
+        acc.side = true;
+        side_add(v0, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(v1, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(v2, csh, acc.s1d, acc.s2d, acc.bad);
+        side_add(v3, csh, acc.s1d, acc.s2d, acc.bad);
+    }
+}
+
+template <bool DECODE, bool FINAL, bool STATS>
 __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
+    static_assert(!(FINAL && STATS), "the last hop's sum is not quantised");
     __shared__ float scb[kNB];
+    __shared__ float red_ff[kWarps][4];
+    __shared__ double red_side[kWarps][2];
+    __shared__ int red_bad[kWarps];
     const int tid = threadIdx.x;
     int cur_t = -1;
+    float csh = 0.f;
+    bool small = false;
+    Acc acc;
+    acc.reset();
     for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + static_cast<int64_t>(kChunk), a.n);
@@ -68,10 +132,21 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            if (DECODE && t != cur_t) {
-                __syncthreads();
-                scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
-                __syncthreads();
+            if (t != cur_t) {
+                if (STATS) {
+                    if (cur_t >= 0)
+                        flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x +
+                                               blockIdx.x,
+                                      red_ff, red_side, red_bad);
+                    acc.reset();
+                    csh = __ldg(a.shift + t);
+                    small = (o1 - o0) < kSmallTensor;
+                }
+                if (DECODE) {
+                    __syncthreads();
+                    scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
+                    __syncthreads();
+                }
                 cur_t = t;
             }
             if (pa == base && pb == base + kChunk) {
@@ -108,6 +183,10 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                             reinterpret_cast<float4*>(a.dbar + base)[gi] = make_float4(v0, v1, v2, v3);
                     } else {
                         reinterpret_cast<float4*>(a.P + base)[gi] = make_float4(v0, v1, v2, v3);
+                        if (STATS) {
+                            acc_group(acc, v0, v1, v2, v3, csh, small);
+                            if ((j & 3) == 3) renorm(acc.s2h, acc.s2l);
+                        }
                     }
                 }
             } else {
@@ -123,45 +202,81 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                         if (a.dbar) a.dbar[i] = v;
                     } else {
                         a.P[i] = v;
+                        if (STATS) {
+                            const float y = __fsub_rn(v, csh);
+                            const float ay = fabsf(y);
+                            if (!small && fast_range(ay)) {
+                                if (ay > acc.yt)
+                                    rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                                ff_add(acc.s1h, acc.s1l, y);
+                                sq_add(acc.s2h, acc.s2l, y);
+                            } else {
+                                acc.side = true;
+                                side_add(v, csh, acc.s1d, acc.s2d, acc.bad);
+                            }
+                        }
                     }
                 }
+                if (STATS) renorm(acc.s2h, acc.s2l);
             }
         }
     }
+    if (STATS && cur_t >= 0)
+        flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x + blockIdx.x, red_ff,
+                      red_side, red_bad);
 }
 
-template <bool DECODE, bool FINAL>
-int launch_hop(const RingArgs& a, cudaStream_t s) {
-    const void* k = reinterpret_cast<const void*>(k_ring_hop<DECODE, FINAL>);
-    const int grid = grid_for(k, kThreads, 0, a.n_chunks);
-    k_ring_hop<DECODE, FINAL><<<grid, kThreads, 0, s>>>(a);
+// One hop on s. With STATS, the shifts and zeroed partials of the new P
+// come first, and *grid_out is the hop's grid (the partials' J).
+template <bool DECODE, bool FINAL, bool STATS>
+int launch_hop(const RingArgs& a, cudaStream_t s, int* grid_out = nullptr) {
+    const void* k = reinterpret_cast<const void*>(k_ring_hop<DECODE, FINAL, STATS>);
+    int grid = grid_for(k, kThreads, 0, a.n_chunks);
+    if (grid > kMaxBlocksTotal) grid = kMaxBlocksTotal;  // partial slots per tensor
+    int st;
+    if (STATS) {
+        const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(a.T) * grid;
+        if ((st = cuda_status(cudaMemsetAsync(a.part, 0, part_bytes, s))) != DL_OK) return st;
+        k_ring_shift<DECODE><<<(a.T * 32 + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
+        if ((st = launch_status()) != DL_OK) return st;
+    }
+    k_ring_hop<DECODE, FINAL, STATS><<<grid, kThreads, 0, s>>>(a);
+    if (grid_out) *grid_out = grid;
     return launch_status();
 }
 
+// Workspace: status header | shifts [T] | partials [T][kMaxBlocksTotal] |
+// quantiser scratch | statistics [T] | codebook [T][256] | P [n] | codes [n]
 struct RingLayout {
-    size_t stats_ws, quant_ws, stats_arr, cb, part, codes;
-    size_t off_quant_ws, off_stats_arr, off_cb, off_part, off_codes, total;
+    size_t shift, part, quant_ws, stats_arr, cb, P, codes;
+    size_t off_shift, off_part, off_quant_ws, off_stats_arr, off_cb, off_P, off_codes, total;
 };
 
 int ring_layout(const dl_fragment* frag, RingLayout* L) {
     HostFrag f;
     const int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
-    L->stats_ws = align256(dl_stats_workspace_bytes(frag, 1));
+    const size_t T1 = static_cast<size_t>(f.T > 0 ? f.T : 1);
+    L->shift = align256(sizeof(float) * T1);
+    L->part = align256(sizeof(Partial) * T1 * kMaxBlocksTotal);
     L->quant_ws = align256(dl_quantize_workspace_bytes(frag, 1));
-    L->stats_arr = align256(sizeof(dl_stats) * static_cast<size_t>(f.T > 0 ? f.T : 1));
-    L->cb = align256(sizeof(float) * kNB * static_cast<size_t>(f.T > 0 ? f.T : 1));
-    L->part = align256(sizeof(float) * static_cast<size_t>(f.n));
+    L->stats_arr = align256(sizeof(dl_stats) * T1);
+    L->cb = align256(sizeof(float) * kNB * T1);
+    L->P = align256(sizeof(float) * static_cast<size_t>(f.n));
     L->codes = align256(static_cast<size_t>(f.n));
-    size_t o = L->stats_ws;  // the stats workspace first: its status word is ours
+    size_t o = kWsHeader;  // the status word first
+    L->off_shift = o;
+    o += L->shift;
+    L->off_part = o;
+    o += L->part;
     L->off_quant_ws = o;
     o += L->quant_ws;
     L->off_stats_arr = o;
     o += L->stats_arr;
     L->off_cb = o;
     o += L->cb;
-    L->off_part = o;
-    o += L->part;
+    L->off_P = o;
+    o += L->P;
     L->off_codes = o;
     o += L->codes;
     L->total = o;
@@ -182,7 +297,8 @@ extern "C" size_t dl_ring_workspace_bytes(const dl_fragment* frag) {
 extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* const* theta_k,
                                   int32_t K, const dl_fragment* frag, const float* weights,
                                   const uint8_t* present, int32_t min_quorum, double clip_sigmas,
-                                  float lr, float mu, float* delta_bar_out, void* d_workspace,
+                                  float lr, float mu, float* delta_bar_out,
+                                  dl_stats* hop_stats_out, void* d_workspace,
                                   size_t workspace_bytes, void* stream) {
     HostFrag f;
     int st = check_fragment(frag, &f);
@@ -215,6 +331,8 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
     if (!aligned16(theta_g) || !aligned16(momentum) ||
         (delta_bar_out && !aligned16(delta_bar_out)))
         return DL_ERR_ALIGN;
+    if (hop_stats_out && (reinterpret_cast<uintptr_t>(hop_stats_out) & 7u) != 0)
+        return DL_ERR_ALIGN;
     for (int s = 0; s < S; ++s) {
         if (!theta_k[idx[s]]) return DL_ERR_ARG;
         if (!aligned16(theta_k[idx[s]])) return DL_ERR_ALIGN;
@@ -225,7 +343,6 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
     if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0) return DL_ERR_ALIGN;
 
     char* ws = static_cast<char*>(d_workspace);
-    dl_stats* stats = reinterpret_cast<dl_stats*>(ws + L.off_stats_arr);
     float* cb = reinterpret_cast<float*>(ws + L.off_cb);
     uint8_t* codes = reinterpret_cast<uint8_t*>(ws + L.off_codes);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
@@ -234,33 +351,45 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
     memset(&a, 0, sizeof(a));
     a.g = theta_g;
     a.m = momentum;
-    a.P = reinterpret_cast<float*>(ws + L.off_part);
+    a.P = reinterpret_cast<float*>(ws + L.off_P);
     a.codes = codes;
     a.cb = cb;
     a.off = f.d_offsets;
     a.dbar = delta_bar_out;
+    a.shift = reinterpret_cast<float*>(ws + L.off_shift);
+    a.part = reinterpret_cast<Partial*>(ws + L.off_part);
     a.n = f.n;
     a.n_chunks = n_chunks_of(f.n);
     a.T = f.T;
     a.lr = lr;
     a.mu = mu;
 
+    // statistics of P_s (quantised at hop s + 1): the caller's row s, or the
+    // workspace's
+    auto stats_of = [&](int s) {
+        return hop_stats_out ? hop_stats_out + static_cast<int64_t>(s) * f.T
+                             : reinterpret_cast<dl_stats*>(ws + L.off_stats_arr);
+    };
     a.r = theta_k[idx[0]];
     a.w = w_hat[0];
-    st = S == 1 ? launch_hop<false, true>(a, strm) : launch_hop<false, false>(a, strm);
-    for (int s = 1; s < S && st == DL_OK; ++s) {
-        // send: quantise the partial sum P itself (values mode)
-        const float* P = a.P;
-        st = dl_pseudograd_stats(P, nullptr, 1, frag, clip_sigmas, stats, ws, L.stats_ws, strm);
-        if (st != DL_OK) break;
+    int J = 0;
+    if (S == 1) return launch_hop<false, true, false>(a, strm);
+    if ((st = launch_hop<false, false, true>(a, strm, &J)) != DL_OK) return st;
+    for (int s = 1; s < S; ++s) {
+        // send: finish P_{s-1}'s statistics and quantise it (values mode)
+        dl_stats* sp = stats_of(s - 1);
+        if ((st = stats_finish(a.off, f.T, 1, J, a.shift, a.part, clip_sigmas, sp, strm)) != DL_OK)
+            return st;
         uint8_t* cp[1] = {codes};
-        st = dl_quantize(P, nullptr, 1, frag, stats, cp, cb, nullptr, ws + L.off_quant_ws,
+        st = dl_quantize(a.P, nullptr, 1, frag, sp, cp, cb, nullptr, ws + L.off_quant_ws,
                          L.quant_ws, strm);
-        if (st != DL_OK) break;
+        if (st != DL_OK) return st;
         // receive: decode and add this learner's weighted pseudo-gradient
         a.r = theta_k[idx[s]];
         a.w = w_hat[s];
-        st = s == S - 1 ? launch_hop<true, true>(a, strm) : launch_hop<true, false>(a, strm);
+        st = s == S - 1 ? launch_hop<true, true, false>(a, strm)
+                        : launch_hop<true, false, true>(a, strm, &J);
+        if (st != DL_OK) return st;
     }
-    return st;
+    return DL_OK;
 }

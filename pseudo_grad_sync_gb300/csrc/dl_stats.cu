@@ -30,16 +30,10 @@
 //  k_stats_fin one warp per (k, t): fixed-order fp64 sum of its J partials, then
 //              mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population).
 // The result is deterministic: every sum has a fixed order.
-#include "dl_common.cuh"
+#include "dl_stats_acc.cuh"
 
 namespace dl {
 namespace {
-
-struct Partial {
-    double s1, s2;
-    long long bad;
-    long long pad;
-};
 
 struct StatsArgs {
     const float* g;
@@ -47,7 +41,6 @@ struct StatsArgs {
     const int64_t* off;
     float* shift;
     Partial* part;
-    dl_stats* out;
     uint32_t* status;
     int64_t n;
     int64_t n_chunks;
@@ -71,151 +64,8 @@ __global__ void __launch_bounds__(kThreads) k_shift(StatsArgs a) {
         h0 ? static_cast<double>(__fsub_rn(a.g[o + lane], rk ? rk[o + lane] : 0.f)) : 0.0;
     const double v1 =
         h1 ? static_cast<double>(__fsub_rn(a.g[o + lane + 32], rk ? rk[o + lane + 32] : 0.f)) : 0.0;
-    double s = v0 + v1;
-    for (int sh = 16; sh; sh >>= 1) s += __shfl_xor_sync(kFull, s, sh);
-    const double mean = m > 0 ? s / m : 0.0;
-    double q = (h0 ? (v0 - mean) * (v0 - mean) : 0.0) + (h1 ? (v1 - mean) * (v1 - mean) : 0.0);
-    for (int sh = 16; sh; sh >>= 1) q += __shfl_xor_sync(kFull, q, sh);
-    if (lane != 0) return;
-    const double sd = m > 0 ? sqrt(q / m) : 0.0;
-    double c = mean;
-    if (sd > 0.0 && isfinite(sd) && isfinite(mean)) {
-        // snap to a power-of-two grid no finer than sd/8: the shift then has
-        // no bits below the ulp of any typical y = Delta - c, so rounding
-        // y to fp32 is unbiased
-        int ex;
-        frexp(sd, &ex);  // sd in [2^(ex-1), 2^ex)
-        const double grid = ldexp(1.0, ex - 3);
-        c = rint(mean / grid) * grid;
-    }
-    a.shift[w] = static_cast<float>(c);
-}
-
-// fp64 contribution of one value (small tensors, huge or non-finite values)
-__device__ __forceinline__ void side_add(float d, float c, double& s1, double& s2, int& bad) {
-    if (!isfinite(d)) {
-        ++bad;
-        return;
-    }
-    const double y = static_cast<double>(d) - static_cast<double>(c);
-    s1 += y;
-    s2 = fma(y, y, s2);
-}
-
-// Per-thread sums. y^2 is summed on an offset: (s2h, s2l) holds H0 + the
-// squares since the last rebase, with H0 = yt^2 and yt a power of two at
-// least as large as every |y| this thread has summed since then; (c2h, c2l)
-// holds the squares summed before it (see sq_add and rebase).
-struct Acc {
-    float s1h, s1l;  // float-float sum of y
-    float s2h, s2l;  // float-float H0 + sum of y^2 since the last rebase
-    float c2h, c2l;  // float-float sum of y^2 before it
-    float yt, h0;    // current bound on |y| and H0 = yt^2
-    double s1d, s2d; // fp64 side sums
-    int bad;
-    bool side;
-    __device__ __forceinline__ void reset() {
-        s1h = s1l = s2h = s2l = c2h = c2l = yt = h0 = 0.f;
-        s1d = s2d = 0.0;
-        bad = 0;
-        side = false;
-    }
-};
-
-// Reduction over the consumer warps of the per-thread sums of tensor t into
-// its partial slot (k, t, j). Fixed order everywhere, so the result is
-// deterministic.
-__device__ void flush_partial(Acc& acc, const StatsArgs& a, int k, int t, int j,
-                              float (*red_ff)[4], double (*red_side)[2], int* red_bad) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // remove the offset (s2h >= H0, a power of two on its ulp grid, so the
-    // difference is exact) and join the squares summed before the last rebase
-    ff_add_ff(acc.c2h, acc.c2l, __fsub_rn(acc.s2h, acc.h0), acc.s2l);
-    acc.s2h = acc.c2h;
-    acc.s2l = acc.c2l;
-#pragma unroll
-    for (int sh = 16; sh; sh >>= 1) {
-        const float o1h = __shfl_xor_sync(kFull, acc.s1h, sh);
-        const float o1l = __shfl_xor_sync(kFull, acc.s1l, sh);
-        const float o2h = __shfl_xor_sync(kFull, acc.s2h, sh);
-        const float o2l = __shfl_xor_sync(kFull, acc.s2l, sh);
-        ff_add_ff(acc.s1h, acc.s1l, o1h, o1l);
-        ff_add_ff(acc.s2h, acc.s2l, o2h, o2l);
-    }
-    if (__any_sync(kFull, acc.side)) {
-        for (int sh = 16; sh; sh >>= 1) {
-            acc.s1d += __shfl_xor_sync(kFull, acc.s1d, sh);
-            acc.s2d += __shfl_xor_sync(kFull, acc.s2d, sh);
-            acc.bad += __shfl_xor_sync(kFull, acc.bad, sh);
-        }
-    } else {
-        acc.s1d = acc.s2d = 0.0;
-        acc.bad = 0;
-    }
-    if (lane == 0) {
-        red_ff[warp][0] = acc.s1h;
-        red_ff[warp][1] = acc.s1l;
-        red_ff[warp][2] = acc.s2h;
-        red_ff[warp][3] = acc.s2l;
-        red_side[warp][0] = acc.s1d;
-        red_side[warp][1] = acc.s2d;
-        red_bad[warp] = acc.bad;
-    }
-    consumer_sync();
-    if (threadIdx.x == 0) {
-        double s1 = 0.0, s2 = 0.0;
-        long long bad = 0;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            s1 += static_cast<double>(red_ff[w][0]) + static_cast<double>(red_ff[w][1]) + red_side[w][0];
-            s2 += static_cast<double>(red_ff[w][2]) + static_cast<double>(red_ff[w][3]) + red_side[w][1];
-            bad += red_bad[w];
-        }
-        Partial p;
-        p.s1 = s1;
-        p.s2 = s2;
-        p.bad = bad;
-        p.pad = 0;
-        a.part[(static_cast<int64_t>(k) * a.T + t) * a.J + j] = p;
-    }
-    consumer_sync();
-}
-
-// y^2 added to the float-float sum (hi, lo) = H0 + squares, for |y| <= yt:
-// then y^2 <= H0 <= hi, the sum s = fl(hi + y^2) stays within [hi, 2 hi],
-// hi - s is exact, and fma(y, y, hi - s) is the rounding error of s, itself
-// rounded once (within 2^-25 ulp(s)). The error goes to lo. Plain fp32
-// squares are not enough: when Delta carries few significant bits relative to
-// sigma (|mu| >> sigma), y is a short integer times a power of two, and the
-// bits that rounding drops from its square follow the pattern of squares (an
-// odd square ends in ...001), so every rounding goes the same way; the error
-// terms keep those bits. As H0 <= 4 max y^2, the ulps involved stay within a
-// factor 2^-21 of the squares themselves.
-__device__ __forceinline__ void sq_add(float& hi, float& lo, float y) {
-    const float s = __fmaf_rn(y, y, hi);
-    const float err = __fmaf_rn(y, y, __fsub_rn(hi, s));
-    hi = s;
-    lo = __fadd_rn(lo, err);
-}
-
-// |y| up to mx (positive, normal) is about to be summed and exceeds yt: move
-// the offset sum into (c2h, c2l) and restart on yt = the power of two >= mx.
-// Taken at a thread's first non-zero group of a tensor and then only when a
-// value exceeds every earlier one by enough to cross a power of two.
-__device__ __forceinline__ void rebase(float& s2h, float& s2l, float& c2h, float& c2l, float& yt,
-                                    float& h0, float mx) {
-    ff_add_ff(c2h, c2l, __fsub_rn(s2h, h0), s2l);
-    yt = __int_as_float((__float_as_int(mx) + 0x7FFFFF) & static_cast<int>(0xFF800000u));
-    h0 = __fmul_rn(yt, yt);
-    s2h = h0;
-    s2l = 0.f;
-}
-
-// fold lo into hi (|lo| <= ulp(hi) afterwards), so that the roundings of
-// later additions to lo stay below 2^-24 ulp(hi)
-__device__ __forceinline__ void renorm(float& hi, float& lo) {
-    const float s = __fadd_rn(hi, lo);
-    lo = __fsub_rn(lo, __fsub_rn(s, hi));
-    hi = s;
+    const float c = warp_shift(v0, v1, h0, h1, m);
+    if (lane == 0) a.shift[w] = c;
 }
 
 constexpr int kTile = 4096;  // elements per pipeline tile
@@ -225,13 +75,6 @@ constexpr int kTile = 4096;  // elements per pipeline tile
 // cover the whole share; a share with a value outside the fast range (or a
 // non-finite one) goes to the fp64 path as a whole.
 constexpr int kGroupsPerTile = kTile / 4 / kThreads;
-
-// max(|a|, b) that returns NaN if either input is NaN (fmaxf would drop it)
-__device__ __forceinline__ float absmax_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(b));
-    return r;
-}
 
 template <bool VALUES>
 __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float* tr, int tid,
@@ -253,7 +96,7 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
     // squares, their error terms and H0 stay normal and finite for
     // 2^-50 <= |y| <= 2^48 (smaller values lose at most 2^-149); mx is NaN if
     // any y is, so the fp64 path (which counts it) takes that share
-    if (mx <= 0x1p48f && (mx >= 0x1p-50f || mx == 0.0f)) {
+    if (fast_range(mx)) {
         if (mx > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, mx);
 #pragma unroll
         for (int q = 0; q < kGroupsPerTile; ++q) {
@@ -320,6 +163,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
         return;
     }
 
+    Partial* part_k = a.part + static_cast<int64_t>(k) * a.T * a.J + j;  // slot (k, t, j) at t * J
     int cur_t = -1;
     float csh = 0.f;
     bool small = false;
@@ -347,7 +191,8 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                 if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
                 if (pa >= pe) continue;
                 if (t != cur_t) {
-                    if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
+                    if (cur_t >= 0)
+                        flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
                     cur_t = t;
                     csh = __ldg(a.shift + k * a.T + t);
                     small = (o1 - o0) < kSmallTensor;
@@ -363,7 +208,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                         const float d = __fsub_rn(gv, rv);
                         const float y = __fsub_rn(d, csh);
                         const float ay = fabsf(y);
-                        if (!small && ay <= 0x1p48f && (ay >= 0x1p-50f || ay == 0.0f)) {
+                        if (!small && fast_range(ay)) {
                             if (ay > acc.yt)
                                 rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
                             ff_add(acc.s1h, acc.s1l, y);
@@ -380,10 +225,19 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
             if (lane == 0) mbar_arrive(&pb.empty[s]);
         }
     }
-    if (cur_t >= 0) flush_partial(acc, a, k, cur_t, j, red_ff, red_side, red_bad);
+    if (cur_t >= 0) flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
 }
 
-__global__ void __launch_bounds__(kThreads) k_stats_fin(StatsArgs a) {
+struct FinArgs {
+    const int64_t* off;
+    const float* shift;
+    const Partial* part;
+    dl_stats* out;
+    int T, K, J;
+    double clip;
+};
+
+__global__ void __launch_bounds__(kThreads) k_stats_fin(FinArgs a) {
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= a.K * a.T) return;
@@ -431,6 +285,24 @@ size_t shift_bytes(int K, int T) { return align256(sizeof(float) * static_cast<s
 int max_blocks_per_learner(int K) { return kMaxBlocksTotal / K; }
 
 }  // namespace
+
+int stats_finish(const int64_t* d_off, int T, int K, int J, const float* shift,
+                 const Partial* part, double clip, dl_stats* out, cudaStream_t s) {
+    if (K * T == 0) return DL_OK;
+    FinArgs f;
+    f.off = d_off;
+    f.shift = shift;
+    f.part = part;
+    f.out = out;
+    f.T = T;
+    f.K = K;
+    f.J = J;
+    f.clip = clip;
+    const int grid = (K * T * 32 + kThreads - 1) / kThreads;
+    k_stats_fin<<<grid, kThreads, 0, s>>>(f);
+    return launch_status();
+}
+
 }  // namespace dl
 
 using namespace dl;
@@ -478,7 +350,6 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     a.status = reinterpret_cast<uint32_t*>(ws);
     a.shift = reinterpret_cast<float*>(ws + kWsHeader);
     a.part = reinterpret_cast<Partial*>(ws + kWsHeader + shift_bytes(K, f.T));
-    a.out = d_stats;
     a.n = f.n;
     a.n_chunks = n_chunks_of(f.n);
     a.T = f.T;
@@ -514,6 +385,5 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
             k_stats<3, 2, false><<<K * a.J, kPipeThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
-    k_stats_fin<<<small_grid, kThreads, 0, s>>>(a);
-    return launch_status();
+    return stats_finish(a.off, f.T, K, a.J, a.shift, a.part, a.clip, d_stats, s);
 }

@@ -26,8 +26,8 @@
 namespace dl {
 namespace {
 
-// Per-device side stream and event ring, created on first use and kept for
-// the life of the process. The mutex serialises enqueueing: two callers
+// Per-device side stream and event ring, created on first use and kept
+// until dl_shutdown. The mutex serialises enqueueing: two callers
 // never interleave their records and waits on the shared events.
 struct SideResources {
     std::mutex mu;
@@ -39,16 +39,40 @@ struct SideResources {
 };
 SideResources g_side[64];
 
-int side_resources(SideResources** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DL_ERR_CUDA;
-    SideResources& r = g_side[dev];
-    *out = &r;
+int side_resources(SideResources** out, int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= 64) return DL_ERR_CUDA;
+    *out = &g_side[*dev];
     return DL_OK;
 }
 
-int create_side(SideResources& r) {
+// Releases one device's side stream and events (the caller holds r.mu).
+int destroy_side(SideResources& r, int dev) {
+    // handles from a create_side that failed part way count too
+    if (!r.side && !r.fork && !r.join && !r.stats_done[0] && !r.stats_done[1] &&
+        !r.quant_done[0] && !r.quant_done[1])
+        return DL_OK;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+        return DL_ERR_CUDA;
+    // the side stream's queued work (and so every event it records) finishes
+    // first, so no pending wait on the caller's stream refers to a dead event
+    bool ok = !r.side || cudaStreamSynchronize(r.side) == cudaSuccess;
+    cudaEvent_t* evs[] = {&r.fork, &r.join, &r.stats_done[0], &r.stats_done[1],
+                          &r.quant_done[0], &r.quant_done[1]};
+    for (cudaEvent_t* e : evs) {
+        if (*e && cudaEventDestroy(*e) != cudaSuccess) ok = false;
+        *e = nullptr;
+    }
+    if (r.side && cudaStreamDestroy(r.side) != cudaSuccess) ok = false;
+    r.side = nullptr;
+    r.ready = false;
+    if (cudaSetDevice(prev) != cudaSuccess) ok = false;
+    return ok ? DL_OK : DL_ERR_CUDA;
+}
+
+int create_side(SideResources& r, int dev) {
     if (r.ready) return DL_OK;
+    if (destroy_side(r, dev) != DL_OK) return DL_ERR_CUDA;  // leftovers of a failed attempt
     const unsigned fl = cudaEventDisableTiming;
     if (cudaStreamCreateWithFlags(&r.side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&r.fork, fl) != cudaSuccess ||
@@ -195,6 +219,16 @@ int gather_present(const dl_fragment_job& job, int32_t K, int32_t min_quorum, Pr
 
 using namespace dl;
 
+extern "C" int dl_shutdown(void) {
+    int st = DL_OK;
+    for (int dev = 0; dev < 64; ++dev) {
+        std::lock_guard<std::mutex> lock(g_side[dev].mu);
+        const int s = destroy_side(g_side[dev], dev);
+        if (st == DL_OK) st = s;
+    }
+    return st;
+}
+
 extern "C" size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs,
                                                 int32_t K, int32_t flags) {
     SyncLayout L;
@@ -244,7 +278,8 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
             gather_present(job, K, min_quorum, &p);
             st = dl_ring_outer_step(job.theta_g, job.momentum, p.rep, p.np, job.frag,
                                     job.weights ? p.w : nullptr, nullptr, min_quorum, clip_sigmas,
-                                    lr, mu, job.delta_bar_out, d_workspace, L.ring_ws, main_s);
+                                    lr, mu, job.delta_bar_out, nullptr, d_workspace, L.ring_ws,
+                                    main_s);
             if (st != DL_OK) return st;
         }
         return DL_OK;
@@ -263,9 +298,10 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
     std::unique_lock<std::mutex> lock;
     cudaStream_t side_s = main_s;
     if (!serial) {
-        if ((st = side_resources(&R)) != DL_OK) return st;
+        int dev = 0;
+        if ((st = side_resources(&R, &dev)) != DL_OK) return st;
         lock = std::unique_lock<std::mutex>(R->mu);
-        if ((st = create_side(*R)) != DL_OK) return st;
+        if ((st = create_side(*R, dev)) != DL_OK) return st;
         side_s = R->side;
         if ((st = cuda_status(cudaEventRecord(R->fork, main_s))) != DL_OK) return st;
         if ((st = cuda_status(cudaStreamWaitEvent(side_s, R->fork, 0))) != DL_OK) return st;

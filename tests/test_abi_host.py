@@ -40,6 +40,12 @@ def test_exports_every_declared_symbol(L):
     assert L.dl_version() == 200
 
 
+def test_shutdown_without_resources_is_a_no_op(L):
+    # nothing was created on this host (no GPU): no CUDA call is made
+    assert L.dl_shutdown() == 0
+    assert L.dl_shutdown() == 0
+
+
 def test_status_strings(L):
     for code in (0, -1, -2, -3, -4, -5, -6, -7, 12345):
         assert dl.status_string(code)
@@ -257,13 +263,13 @@ def test_values_mode_needs_one_learner(L):
     assert L.dl_pseudograd_stats(FAKE, None, 1, fb, 6.0, FAKE, FAKE, 0, None) == -6
 
 
-def _ring(L, fb, K, weights=None, present=None, min_quorum=1, ws=FAKE, nbytes=0):
+def _ring(L, fb, K, weights=None, present=None, min_quorum=1, ws=FAKE, nbytes=0, hop_stats=None):
     w = None if weights is None else np.ascontiguousarray(weights, np.float32)
     p = None if present is None else np.ascontiguousarray(present, np.uint8)
     return L.dl_ring_outer_step(FAKE, FAKE, _ptrs(*([FAKE] * K)), K, fb,
                                 None if w is None else w.ctypes.data,
                                 None if p is None else p.ctypes.data, min_quorum, 6.0, 0.7, 0.9,
-                                None, ws, nbytes, None)
+                                None, hop_stats, ws, nbytes, None)
 
 
 def test_ring_validation_and_quorum_rules(L):
@@ -274,6 +280,8 @@ def test_ring_validation_and_quorum_rules(L):
     assert _ring(L, fb, 0) == -1 and _ring(L, fb, 33) == -1
     assert _ring(L, fb, 3, nbytes=need - 1) == -6       # valid otherwise: short workspace
     assert _ring(L, fb, 3, ws=FAKE + 16, nbytes=need) == -2
+    assert _ring(L, fb, 3, nbytes=need, hop_stats=FAKE + 4) == -2  # stats need 8-byte alignment
+    assert _ring(L, fb, 3, nbytes=need - 1, hop_stats=FAKE + 8) == -6
     rng = np.random.default_rng(8)
     for _ in range(150):
         K = int(rng.integers(1, 9))

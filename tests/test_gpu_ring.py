@@ -175,3 +175,51 @@ def test_ring_quorum_failure_leaves_state_untouched(dl):
     assert e.value.status == -3
     torch.cuda.synchronize()
     assert np.array_equal(gd.cpu().numpy(), g) and np.array_equal(md.cpu().numpy(), m)
+
+
+def test_hop_statistics_match_the_oracle(dl):
+    """The hops accumulate the statistics of the partial sums they write
+    (no separate pass). Checked against the oracle's statistics of the same
+    fp32 values, to the statistics bar: P_0 = w_0 Delta_0 is formed exactly as
+    the oracle forms it, and P_1 is read back as D of a two-learner ring (a
+    third learner of weight 0 keeps both rings' first two hops identical)."""
+    K = 3
+    g, reps, m = _inputs(61, RAGGED, K)
+    off = np.concatenate([[0], np.cumsum(RAGGED)]).astype(np.int64)
+    F = dl.Fragment(RAGGED)
+    reps_d = [torch.from_numpy(r).cuda() for r in reps]
+    hs = dl.new_stats(2, F.T)
+    gd, md = torch.from_numpy(g).cuda(), torch.from_numpy(m).cuda()
+    ws = dl.ring_outer_step(gd, md, F, reps_d, weights=[1.0, 1.0, 0.0], hop_stats=hs)
+    g2, m2 = torch.from_numpy(g).cuda(), torch.from_numpy(m).cuda()
+    p1 = torch.empty_like(g2)
+    dl.ring_outer_step(g2, m2, F, reps_d[:2], delta_bar=p1)
+    torch.cuda.synchronize()
+    assert dl.read_device_status(ws) == 0
+    got = dl.stats_to_host(hs)
+    zero = np.zeros_like(g)
+    p0 = (np.float32(0.5) * (g - reps[0])).astype(np.float32)  # w_hat = 1/2 exactly
+    for row, vals in ((0, p0), (1, p1.cpu().numpy())):
+        st_o = oracle.stats(vals, [zero], off)
+        check_stats(st_o, {key: v[row:row + 1] for key, v in got.items()}, 1, len(RAGGED))
+
+
+def test_hop_statistics_of_a_long_ring(dl):
+    """Every row of the hop statistics is written, with counts and a spread
+    that grows with the partial sum."""
+    K = 6
+    g, reps, m = _inputs(62, RAGGED, K)
+    F = dl.Fragment(RAGGED)
+    hs = dl.new_stats(K - 1, F.T)
+    hs.fill_(-1)
+    dl.ring_outer_step(torch.from_numpy(g).cuda(), torch.from_numpy(m).cuda(), F,
+                       [torch.from_numpy(r).cuda() for r in reps], hop_stats=hs,
+                       weights=np.ones(K, np.float32))
+    torch.cuda.synchronize()
+    got = dl.stats_to_host(hs)
+    assert np.array_equal(got["count"], np.tile(np.asarray(RAGGED), (K - 1, 1)))
+    assert np.all(got["nonfinite"] == 0)
+    big = np.asarray(RAGGED) >= 1000
+    # P_s sums s + 1 independent pseudo-gradients of weight 1/K: sigma ~ sqrt(s + 1)
+    ratio = got["std"][-1, big] / got["std"][0, big]
+    assert np.all((ratio > 0.8 * np.sqrt(K - 1)) & (ratio < 1.25 * np.sqrt(K - 1))), ratio

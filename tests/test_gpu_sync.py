@@ -249,3 +249,20 @@ def test_rda_and_ring_modes_bitwise_equal_per_call(dl, mode):
         _assert_same(out["pipe"], out["calls"])
         assert dl.read_device_status(ms.workspace) == 0
         assert all(np.isfinite(x).all() for x in out["pipe"][0])
+
+
+def test_shutdown_releases_and_the_next_call_recreates(dl):
+    """dl_shutdown drops the side stream and events; the next pipelined call
+    creates them again and gives the same bits."""
+    K = 3
+    rng, g, sig = _model(8, K)
+    reps_d = [_dev(r) for r in _replicas(rng, g, sig, K)]
+    a, b = Run(dl, g), Run(dl, g)
+    ms = dl.ModelSync(a.frags, K)
+    ms.step(a.g, a.m, reps_d, delta_bar=a.db)
+    dl.shutdown()  # with a's work possibly still in flight
+    dl.shutdown()
+    ms.step(b.g, b.m, reps_d, delta_bar=b.db)
+    torch.cuda.synchronize()
+    _assert_same(a.host(), b.host())
+    assert dl.read_device_status(ms.workspace) == 0
