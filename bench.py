@@ -355,12 +355,11 @@ def ring_algo_bytes(S):
 
 
 def ring_launches(S):
-    """Kernels of one ring step per fragment: hop 0 (shift + hop), then per
-    later hop the statistics finalisation and the quantiser's three kernels,
-    and the hop (shift + hop, the last one alone)."""
+    """Kernels of one ring step per fragment: hop 0, then per later hop the
+    statistics finalisation, the quantiser's three kernels and the hop."""
     if S == 1:
         return 1
-    return 2 + 4 * (S - 1) + 2 * (S - 2) + 1
+    return 1 + 5 * (S - 1)
 
 
 def run_ring(args, rank, world, local):

@@ -17,10 +17,10 @@
 // statistics as it writes P, with the exact scheme of the statistics kernel
 // (float-float sums of y = P - c and of y^2 on a power-of-two offset, fp64
 // for values outside the fast range): the quantiser's statistics then cost
-// no extra pass over P. k_ring_shift computes each tensor's shift c first,
-// from the hop's own formula at the tensor's first 64 elements, with the
-// statistics kernel's rule, and stats_finish turns the partials into
-// mu, sigma, lo, hi.
+// no extra pass over P. Each block entering a tensor computes its shift c
+// (one warp, from the hop's own formula at the tensor's first 64 elements,
+// with the statistics kernel's rule; every block gets the same value), and
+// stats_finish turns the partials into mu, sigma, lo, hi.
 #include <math.h>
 #include <string.h>
 
@@ -40,7 +40,7 @@ struct RingArgs {
     const float* cb;        // its codebook [T][256] (DECODE)
     const int64_t* off;
     float* dbar;            // optional D (FINAL)
-    float* shift;           // [T] shifts of the new P (STATS)
+    float* shift;           // [T] shifts of the new P, for the finalisation (STATS)
     Partial* part;          // [T][gridDim.x] partial sums of the new P (STATS)
     int64_t n;
     int64_t n_chunks;
@@ -63,15 +63,13 @@ __device__ __forceinline__ void nesterov(float acc, float& th, float& mm, float 
     mm = m1;
 }
 
-// One warp per tensor: the shift of the P this hop writes, from P at the
-// tensor's first min(N, 64) elements (the hop's formula, bit for bit).
+// The shift of tensor t of the P this hop writes, computed by one warp from
+// P at the tensor's first min(N, 64) elements (the hop's formula, bit for
+// bit) with the statistics kernel's rule; every lane returns it. Each block
+// entering the tensor computes the same value.
 template <bool DECODE>
-__global__ void __launch_bounds__(kThreads) k_ring_shift(RingArgs a) {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__device__ __forceinline__ float ring_shift(const RingArgs& a, int t, int64_t o, int64_t N) {
     const int lane = threadIdx.x & 31;
-    if (t >= a.T) return;
-    const int64_t o = a.off[t];
-    const int64_t N = a.off[t + 1] - o;
     const int m = N < 64 ? static_cast<int>(N) : 64;
     const bool h0 = lane < m, h1 = lane + 32 < m;
     const float* cbt = a.cb + static_cast<int64_t>(t) * kNB;
@@ -80,11 +78,10 @@ __global__ void __launch_bounds__(kThreads) k_ring_shift(RingArgs a) {
     for (int h = 0; h < 2; ++h) {
         if (!(h ? h1 : h0)) continue;
         const int64_t i = o + lane + 32 * h;
-        const float dec = DECODE ? cbt[a.codes[i]] : 0.f;
-        v[h] = static_cast<double>(hop_value<DECODE>(a.g[i], a.r[i], dec, a.w));
+        const float dec = DECODE ? __ldg(cbt + __ldg(a.codes + i)) : 0.f;
+        v[h] = static_cast<double>(hop_value<DECODE>(__ldg(a.g + i), __ldg(a.r + i), dec, a.w));
     }
-    const float c = warp_shift(v[0], v[1], h0, h1, m);
-    if (lane == 0) a.shift[t] = c;
+    return warp_shift(v[0], v[1], h0, h1, m);
 }
 
 // Statistics of four P values of one group (the fast path when all four are
@@ -114,6 +111,7 @@ template <bool DECODE, bool FINAL, bool STATS>
 __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
     static_assert(!(FINAL && STATS), "the last hop's sum is not quantised");
     __shared__ float scb[kNB];
+    __shared__ float s_shift;
     __shared__ float red_ff[kWarps][4];
     __shared__ double red_side[kWarps][2];
     __shared__ int red_bad[kWarps];
@@ -133,19 +131,25 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
             if (t != cur_t) {
-                if (STATS) {
-                    if (cur_t >= 0)
-                        flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x +
-                                               blockIdx.x,
-                                      red_ff, red_side, red_bad);
-                    acc.reset();
-                    csh = __ldg(a.shift + t);
-                    small = (o1 - o0) < kSmallTensor;
+                if (STATS && cur_t >= 0)
+                    flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x + blockIdx.x,
+                                  red_ff, red_side, red_bad);
+                if (DECODE || STATS) {
+                    __syncthreads();  // every read of the previous tensor's scb / s_shift is done
+                    if (DECODE) scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
+                    if (STATS && tid < 32) {
+                        const float cs = ring_shift<DECODE>(a, t, o0, o1 - o0);
+                        if (tid == 0) {
+                            s_shift = cs;
+                            if (pa == o0) a.shift[t] = cs;  // the one block holding element o0
+                        }
+                    }
+                    __syncthreads();
                 }
-                if (DECODE) {
-                    __syncthreads();
-                    scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
-                    __syncthreads();
+                if (STATS) {
+                    acc.reset();
+                    csh = s_shift;
+                    small = (o1 - o0) < kSmallTensor;
                 }
                 cur_t = t;
             }
@@ -226,8 +230,8 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                       red_side, red_bad);
 }
 
-// One hop on s. With STATS, the shifts and zeroed partials of the new P
-// come first, and *grid_out is the hop's grid (the partials' J).
+// One hop on s. With STATS, the partials of the new P are zeroed first, and
+// *grid_out is the hop's grid (the partials' J).
 template <bool DECODE, bool FINAL, bool STATS>
 int launch_hop(const RingArgs& a, cudaStream_t s, int* grid_out = nullptr) {
     const void* k = reinterpret_cast<const void*>(k_ring_hop<DECODE, FINAL, STATS>);
@@ -237,8 +241,6 @@ int launch_hop(const RingArgs& a, cudaStream_t s, int* grid_out = nullptr) {
     if (STATS) {
         const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(a.T) * grid;
         if ((st = cuda_status(cudaMemsetAsync(a.part, 0, part_bytes, s))) != DL_OK) return st;
-        k_ring_shift<DECODE><<<(a.T * 32 + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
-        if ((st = launch_status()) != DL_OK) return st;
     }
     k_ring_hop<DECODE, FINAL, STATS><<<grid, kThreads, 0, s>>>(a);
     if (grid_out) *grid_out = grid;

@@ -27,7 +27,7 @@
 //              (k, t, j). Tensors shorter than 4096 elements and groups of
 //              rare huge, tiny (squares would leave the fp32 normal range) or
 //              non-finite values take an fp64 path.
-//  k_stats_fin one warp per (k, t): fixed-order fp64 sum of its J partials, then
+//  k_stats_fin one block per (k, t): fixed-order fp64 sum of its J partials, then
 //              mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population).
 // The result is deterministic: every sum has a fixed order.
 #include "dl_stats_acc.cuh"
@@ -237,16 +237,21 @@ struct FinArgs {
     double clip;
 };
 
-__global__ void __launch_bounds__(kThreads) k_stats_fin(FinArgs a) {
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= a.K * a.T) return;
+constexpr int kFinThreads = 128;
+
+// One block per (k, t): thread i sums partials i, i + 128, ... in order, then
+// a fixed butterfly per warp and the four warps in order.
+__global__ void __launch_bounds__(kFinThreads) k_stats_fin(FinArgs a) {
+    __shared__ double r1[kFinThreads / 32], r2[kFinThreads / 32];
+    __shared__ long long rb[kFinThreads / 32];
+    const int w = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = w % a.T;
     const int64_t N = a.off[t + 1] - a.off[t];
     double s1 = 0.0, s2 = 0.0;
     long long bad = 0;
     const Partial* pw = a.part + static_cast<int64_t>(w) * a.J;
-    for (int jj = lane; jj < a.J; jj += 32) {
+    for (int jj = threadIdx.x; jj < a.J; jj += kFinThreads) {
         const Partial p = pw[jj];
         s1 += p.s1;
         s2 += p.s2;
@@ -257,7 +262,21 @@ __global__ void __launch_bounds__(kThreads) k_stats_fin(FinArgs a) {
         s2 += __shfl_xor_sync(kFull, s2, sh);
         bad += __shfl_xor_sync(kFull, bad, sh);
     }
-    if (lane != 0) return;
+    if (lane == 0) {
+        r1[warp] = s1;
+        r2[warp] = s2;
+        rb[warp] = bad;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    s1 = r1[0];
+    s2 = r2[0];
+    bad = rb[0];
+    for (int i = 1; i < kFinThreads / 32; ++i) {
+        s1 += r1[i];
+        s2 += r2[i];
+        bad += rb[i];
+    }
     dl_stats st;
     st.count = N;
     st.nonfinite = bad;
@@ -298,8 +317,7 @@ int stats_finish(const int64_t* d_off, int T, int K, int J, const float* shift,
     f.K = K;
     f.J = J;
     f.clip = clip;
-    const int grid = (K * T * 32 + kThreads - 1) / kThreads;
-    k_stats_fin<<<grid, kThreads, 0, s>>>(f);
+    k_stats_fin<<<K * T, kFinThreads, 0, s>>>(f);
     return launch_status();
 }
 
