@@ -45,6 +45,11 @@
  *  - planner: longest-processing-time greedy; tensors sorted by size
  *    descending (index ascending on ties), each placed on the least-loaded
  *    fragment (lowest index on ties).
+ *
+ * Pins: every function is checked by the tests against what the pages and
+ * the mathematics fix, except oracle_rda_merge_outer_step, which is PARITY
+ * UNPINNED (the page names Radial-Directional Averaging without a formula;
+ * its tests check only the defining properties of the reading taken).
  */
 #include <float.h>
 #include <math.h>
