@@ -738,15 +738,27 @@ def cpu_baseline(wl, frags, host, budget_s=10.0):
     import oracle
 
     offsets = fragment_offsets(wl, frags)
+    oracle.lib()  # build and load it outside the timed passes
     total, passes = 0.0, 0
     while passes == 0 or total < budget_s:
         total += oracle_pass(wl, host, offsets)
         passes += 1
-    return {"value": wl.n_elems * passes / total, "unit": UNIT, "cores": oracle.threads(),
+    # one thread, on the first fragment (a whole pass would take minutes)
+    cores = oracle.threads()
+    n0 = int(offsets[0][-1])
+    oracle.set_threads(1)
+    try:
+        t1 = oracle_pass(wl, host[:1], offsets[:1])
+    finally:
+        oracle.set_threads(cores)
+    return {"value": wl.n_elems * passes / total, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"the whole workload ({wl.n_elems} elements x K={wl.K}, "
                       f"{len(frags)} fragments), full outer step (stats+quantise+merge+"
-                      f"Nesterov) per fragment, {passes} pass(es) in {total:.1f} s"}
+                      f"Nesterov) per fragment, {passes} pass(es) in {total:.1f} s",
+            "single_thread": {"value": n0 / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"fragment 0 ({n0} elements x K={wl.K}), one pass "
+                                        f"in {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
@@ -761,6 +773,7 @@ def run_reference(args, rank, world):
     frags = fragment_tensors(wl, frag_of)
     host = generate_host(wl, frags, pin=False)
     offsets = fragment_offsets(wl, frags)
+    oracle.lib()
     for _ in range(args.warmup):
         oracle_pass(wl, host, offsets)
     dt = sum(oracle_pass(wl, host, offsets) for _ in range(args.steps))

@@ -68,6 +68,8 @@ def lib():
         L.oracle_rda_merge_outer_step.restype = ctypes.c_int
         L.oracle_rda_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
                                                   f32, f32, vp]
+        L.oracle_set_threads.restype = None
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
         L.oracle_ring_outer_step.restype = ctypes.c_int
         L.oracle_ring_outer_step.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, f64, f32,
                                              f32, vp]
@@ -77,6 +79,11 @@ def lib():
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's later parallel loops (timing only)."""
+    lib().oracle_set_threads(int(n))
 
 
 def _f32(a):

@@ -74,6 +74,16 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Threads of the later parallel loops (n >= 1); timing only, no effect on
+ * any result (every parallel loop writes disjoint outputs). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* Fragment planner (Decoupled DiLoCo note, architecture item 4).           */
 
