@@ -11,8 +11,9 @@
 //   last hop:     instead of storing P, apply the outer Nesterov step with
 //                 D = P (and write D out if asked).
 // k_ring_hop<DECODE, FINAL, STATS> does one hop's element work: persistent
-// blocks over 8192-element chunks, the previous codebook of the current
-// tensor in shared memory, 128-bit loads and stores, 32-bit code loads. A
+// blocks, each over one contiguous run of 8192-element chunks (so a block
+// meets few tensors), the previous codebook of the current tensor in shared
+// memory, 128-bit loads and stores, 32-bit code loads. A
 // hop whose P is quantised next (STATS) also accumulates P's per-tensor
 // statistics as it writes P, with the exact scheme of the statistics kernel
 // (float-float sums of y = P - c and of y^2 on a power-of-two offset, fp64
@@ -121,7 +122,9 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
     bool small = false;
     Acc acc;
     acc.reset();
-    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    int64_t c0, c1;
+    block_chunks(a.n_chunks, c0, c1);
+    for (int64_t c = c0; c < c1; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + static_cast<int64_t>(kChunk), a.n);
         for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {
