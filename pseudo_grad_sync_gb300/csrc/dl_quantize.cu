@@ -3,10 +3,11 @@
 //
 // k_qparams    one thread per (k, t): the segment's quantiser parameters.
 // k_quantize   learner-major persistent grid: block b serves learner k = b % K
-//              and every J-th 8192-element chunk, so the K blocks reading one
-//              chunk of theta_g run together (theta_g crosses HBM once, then
-//              comes from L2); each chunk is loaded in two halves with
-//              128-bit loads. Per element of learner k:
+//              and the j-th of J contiguous runs of 8192-element chunks
+//              (j = b / K), so the K blocks reading one chunk of theta_g run
+//              together (theta_g crosses HBM once, then comes from L2) and a
+//              block meets few tensors; each chunk is loaded in two halves
+//              with 128-bit loads. Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
 //                  fp32 with one fma; when u is within a proven error guard of an integer
 //                  (or outside (0, 256)) the element is redone in fp64 with
@@ -155,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     int seg_t = -1;  // tensor whose parameters are in p
     int par = 0;
     SegRt p;
-    for (int64_t c = j; c < a.n_chunks; c += a.J) {
+    const int64_t c_lo = a.n_chunks * j / a.J, c_hi = a.n_chunks * (j + 1) / a.J;
+    for (int64_t c = c_lo; c < c_hi; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + kChunk, a.n);
         for (int t = tensor_containing(a.off, a.T, base); t < a.T; ++t) {

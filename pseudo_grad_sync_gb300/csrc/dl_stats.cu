@@ -12,9 +12,10 @@
 //              rounding of y unbiased (a shift with low-order bits below
 //              ulp(y) biases every rounding the same way).
 //  k_stats     learner-major persistent grid: block b serves learner
-//              k = b % K and every J-th 8192-element chunk, so the K blocks
-//              that read one chunk of theta_g run together and theta_g comes
-//              from HBM once, then from L2. A producer warp streams the
+//              k = b % K and the j-th of J contiguous runs of 8192-element
+//              chunks (j = b / K), so the K blocks that read one chunk of
+//              theta_g run together and theta_g comes from HBM once, then
+//              from L2. A producer warp streams the
 //              (theta_g, theta_k) tiles into a 3-stage shared-memory ring
 //              with bulk copies (TMA engine), 8 consumer warps compute from
 //              shared memory. Per thread: fp32
@@ -121,8 +122,8 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
     }
 }
 
-// Learner-major persistent grid: block b serves learner k = b % K and chunks
-// j, j + J, j + 2J, ... with j = b / K. The K blocks that read the same chunk
+// Learner-major persistent grid: block b serves learner k = b % K and the
+// j-th contiguous run of chunks, j = b / K. The K blocks that read the same chunk
 // of theta_g run side by side, so theta_g crosses HBM once and is served to
 // the other K - 1 from L2. A producer warp streams the (theta_g, theta_k)
 // tiles of those chunks into a STAGES-deep shared-memory ring with bulk
@@ -146,6 +147,9 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
+    // the contiguous chunk run [c_lo, c_hi) of block index j (the same for
+    // every learner, so the K blocks of one j read the same theta_g chunks)
+    const int64_t c_lo = a.n_chunks * j / a.J, c_hi = a.n_chunks * (j + 1) / a.J;
     const float* __restrict__ rk = a.r[k];
     const float* __restrict__ g = a.g;
     pipe_init<kStages>(&pb);
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t c = j; c < a.n_chunks; c += a.J) {
+            for (int64_t c = c_lo; c < c_hi; ++c) {
                 const int64_t base = c * kChunk;
                 const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
                 for (int o = 0; o < cn; o += kTile, ++it)
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     Acc acc;
     acc.reset();
     uint32_t it = 0;
-    for (int64_t c = j; c < a.n_chunks; c += a.J) {
+    for (int64_t c = c_lo; c < c_hi; ++c) {
         const int64_t base = c * kChunk;
         const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
         int t0 = tensor_containing(a.off, a.T, base);  // first tensor of the chunk
