@@ -95,6 +95,20 @@ __device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, ui
     qv = static_cast<uint32_t>(x);
 }
 
+// q (< 2^23) enters the histogram as qb = 0x4B000000 + q, the bit pattern of
+// the fp32 value 2^23 + q: word A of bin b gets one count plus q >> 19, word B
+// gets the low 19 bits of q (those of qb, as 0x4B000000 has none)
+constexpr uint32_t kQBits = 0x4B000000u;
+__device__ __forceinline__ void hist_add(uint32_t* __restrict__ hA, int b, uint32_t qb) {
+    atomicAdd(hA + b, (qb >> 19) + (kCountOne - (kQBits >> 19)));
+    atomicAdd(hA + kNB + b, qb & kLoMask);
+}
+
+// four codes as one 32-bit word, b0 in the lowest byte
+__device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+    return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 // bucket of one value and its histogram update; returns the code
 __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_t* __restrict__ hA) {
     const float uf = __fmaf_rn(d, p.q.s_f, p.q.c_f);
@@ -104,15 +118,16 @@ __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_
     int b = __float_as_int(tf) - kFloorMagicBits;
     const float bf = __fsub_rn(tf, kFloorMagic);
     const float fr = __fsub_rn(uf, bf);
-    uint32_t qv;
+    uint32_t qb;  // q on the bit grid of [2^23, 2^24): 0x4B000000 + q
     if (static_cast<unsigned>(b) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
         const float r = __fsub_rn(d, __fmaf_rn(bf, p.q.w_f, p.q.lo_f));
-        qv = __float_as_uint(__fmaf_rn(r, p.q.scale, p.q.qoff)) & 0x7FFFFFu;
+        qb = __float_as_uint(__fmaf_rn(r, p.q.scale, p.q.qoff));
     } else {
+        uint32_t qv;
         rare_code(d, p.q, b, qv);
+        qb = kQBits + qv;
     }
-    atomicAdd(hA + b, kCountOne + (qv >> 19));
-    atomicAdd(hA + kNB + b, qv & kLoMask);
+    hist_add(hA, b, qb);
     return static_cast<uint32_t>(b);
 }
 
@@ -121,8 +136,7 @@ __device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p, uint32_t
     int b;
     uint32_t qv;
     rare_code(d, p.q, b, qv);
-    atomicAdd(hA + b, kCountOne + (qv >> 19));
-    atomicAdd(hA + kNB + b, qv & kLoMask);
+    hist_add(hA, b, kQBits + qv);
     return static_cast<uint32_t>(b);
 }
 
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                             const uint32_t b1 = encode_fast(__fsub_rn(gv[q].y, rv[q].y), p, hA);
                             const uint32_t b2 = encode_fast(__fsub_rn(gv[q].z, rv[q].z), p, hA);
                             const uint32_t b3 = encode_fast(__fsub_rn(gv[q].w, rv[q].w), p, hA);
-                            c4[tid + (h + q) * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                            c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
                         }
                     } else {
                         for (int q = 0; q < kGroups / 2; ++q) {
@@ -210,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                             const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
                             const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
                             const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
-                            c4[tid + (h + q) * kThreads] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                            c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
                         }
                     }
                 }
