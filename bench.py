@@ -216,7 +216,7 @@ class DeviceRun:
                 events[f][3].record(stream)
 
 
-LAUNCHES_PER_FRAGMENT = {"stats": 3, "quantize": 3, "merge": 1}
+LAUNCHES_PER_FRAGMENT = {"stats": 3, "quantize": 2, "merge": 1}
 
 
 def traffic_record(name):
@@ -337,7 +337,7 @@ def run_learner(args, rank, world, local):
                      "traffic": None, "kernel": {"stats": "k_stats",
                                                  "quantize": "k_quantize"}[dominant],
                      "note": f"peak = {peak_kind} copy bandwidth"},
-        "clocks": clk, "gpu_launches": args.steps * 6, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * 5, "e2e": None,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -356,10 +356,10 @@ def ring_algo_bytes(S):
 
 def ring_launches(S):
     """Kernels of one ring step per fragment: hop 0, then per later hop the
-    statistics finalisation, the quantiser's three kernels and the hop."""
+    statistics finalisation, the quantiser's two kernels and the hop."""
     if S == 1:
         return 1
-    return 1 + 5 * (S - 1)
+    return 1 + 4 * (S - 1)
 
 
 def run_ring(args, rank, world, local):
@@ -504,7 +504,7 @@ def run_rda(args, rank, world, local):
                      "note": f"{ab} algorithmic B/elem per step; peak = {peak_kind} copy "
                              "bandwidth"},
         "per_call_ms_per_step": tot_calls / args.steps,
-        "clocks": clk, "gpu_launches": args.steps * len(frags) * 10, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * 9, "e2e": None,
         "gpu_launches_note": "kernels in the headline dl_outer_sync (DL_SYNC_RDA) region; the "
                              "per-call sequence, timed after it, launches as many again",
     }

@@ -1,13 +1,14 @@
 // Uniform quantisation with clipping and a bucket-mean codebook (INTELLECT-1
 // notes, section 4.1 steps 2-4), fused with the uint8 encode.
 //
-// k_qparams    one thread per (k, t): the segment's quantiser parameters.
 // k_quantize   learner-major persistent grid: block b serves learner k = b % K
 //              and the j-th of J contiguous runs of 8192-element chunks
 //              (j = b / K), so the K blocks reading one chunk of theta_g run
 //              together (theta_g crosses HBM once, then comes from L2) and a
-//              block meets few tensors; each chunk is loaded in two halves
-//              with 128-bit loads. Per element of learner k:
+//              block meets few tensors; thread 0 derives a tensor's
+//              quantiser parameters from its statistics when the block
+//              enters it (no separate launch); each chunk is loaded in two
+//              halves with 128-bit loads. Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
 //                  fp32 with one fma; when u is within a proven error guard of an integer
 //                  (or outside (0, 256)) the element is redone in fp64 with
@@ -52,7 +53,6 @@ struct QuantArgs {
     uint8_t* codes[DL_MAX_LEARNERS];
     const int64_t* off;
     const dl_stats* stats;
-    SegRt* seg;               // [K*T]
     unsigned long long* acc;  // [K*T*256] x (count, biased residual sum)
     float* cb;
     uint32_t* counts;
@@ -70,14 +70,11 @@ constexpr uint32_t kQMax = (1u << 23) - 1;
 constexpr float kFloorMagic = 12582912.0f;    // 1.5 * 2^23
 constexpr int kFloorMagicBits = 0x4B400000;  // its fp32 bit pattern
 
-__global__ void __launch_bounds__(kThreads) k_qparams(QuantArgs a) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= a.K * a.T) return;
-    const dl_stats st = a.stats[i];
+__device__ __forceinline__ SegRt seg_params(const dl_stats& st) {
     SegRt p;
     p.q = seg_quant(st.lo, st.hi, st.nonfinite);
     p.mid_g = 0.5f - p.q.guard;
-    a.seg[i] = p;
+    return p;
 }
 
 // fp64 path of one element: the exact bucket rule and residual
@@ -156,6 +153,7 @@ template <bool VALUES>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     __shared__ uint32_t l1[2][2 * kNB];             // [parity][word A bins | word B bins]
     __shared__ unsigned long long l2[2 * kNB];       // [count bins | residual-sum bins]
+    __shared__ SegRt s_seg;                          // parameters of the current tensor
 
     const int tid = threadIdx.x;
     const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
@@ -180,8 +178,11 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            if (t != seg_t) {
-                p = a.seg[static_cast<int64_t>(k) * a.T + t];
+            if (t != seg_t) {  // block-uniform: thread 0 derives the parameters
+                __syncthreads();  // every thread has its copy of the previous ones
+                if (tid == 0) s_seg = seg_params(a.stats[static_cast<int64_t>(k) * a.T + t]);
+                __syncthreads();
+                p = s_seg;
                 seg_t = t;
             }
             const bool full = (pa == base) && (pb == base + kChunk);
@@ -283,8 +284,6 @@ __global__ void __launch_bounds__(kThreads) k_cb_fin(QuantArgs a) {
     if (a.counts) a.counts[idx] = static_cast<uint32_t>(cnt);
 }
 
-size_t seg_bytes(int K, int T) { return align256(sizeof(SegRt) * static_cast<size_t>(K) * T); }
-
 size_t acc_bytes(int K, int T) {
     return align256(sizeof(unsigned long long) * 2 * static_cast<size_t>(K) * T * kNB);
 }
@@ -297,7 +296,7 @@ using namespace dl;
 extern "C" size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    return kWsHeader + seg_bytes(K, f.T) + acc_bytes(K, f.T);
+    return kWsHeader + acc_bytes(K, f.T);
 }
 
 extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
@@ -337,8 +336,7 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     a.stats = d_stats;
     char* ws = static_cast<char*>(d_workspace);
     a.status = reinterpret_cast<uint32_t*>(ws);
-    a.seg = reinterpret_cast<SegRt*>(ws + kWsHeader);
-    a.acc = reinterpret_cast<unsigned long long*>(ws + kWsHeader + seg_bytes(K, f.T));
+    a.acc = reinterpret_cast<unsigned long long*>(ws + kWsHeader);
     a.cb = d_codebook;
     a.counts = d_counts;
     a.n = f.n;
@@ -348,9 +346,6 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, acc_bytes(K, f.T), s))) != DL_OK) return st;
-    const int segs = K * f.T;
-    k_qparams<<<(segs + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
-    if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
         const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true>)
                                   : reinterpret_cast<const void*>(k_quantize<false>);
