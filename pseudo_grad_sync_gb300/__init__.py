@@ -119,6 +119,43 @@ def status_string(status: int) -> str:
     return lib().dl_status_string(status).decode()
 
 
+_F32 = (torch.float32,)
+_U8 = (torch.uint8,)
+_I64 = (torch.int64,)
+_U32 = tuple(d for d in (torch.int32, getattr(torch, "uint32", None)) if d is not None)
+
+
+def _need(t, dtypes, n, name):
+    """The C ABI takes raw pointers and sizes from the fragment layout; check
+    here what it cannot: a contiguous tensor of the right element type with at
+    least n elements (None passes: the ABI decides whether NULL is allowed).
+    The device is checked by _cuda once all of a call's tensors passed."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < n:
+        raise ValueError(f"{name}: {t.numel()} elements, need at least {n}")
+
+
+def _cuda(*items):
+    """After the per-tensor checks: every tensor given (or in a list given)
+    lives on a CUDA device."""
+    for it in items:
+        for t in (it if isinstance(it, (list, tuple)) else [it]):
+            if t is not None and t.device.type != "cuda":
+                raise ValueError(f"tensors must be on a CUDA device, found one on {t.device}")
+
+
+def _need_all(ts, dtypes, n, name):
+    for i, t in enumerate(ts):
+        _need(t, dtypes, n, f"{name}[{i}]")
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -196,6 +233,11 @@ def pseudograd_stats(theta_g, replicas, frag: Fragment, clip_sigmas=6.0, stats=N
     need = stats_workspace_bytes(frag, K)
     if workspace is None:
         workspace = new_workspace(need, theta_g.device)
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need_all(replicas or [], _F32, frag.n, "replicas")
+    _need(stats, _I64, K * frag.T * 6, "stats")
+    _need(workspace, _U8, 0, "workspace")
+    _cuda(theta_g, replicas or [], stats, workspace)
     _check("dl_pseudograd_stats", lib().dl_pseudograd_stats(
         _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
         float(clip_sigmas), _ptr(stats),
@@ -214,6 +256,14 @@ def quantize(theta_g, replicas, frag: Fragment, stats, codes=None, codebook=None
         codebook = torch.empty((K, frag.T, DL_NBUCKETS), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(quantize_workspace_bytes(frag, K), dev)
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need_all(replicas or [], _F32, frag.n, "replicas")
+    _need(stats, _I64, K * frag.T * 6, "stats")
+    _need_all(codes, _U8, frag.n, "codes")
+    _need(codebook, _F32, K * frag.T * DL_NBUCKETS, "codebook")
+    _need(counts, _U32, K * frag.T * DL_NBUCKETS, "counts")
+    _need(workspace, _U8, 0, "workspace")
+    _cuda(theta_g, replicas or [], stats, codes, codebook, counts, workspace)
     _check("dl_quantize", lib().dl_quantize(
         _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
         _ptr(stats), _ptr_array(codes),
@@ -228,11 +278,26 @@ def merge_outer_step(theta_g, momentum, frag: Fragment, codes=None, codebook=Non
         K = len(codes) if codes is not None else len(replicas)
     w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
     p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need(momentum, _F32, frag.n, "momentum")
+    _need_all(codes or [], _U8, frag.n, "codes")
+    _need(codebook, _F32, K * frag.T * DL_NBUCKETS, "codebook")
+    _need_all(replicas or [], _F32, frag.n, "replicas")
+    _need(delta_bar, _F32, frag.n, "delta_bar")
+    _host_k(w, p, K)
+    _cuda(theta_g, momentum, codes or [], codebook, replicas or [], delta_bar)
     _check("dl_merge_outer_step", lib().dl_merge_outer_step(
         _ptr(theta_g), _ptr(momentum), None if codes is None else _ptr_array(codes),
         _ptr(codebook), None if replicas is None else _ptr_array(replicas), K, frag.c,
         None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
         int(min_quorum), float(lr), float(mu), _ptr(delta_bar), _stream(stream)))
+
+
+def _host_k(weights, present, K):
+    """Host arrays the ABI reads K entries of."""
+    for name, arr in (("weights", weights), ("present", present)):
+        if arr is not None and arr.size < K:
+            raise ValueError(f"{name}: {arr.size} entries, need {K}")
 
 
 def _jobs(frags, theta_g=None, momentum=None, replicas=None, weights=None, present=None,
@@ -246,9 +311,12 @@ def _jobs(frags, theta_g=None, momentum=None, replicas=None, weights=None, prese
         job = arr[j]
         job.frag = ctypes.pointer(F._c)
         if theta_g is not None:
+            _need(theta_g[j], _F32, F.n, f"theta_g[{j}]")
+            _need(momentum[j], _F32, F.n, f"momentum[{j}]")
             job.theta_g = theta_g[j].data_ptr()
             job.momentum = momentum[j].data_ptr()
         if replicas is not None:
+            _need_all(replicas[j], _F32, F.n, f"replicas[{j}]")
             ra = _ptr_array(replicas[j])
             keep.append(ra)
             job.theta_k = ctypes.cast(ra, ctypes.c_void_p)
@@ -261,6 +329,7 @@ def _jobs(frags, theta_g=None, momentum=None, replicas=None, weights=None, prese
             keep.append(pr)
             job.present = pr.ctypes.data
         if delta_bar is not None and delta_bar[j] is not None:
+            _need(delta_bar[j], _F32, F.n, f"delta_bar[{j}]")
             job.delta_bar_out = delta_bar[j].data_ptr()
     return arr, keep
 
@@ -281,6 +350,9 @@ def outer_sync(frags, theta_g, momentum, replicas, K, workspace=None, weights=No
     arr, keep = _jobs(frags, theta_g, momentum, replicas, weights, present, delta_bar)
     if workspace is None and not flags & DL_SYNC_UNQUANTIZED:
         workspace = new_workspace(outer_sync_workspace_bytes(frags, K, flags), theta_g[0].device)
+    _need(workspace, _U8, 0, "workspace")
+    _cuda(workspace, list(theta_g), list(momentum), [r for rs in replicas for r in rs],
+          [d for d in (delta_bar or [])])
     nbytes = 0 if workspace is None else workspace.numel()
     _check("dl_outer_sync", lib().dl_outer_sync(
         arr, len(frags), K, float(clip_sigmas), int(min_quorum), float(lr), float(mu), int(flags),
@@ -309,6 +381,15 @@ def rda_merge_outer_step(theta_g, momentum, frag: Fragment, codes, codebook, cou
         workspace = new_workspace(rda_workspace_bytes(frag, K), theta_g.device)
     w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
     p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need(momentum, _F32, frag.n, "momentum")
+    _need_all(codes, _U8, frag.n, "codes")
+    _need(codebook, _F32, K * frag.T * DL_NBUCKETS, "codebook")
+    _need(counts, _U32, K * frag.T * DL_NBUCKETS, "counts")
+    _need(delta_bar, _F32, frag.n, "delta_bar")
+    _need(workspace, _U8, 0, "workspace")
+    _host_k(w, p, K)
+    _cuda(theta_g, momentum, codes, codebook, counts, delta_bar, workspace)
     _check("dl_rda_merge_outer_step", lib().dl_rda_merge_outer_step(
         _ptr(theta_g), _ptr(momentum), _ptr_array(codes), _ptr(codebook), _ptr(counts), K,
         frag.c, None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
@@ -333,6 +414,17 @@ def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, p
         workspace = new_workspace(ring_workspace_bytes(frag), theta_g.device)
     w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32)
     p = None if present is None else np.ascontiguousarray(present, dtype=np.uint8)
+    K = len(replicas)
+    _host_k(w, p, K)
+    S = K if p is None else int(np.count_nonzero(p[:K]))
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need(momentum, _F32, frag.n, "momentum")
+    _need_all([r for k, r in enumerate(replicas) if p is None or p[k]], _F32, frag.n, "replicas")
+    _need(delta_bar, _F32, frag.n, "delta_bar")
+    _need(hop_stats, _I64, max(S - 1, 0) * frag.T * 6, "hop_stats")
+    _need(workspace, _U8, 0, "workspace")
+    _cuda(theta_g, momentum, [r for k, r in enumerate(replicas) if p is None or p[k]], delta_bar,
+          hop_stats, workspace)
     _check("dl_ring_outer_step", lib().dl_ring_outer_step(
         _ptr(theta_g), _ptr(momentum), _ptr_array(replicas), len(replicas), frag.c,
         None if w is None else w.ctypes.data, None if p is None else p.ctypes.data,
@@ -344,11 +436,15 @@ def ring_outer_step(theta_g, momentum, frag: Fragment, replicas, weights=None, p
 def selftest_wait_timeout(workspace, polls=1000, stream=None):
     """Run one bounded wait that nothing completes (dl_selftest_wait_timeout);
     the workspace's status word then reports it."""
+    _need(workspace, _U8, 4, "workspace")
+    _cuda(workspace)
     _check("dl_selftest_wait_timeout",
            lib().dl_selftest_wait_timeout(_ptr(workspace), int(polls), _stream(stream)))
 
 
 def read_device_status(workspace, stream=None) -> int:
+    _need(workspace, _U8, 4, "workspace")
+    _cuda(workspace)
     v = ctypes.c_uint32(0)
     _check("dl_read_device_status",
            lib().dl_read_device_status(_ptr(workspace), ctypes.byref(v), _stream(stream)))
