@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                 const float4* g4 = reinterpret_cast<const float4*>(a.g + base);
                 const float4* r4 = reinterpret_cast<const float4*>(a.r + base);
                 const uint32_t* c4 = reinterpret_cast<const uint32_t*>(a.codes + base);
-#pragma unroll 2
+#pragma unroll 4
                 for (int j = 0; j < kGroups; ++j) {
                     const int gi = tid + j * kThreads;
                     float4 gv = FINAL ? g4[gi] : __ldg(g4 + gi);  // the last hop writes theta_g
