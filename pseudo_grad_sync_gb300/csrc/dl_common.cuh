@@ -336,4 +336,10 @@ int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items);
 int blocks_per_learner(const void* kernel, int threads, size_t smem, int K, int64_t n_chunks);
 int cuda_status(cudaError_t e);
 int launch_status();
+// dl_pseudograd_stats; share_sms: at most one of its blocks resident per SM
+// (same grid, same results)
+int pseudograd_stats_shared(const float* theta_g, const float* const* theta_k, int32_t K,
+                            const dl_fragment* frag, double clip_sigmas, dl_stats* d_stats,
+                            void* d_workspace, size_t workspace_bytes, void* stream,
+                            bool share_sms);
 }  // namespace dl

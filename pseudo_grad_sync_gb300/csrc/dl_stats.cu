@@ -47,7 +47,8 @@ struct StatsArgs {
     int64_t n_chunks;
     int T;
     int K;
-    int J;  // blocks per learner
+    int J;    // chunk runs per learner: the partition of the sums, fixed per fragment and K
+    int RPB;  // runs per block: block j takes runs j * RPB .. (j + 1) * RPB - 1
     double clip;
 };
 
@@ -147,9 +148,11 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
-    // the contiguous chunk run [c_lo, c_hi) of block index j (the same for
-    // every learner, so the K blocks of one j read the same theta_g chunks)
-    const int64_t c_lo = a.n_chunks * j / a.J, c_hi = a.n_chunks * (j + 1) / a.J;
+    // chunk run r is [n_chunks r / J, n_chunks (r + 1) / J); block j takes the
+    // adjacent runs [j RPB, (j + 1) RPB) (the same for every learner, so the K
+    // blocks of one j read the same theta_g chunks). The sums restart at every
+    // run, so the result depends on J only, not on how many blocks share them.
+    const int r_lo = j * a.RPB, r_hi = min(a.J, r_lo + a.RPB);
     const float* __restrict__ rk = a.r[k];
     const float* __restrict__ g = a.g;
     pipe_init<kStages>(&pb);
@@ -157,79 +160,87 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t c = c_lo; c < c_hi; ++c) {
-                const int64_t base = c * kChunk;
-                const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-                for (int o = 0; o < cn; o += kTile, ++it)
-                    pipe_produce<kTile, kStages>(&pb, sg, sr, g, rk, base + o, min(kTile, cn - o), it, a.status);
+            for (int r = r_lo; r < r_hi; ++r) {
+                const int64_t c_hi = a.n_chunks * (r + 1) / a.J;
+                for (int64_t c = a.n_chunks * r / a.J; c < c_hi; ++c) {
+                    const int64_t base = c * kChunk;
+                    const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+                    for (int o = 0; o < cn; o += kTile, ++it)
+                        pipe_produce<kTile, kStages>(&pb, sg, sr, g, rk, base + o, min(kTile, cn - o),
+                                                     it, a.status);
+                }
             }
         }
         return;
     }
 
-    Partial* part_k = a.part + static_cast<int64_t>(k) * a.T * a.J + j;  // slot (k, t, j) at t * J
-    int cur_t = -1;
-    float csh = 0.f;
-    bool small = false;
-    Acc acc;
-    acc.reset();
     uint32_t it = 0;
-    for (int64_t c = c_lo; c < c_hi; ++c) {
-        const int64_t base = c * kChunk;
-        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        int t0 = tensor_containing(a.off, a.T, base);  // first tensor of the chunk
-        for (int o = 0; o < cn; o += kTile, ++it) {
-            const int s = static_cast<int>(it % kStages);
-            const int64_t tb = base + o;
-            const int tn = min(kTile, cn - o);
-            const int tvec = tn & ~3;  // elements staged in shared memory
-            const int64_t tend = tb + tn;
-            wait_or_flag(&pb.full[s], (it / kStages) & 1u, a.status);
-            const float* tg = sg + s * kTile;
-            const float* tr = sr + s * kTile;
-            for (int t = t0; t < a.T; ++t) {
-                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-                if (o0 >= tend) break;
-                const int64_t pa = o0 > tb ? o0 : tb;
-                const int64_t pe = o1 < tend ? o1 : tend;
-                if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
-                if (pa >= pe) continue;
-                if (t != cur_t) {
-                    if (cur_t >= 0)
-                        flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
-                    cur_t = t;
-                    csh = __ldg(a.shift + k * a.T + t);
-                    small = (o1 - o0) < kSmallTensor;
-                    acc.reset();
-                }
-                if (pa == tb && pe == tb + kTile && !small) {
-                    add_tile<VALUES>(acc, tg, tr, tid, csh);
-                } else {
-                    for (int64_t e = pa + tid; e < pe; e += kThreads) {
-                        const int l = static_cast<int>(e - tb);
-                        const float gv = l < tvec ? tg[l] : __ldg(g + e);
-                        const float rv = VALUES ? 0.f : (l < tvec ? tr[l] : __ldg(rk + e));
-                        const float d = __fsub_rn(gv, rv);
-                        const float y = __fsub_rn(d, csh);
-                        const float ay = fabsf(y);
-                        if (!small && fast_range(ay)) {
-                            if (ay > acc.yt)
-                                rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
-                            ff_add(acc.s1h, acc.s1l, y);
-                            sq_add(acc.s2h, acc.s2l, y);
-                        } else {
-                            acc.side = true;
-                            side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
-                        }
+    for (int r = r_lo; r < r_hi; ++r) {
+        // slot (k, t, r) of this run's sums sits at part_k + t * J
+        Partial* part_k = a.part + static_cast<int64_t>(k) * a.T * a.J + r;
+        int cur_t = -1;
+        float csh = 0.f;
+        bool small = false;
+        Acc acc;
+        acc.reset();
+        const int64_t c_lo = a.n_chunks * r / a.J, c_hi = a.n_chunks * (r + 1) / a.J;
+        for (int64_t c = c_lo; c < c_hi; ++c) {
+            const int64_t base = c * kChunk;
+            const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+            int t0 = tensor_containing(a.off, a.T, base);  // first tensor of the chunk
+            for (int o = 0; o < cn; o += kTile, ++it) {
+                const int s = static_cast<int>(it % kStages);
+                const int64_t tb = base + o;
+                const int tn = min(kTile, cn - o);
+                const int tvec = tn & ~3;  // elements staged in shared memory
+                const int64_t tend = tb + tn;
+                wait_or_flag(&pb.full[s], (it / kStages) & 1u, a.status);
+                const float* tg = sg + s * kTile;
+                const float* tr = sr + s * kTile;
+                for (int t = t0; t < a.T; ++t) {
+                    const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+                    if (o0 >= tend) break;
+                    const int64_t pa = o0 > tb ? o0 : tb;
+                    const int64_t pe = o1 < tend ? o1 : tend;
+                    if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
+                    if (pa >= pe) continue;
+                    if (t != cur_t) {
+                        if (cur_t >= 0)
+                            flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
+                        cur_t = t;
+                        csh = __ldg(a.shift + k * a.T + t);
+                        small = (o1 - o0) < kSmallTensor;
+                        acc.reset();
                     }
-                    renorm(acc.s2h, acc.s2l);
+                    if (pa == tb && pe == tb + kTile && !small) {
+                        add_tile<VALUES>(acc, tg, tr, tid, csh);
+                    } else {
+                        for (int64_t e = pa + tid; e < pe; e += kThreads) {
+                            const int l = static_cast<int>(e - tb);
+                            const float gv = l < tvec ? tg[l] : __ldg(g + e);
+                            const float rv = VALUES ? 0.f : (l < tvec ? tr[l] : __ldg(rk + e));
+                            const float d = __fsub_rn(gv, rv);
+                            const float y = __fsub_rn(d, csh);
+                            const float ay = fabsf(y);
+                            if (!small && fast_range(ay)) {
+                                if (ay > acc.yt)
+                                    rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                                ff_add(acc.s1h, acc.s1l, y);
+                                sq_add(acc.s2h, acc.s2l, y);
+                            } else {
+                                acc.side = true;
+                                side_add(d, csh, acc.s1d, acc.s2d, acc.bad);
+                            }
+                        }
+                        renorm(acc.s2h, acc.s2l);
+                    }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pb.empty[s]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pb.empty[s]);
         }
+        if (cur_t >= 0) flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
     }
-    if (cur_t >= 0) flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
 }
 
 struct FinArgs {
@@ -338,9 +349,17 @@ extern "C" size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K) {
            align256(sizeof(Partial) * static_cast<size_t>(f.T) * kMaxBlocksTotal);
 }
 
-extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* theta_k, int32_t K,
-                                   const dl_fragment* frag, double clip_sigmas, dl_stats* d_stats,
-                                   void* d_workspace, size_t workspace_bytes, void* stream) {
+namespace dl {
+// The statistics call; with share_sms the grid has half as many blocks, each
+// taking two chunk runs in turn, so that one block per SM leaves registers for
+// two quantiser blocks: dl_outer_sync uses it for the statistics of the next
+// fragment, which then share each SM with the quantiser of the current one
+// instead of taking it whole. The runs (the partition of the sums) are the
+// same either way, so the results are bitwise the same.
+int pseudograd_stats_shared(const float* theta_g, const float* const* theta_k, int32_t K,
+                            const dl_fragment* frag, double clip_sigmas, dl_stats* d_stats,
+                            void* d_workspace, size_t workspace_bytes, void* stream,
+                            bool share_sms) {
     HostFrag f;
     int st = check_fragment(frag, &f);
     if (st != DL_OK) return st;
@@ -383,14 +402,19 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
         shallow ? (values ? reinterpret_cast<const void*>(k_stats<2, 3, true>)
                           : reinterpret_cast<const void*>(k_stats<2, 3, false>))
                 : reinterpret_cast<const void*>(k_stats<3, 2, false>);
-    const size_t smem = sizeof(float) * 2 * (shallow ? 2 : 3) * kTile;
+    const size_t smem_used = sizeof(float) * 2 * (shallow ? 2 : 3) * kTile;
+    const size_t smem = smem_used;
     if (a.n_chunks > 0) {
         if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem)))) != DL_OK)
             return st;
-        a.J = blocks_per_learner(kern, kPipeThreads, smem, K, a.n_chunks);
+        a.J = blocks_per_learner(kern, kPipeThreads, smem_used, K, a.n_chunks);
         if (a.J > max_blocks_per_learner(K)) a.J = max_blocks_per_learner(K);
     }
+    // one block per run, or, sharing the SMs, one per two runs (one block per
+    // SM where the full grid has two)
+    a.RPB = share_sms && a.J > 1 ? 2 : 1;
+    const int JB = (a.J + a.RPB - 1) / a.RPB;  // blocks per learner
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(K) * f.T * a.J;
@@ -401,11 +425,19 @@ extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* the
     if ((st = launch_status()) != DL_OK) return st;
     if (a.n_chunks > 0) {
         if (shallow)
-            values ? k_stats<2, 3, true><<<K * a.J, kPipeThreads, smem, s>>>(a)
-                   : k_stats<2, 3, false><<<K * a.J, kPipeThreads, smem, s>>>(a);
+            values ? k_stats<2, 3, true><<<K * JB, kPipeThreads, smem, s>>>(a)
+                   : k_stats<2, 3, false><<<K * JB, kPipeThreads, smem, s>>>(a);
         else
-            k_stats<3, 2, false><<<K * a.J, kPipeThreads, smem, s>>>(a);
+            k_stats<3, 2, false><<<K * JB, kPipeThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     return stats_finish(a.off, f.T, K, a.J, a.shift, a.part, a.clip, d_stats, s);
+}
+}  // namespace dl
+
+extern "C" int dl_pseudograd_stats(const float* theta_g, const float* const* theta_k, int32_t K,
+                                   const dl_fragment* frag, double clip_sigmas, dl_stats* d_stats,
+                                   void* d_workspace, size_t workspace_bytes, void* stream) {
+    return pseudograd_stats_shared(theta_g, theta_k, K, frag, clip_sigmas, d_stats, d_workspace,
+                                   workspace_bytes, stream, false);
 }

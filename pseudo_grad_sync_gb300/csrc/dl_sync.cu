@@ -316,8 +316,8 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
         if (!serial && j >= 2 &&
             (st = cuda_status(cudaStreamWaitEvent(side_s, R->quant_done[b], 0))) != DL_OK)
             break;
-        st = dl_pseudograd_stats(job.theta_g, p.rep, p.np, job.frag, clip_sigmas, stats_arr[b],
-                                 stats_ws, L.stats_ws, side_s);
+        st = pseudograd_stats_shared(job.theta_g, p.rep, p.np, job.frag, clip_sigmas, stats_arr[b],
+                                     stats_ws, L.stats_ws, side_s, !serial);
         if (st != DL_OK) break;
         if (!serial) {
             if ((st = cuda_status(cudaEventRecord(R->stats_done[b], side_s))) != DL_OK) break;
