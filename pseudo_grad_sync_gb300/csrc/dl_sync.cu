@@ -15,7 +15,11 @@
 //   main: wait stats_done[b]; quantize(f) from S[b]; record quant_done[b];
 //         merge(f)
 // The side stream forks from the caller's stream at entry and joins it at
-// exit, so on return every effect of the call is ordered on `stream`.
+// exit, so on return every effect of the call is ordered on `stream`. The
+// statistics run at one block per SM here (two chunk runs per block, the same
+// runs as the full grid, so the same sums): a statistics block then leaves
+// room on its SM for two quantiser blocks, and the kernels share the SMs
+// instead of taking turns.
 #include <stdint.h>
 #include <string.h>
 
