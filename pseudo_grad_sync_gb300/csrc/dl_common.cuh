@@ -103,37 +103,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
-// Stage [base, base+cn) of src into shared memory: the 16-byte multiple goes
-// through one bulk copy issued by thread 0, the 0..3 trailing floats through
-// plain loads. Every thread returns true when the data is visible to it;
-// on a copy that never lands, all threads return false and the status word
-// records it. `iter` counts completed phases of `bar`.
-__device__ __forceinline__ bool stage_chunk(float* dst, const float* src, int cn, uint64_t* bar,
-                                            uint32_t iter, int* flag, uint32_t* status) {
-    const int nvec = cn >> 2;
-    if (threadIdx.x == 0) {
-        fence_proxy_async();
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvec) * 16u);
-        if (nvec > 0) bulk_copy_g2s(dst, src, static_cast<uint32_t>(nvec) * 16u, bar);
-    }
-    const int tail = cn & 3;
-    if (static_cast<int>(threadIdx.x) < tail) dst[nvec * 4 + threadIdx.x] = src[nvec * 4 + threadIdx.x];
-    if (threadIdx.x == 0) {
-        bool ok = mbar_wait_bounded(bar, iter & 1u);
-        if (!ok) {
-            atomicOr(status, kDevErrCopyTimeout);
-            mbar_wait_bounded(bar, iter & 1u);  // give the copy one more bounded chance to land
-        }
-        *flag = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (*flag == 0) return false;
-    // acquire the phase thread 0 saw complete (returns at once in every thread)
-    (void)mbar_try_wait(bar, iter & 1u);
-    return true;
-}
-
-// ---------------------------------------------------------------------------
 // Tile pipeline: a producer warp streams (theta_g, theta_k) tiles of TILE
 // elements into a ring of STAGES shared-memory stages with bulk copies;
 // consumer warps wait on the stage's "full" mbarrier and release it through
