@@ -592,7 +592,8 @@ def run_ours(args, rank, world, local):
                        "frac": gbs / peak}
     full_gbs = (sum(ab.values()) * n_total) / (ms_per_step / 1e3) / 1e9
     dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
-    kernel_of = {"stats": "k_stats", "quantize": "k_quantize", "merge": "k_merge_q"}
+    kernel_of = {"stats": "k_stats", "quantize": "k_quantize",
+                 "merge": "k_merge_tma" if K <= 4 else "k_merge_q"}
     tr = traffic_record(kernel_of[dominant])
     traffic = None
     if tr is not None:

@@ -182,6 +182,10 @@ int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
  *               DL_ERR_QUORUM and leaves the state untouched
  *   delta_bar_out device [n] fp32, out (D); may be NULL
  * A zero total weight or a negative / non-finite weight gives DL_ERR_ARG.
+ * With up to 4 present learners (quantised mode) the data is staged through
+ * shared memory by bulk copies whose waits are bounded; a wait that runs out
+ * sets a bit in the library's own status word (this call has no workspace),
+ * read with dl_read_device_status(NULL, ...).
  */
 int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
                         const float* d_codebook, const float* const* theta_k, int32_t K,
@@ -367,8 +371,9 @@ int dl_quantize_noalloc(const float* theta_g, const float* const* theta_k, int32
  * a bulk copy give up after a bounded time instead of hanging; they then set
  * a bit here and the call's outputs are undefined. Blocks until the stream
  * has finished, then copies the word to the host and clears it.
- *   d_workspace  a workspace previously passed to dl_pseudograd_stats or
- *                dl_quantize
+ *   d_workspace  a workspace previously passed to a call that takes one, or
+ *                NULL for the library's own word on the current device (set
+ *                by dl_merge_outer_step, which takes no workspace)
  *   status_out   host, out
  */
 int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream);

@@ -305,6 +305,15 @@ int grid_for(const void* kernel, int threads, size_t smem, int64_t work_items);
 int blocks_per_learner(const void* kernel, int threads, size_t smem, int K, int64_t n_chunks);
 int cuda_status(cudaError_t e);
 int launch_status();
+// the library's device status word (for calls without a workspace)
+int library_status_word(uint32_t** out);
+// dl_merge_outer_step reporting bounded-wait failures to `status` (NULL: the
+// library's word)
+int merge_outer_step_status(float* theta_g, float* momentum, const uint8_t* const* codes,
+                            const float* d_codebook, const float* const* theta_k, int32_t K,
+                            const dl_fragment* frag, const float* weights, const uint8_t* present,
+                            int32_t min_quorum, float lr, float mu, float* delta_bar_out,
+                            uint32_t* status, void* stream);
 // dl_pseudograd_stats; share_sms: at most one of its blocks resident per SM
 // (same grid, same results)
 int pseudograd_stats_shared(const float* theta_g, const float* const* theta_k, int32_t K,

@@ -59,7 +59,13 @@ extern "C" int dl_plan_fragments(const int64_t* numel, int32_t n_tensors, int32_
 }
 
 extern "C" int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream) {
-    if (!d_workspace || !status_out) return DL_ERR_ARG;
+    if (!status_out) return DL_ERR_ARG;
+    if (!d_workspace) {  // the library's own word (calls without a workspace)
+        uint32_t* w = nullptr;
+        const int st = dl::library_status_word(&w);
+        if (st != DL_OK) return st;
+        d_workspace = w;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t v = 0;
     cudaError_t e = cudaMemcpyAsync(&v, d_workspace, sizeof(v), cudaMemcpyDeviceToHost, s);

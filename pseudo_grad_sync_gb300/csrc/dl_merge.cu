@@ -35,6 +35,8 @@
 //                 the values in fp32 in ascending k.
 #include <math.h>
 
+#include <mutex>
+
 #include "dl_common.cuh"
 
 namespace dl {
@@ -57,6 +59,7 @@ struct MergeArgs {
     float lr;
     float mu;
     const float* rda_c;  // RDA: [np][T] codebook scales (else unused)
+    uint32_t* status;    // staged merge: workspace status word (bounded waits)
 };
 
 __device__ __forceinline__ void outer_update(float acc, float& th, float& mm, float lr, float mu) {
@@ -158,6 +161,148 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
             }
         }
     }
+}
+
+// Staged variant of k_merge_q for up to NPM present learners: a producer warp
+// streams tiles of theta, m and every learner's codes into a STAGES-deep
+// shared-memory ring with bulk copies (every wait bounded, failures set the
+// status word), 8 consumer warps decode from shared memory and store theta
+// and m back with 128-bit stores. Per element the arithmetic is k_merge_q's,
+// in the same order, so the results are bitwise the same.
+constexpr int kMTile = 2048;  // elements per stage
+
+template <int NPM, int STAGES>
+__global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
+    extern __shared__ __align__(128) unsigned char mbuf[];
+    // stage s: theta [kMTile] f32 | m [kMTile] f32 | codes [NPM][kMTile] u8
+    constexpr int kStageBytes = kMTile * 8 + NPM * kMTile;
+    __shared__ float scb[NPM * kNB];
+    __shared__ PipeBarriers pb;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int np = a.np;
+    pipe_init<STAGES>(&pb);
+
+    if ((tid >> 5) == kConsumerWarps) {  // producer warp
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+                const int64_t base = c * kChunk;
+                const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+                for (int o = 0; o < cn; o += kMTile, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    if (it >= STAGES) wait_or_flag(&pb.empty[s], ((it / STAGES) - 1) & 1u, a.status);
+                    const int tn = min(kMTile, cn - o);
+                    const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;  // whole float4s
+                    const uint32_t cbytes = static_cast<uint32_t>(tn >> 4) * 16u;  // whole 16-byte runs
+                    unsigned char* st = mbuf + s * kStageBytes;
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(&pb.full[s], 2u * fbytes + static_cast<uint32_t>(np) * cbytes);
+                    const int64_t e0 = base + o;
+                    if (fbytes) {
+                        bulk_copy_g2s(st, a.g + e0, fbytes, &pb.full[s]);
+                        bulk_copy_g2s(st + kMTile * 4, a.m + e0, fbytes, &pb.full[s]);
+                    }
+                    if (cbytes)
+                        for (int k = 0; k < np; ++k)
+                            bulk_copy_g2s(st + kMTile * 8 + k * kMTile, a.cp[k] + e0, cbytes, &pb.full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    int cur_t = -1;
+    uint32_t it = 0;
+    for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+        const int64_t base = c * kChunk;
+        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+        int t0 = tensor_containing(a.off, a.T, base);
+        for (int o = 0; o < cn; o += kMTile, ++it) {
+            const int s = static_cast<int>(it % STAGES);
+            const int64_t tb = base + o;
+            const int tn = min(kMTile, cn - o);
+            const int fvec = tn & ~3, cvec = tn & ~15;  // elements staged
+            const int64_t tend = tb + tn;
+            wait_or_flag(&pb.full[s], (it / STAGES) & 1u, a.status);
+            const unsigned char* st = mbuf + s * kStageBytes;
+            const float* sg = reinterpret_cast<const float*>(st);
+            const float* sm = reinterpret_cast<const float*>(st + kMTile * 4);
+            const unsigned char* sc = st + kMTile * 8;
+            for (int t = t0; t < a.T; ++t) {
+                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+                if (o0 >= tend) break;
+                const int64_t pa = o0 > tb ? o0 : tb;
+                const int64_t pe = o1 < tend ? o1 : tend;
+                if (pe <= tb) t0 = t + 1;
+                if (pa >= pe) continue;
+                if (t != cur_t) {  // consumer-uniform
+                    consumer_sync();
+                    for (int i = tid; i < np * kNB; i += kThreads)
+                        scb[i] = __ldg(a.cb + (static_cast<int64_t>(a.kidx[i >> 8]) * a.T + t) * kNB +
+                                       (i & (kNB - 1)));
+                    consumer_sync();
+                    cur_t = t;
+                }
+                if (pa == tb && pe == tb + kMTile) {
+#pragma unroll
+                    for (int q = 0; q < kMTile / 4 / kThreads; ++q) {
+                        const int gi = tid + q * kThreads;  // float4 group in the tile
+                        float4 th = reinterpret_cast<const float4*>(sg)[gi];
+                        float4 mm = reinterpret_cast<const float4*>(sm)[gi];
+                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                        for (int k = 0; k < NPM; ++k) {
+                            if (k < np) {
+                                const uint32_t w4 = reinterpret_cast<const uint32_t*>(sc + k * kMTile)[gi];
+                                const float* cbs = scb + k * kNB;
+                                const float ws = a.w[k];
+                                a0 = __fmaf_rn(ws, cbs[w4 & 255u], a0);
+                                a1 = __fmaf_rn(ws, cbs[(w4 >> 8) & 255u], a1);
+                                a2 = __fmaf_rn(ws, cbs[(w4 >> 16) & 255u], a2);
+                                a3 = __fmaf_rn(ws, cbs[w4 >> 24], a3);
+                            }
+                        }
+                        outer_update(a0, th.x, mm.x, a.lr, a.mu);
+                        outer_update(a1, th.y, mm.y, a.lr, a.mu);
+                        outer_update(a2, th.z, mm.z, a.lr, a.mu);
+                        outer_update(a3, th.w, mm.w, a.lr, a.mu);
+                        reinterpret_cast<float4*>(a.g + tb)[gi] = th;
+                        reinterpret_cast<float4*>(a.m + tb)[gi] = mm;
+                        if (a.dbar) reinterpret_cast<float4*>(a.dbar + tb)[gi] = make_float4(a0, a1, a2, a3);
+                    }
+                } else {
+                    for (int64_t e = pa + tid; e < pe; e += kThreads) {
+                        const int l = static_cast<int>(e - tb);
+                        float th = l < fvec ? sg[l] : a.g[e];
+                        float mm = l < fvec ? sm[l] : a.m[e];
+                        float acc = 0.f;
+                        for (int k = 0; k < np; ++k) {
+                            const uint32_t code = l < cvec ? sc[k * kMTile + l] : a.cp[k][e];
+                            acc = __fmaf_rn(a.w[k], scb[k * kNB + code], acc);
+                        }
+                        outer_update(acc, th, mm, a.lr, a.mu);
+                        a.g[e] = th;
+                        a.m[e] = mm;
+                        if (a.dbar) a.dbar[e] = acc;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pb.empty[s]);
+        }
+    }
+}
+
+template <int NPM, int STAGES>
+int launch_tma(const MergeArgs& a, cudaStream_t s) {
+    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, STAGES>);
+    const size_t smem = static_cast<size_t>(STAGES) * (kMTile * 8 + NPM * kMTile);
+    int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(smem)));
+    if (st != DL_OK) return st;
+    const int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
+    k_merge_tma<NPM, STAGES><<<grid, kPipeThreads, smem, s>>>(a);
+    return launch_status();
 }
 
 __global__ void __launch_bounds__(kThreads) k_merge_u(MergeArgs a) {
@@ -459,11 +604,32 @@ RdaLayout rda_layout(const HostFrag& f, int K) {
 }  // namespace
 }  // namespace dl
 
-extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
-                                   const float* d_codebook, const float* const* theta_k, int32_t K,
-                                   const dl_fragment* frag, const float* weights,
-                                   const uint8_t* present, int32_t min_quorum, float lr, float mu,
-                                   float* delta_bar_out, void* stream) {
+// The library's own device status word: bounded waits of calls that take no
+// workspace (the staged merge of dl_merge_outer_step) report here, and
+// dl_read_device_status(NULL, ...) reads it. One per device.
+static __device__ uint32_t g_library_status;
+
+namespace dl {
+int library_status_word(uint32_t** out) {
+    static std::mutex mu;
+    static uint32_t* p[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DL_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!p[dev]) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_library_status) != cudaSuccess || !q) return DL_ERR_CUDA;
+        p[dev] = static_cast<uint32_t*>(q);
+    }
+    *out = p[dev];
+    return DL_OK;
+}
+
+int merge_outer_step_status(float* theta_g, float* momentum, const uint8_t* const* codes,
+                            const float* d_codebook, const float* const* theta_k, int32_t K,
+                            const dl_fragment* frag, const float* weights, const uint8_t* present,
+                            int32_t min_quorum, float lr, float mu, float* delta_bar_out,
+                            uint32_t* status, void* stream) {
     MergeArgs a;
     const int st = prepare_merge(a, theta_g, momentum, codes, d_codebook, theta_k, K, frag,
                                  weights, present, min_quorum, lr, mu, delta_bar_out);
@@ -475,7 +641,25 @@ extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_
         k_merge_u<<<grid, kThreads, 0, s>>>(a);
         return launch_status();
     }
+    if (a.np <= 4) {  // staged through shared memory, 3 stages (2 blocks/SM)
+        int st2 = DL_OK;
+        if (!status) st2 = library_status_word(&status);
+        if (st2 != DL_OK) return st2;
+        a.status = status;
+        return launch_tma<4, 3>(a, s);
+    }
     return launch_quantised<false>(a, s);
+}
+}  // namespace dl
+
+extern "C" int dl_merge_outer_step(float* theta_g, float* momentum, const uint8_t* const* codes,
+                                   const float* d_codebook, const float* const* theta_k, int32_t K,
+                                   const dl_fragment* frag, const float* weights,
+                                   const uint8_t* present, int32_t min_quorum, float lr, float mu,
+                                   float* delta_bar_out, void* stream) {
+    return merge_outer_step_status(theta_g, momentum, codes, d_codebook, theta_k, K, frag,
+                                   weights, present, min_quorum, lr, mu, delta_bar_out, nullptr,
+                                   stream);
 }
 
 extern "C" size_t dl_rda_workspace_bytes(const dl_fragment* frag, int32_t K) {

@@ -341,9 +341,10 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
                                          min_quorum, lr, mu, job.delta_bar_out,
                                          ws + L.off_rda_ws, L.rda_ws, main_s);
         else
-            st = dl_merge_outer_step(job.theta_g, job.momentum, codes, codebook, nullptr, p.np,
-                                     job.frag, job.weights ? p.w : nullptr, nullptr, min_quorum,
-                                     lr, mu, job.delta_bar_out, main_s);
+            st = merge_outer_step_status(job.theta_g, job.momentum, codes, codebook, nullptr,
+                                         p.np, job.frag, job.weights ? p.w : nullptr, nullptr,
+                                         min_quorum, lr, mu, job.delta_bar_out,
+                                         reinterpret_cast<uint32_t*>(ws), main_s);
     }
     if (!serial) {
         // join even after a failure, so that the caller's stream stays ordered

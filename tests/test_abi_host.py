@@ -40,6 +40,13 @@ def test_exports_every_declared_symbol(L):
     assert L.dl_version() == 200
 
 
+def test_read_device_status_arguments(L):
+    out = ctypes.c_uint32(0)
+    assert L.dl_read_device_status(FAKE, None, None) == -1  # no place for the word
+    # NULL workspace: the library's own word, which needs a device (none here)
+    assert L.dl_read_device_status(None, ctypes.byref(out), None) == -4
+
+
 def test_shutdown_without_resources_is_a_no_op(L):
     # nothing was created on this host (no GPU): no CUDA call is made
     assert L.dl_shutdown() == 0
