@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
 // in the same order, so the results are bitwise the same.
 constexpr int kMTile = 2048;  // elements per stage
 
-template <int NPM, int STAGES>
+template <int NPM, int STAGES, bool RDA>
 __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
     extern __shared__ __align__(128) unsigned char mbuf[];
     // stage s: theta [kMTile] f32 | m [kMTile] f32 | codes [NPM][kMTile] u8
@@ -237,9 +237,12 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                 if (pa >= pe) continue;
                 if (t != cur_t) {  // consumer-uniform
                     consumer_sync();
-                    for (int i = tid; i < np * kNB; i += kThreads)
-                        scb[i] = __ldg(a.cb + (static_cast<int64_t>(a.kidx[i >> 8]) * a.T + t) * kNB +
-                                       (i & (kNB - 1)));
+                    for (int i = tid; i < np * kNB; i += kThreads) {
+                        float v = __ldg(a.cb + (static_cast<int64_t>(a.kidx[i >> 8]) * a.T + t) * kNB +
+                                        (i & (kNB - 1)));
+                        if (RDA) v = __fmul_rn(__ldg(a.rda_c + (i >> 8) * a.T + t), v);
+                        scb[i] = v;
+                    }
                     consumer_sync();
                     cur_t = t;
                 }
@@ -256,10 +259,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                                 const uint32_t w4 = reinterpret_cast<const uint32_t*>(sc + k * kMTile)[gi];
                                 const float* cbs = scb + k * kNB;
                                 const float ws = a.w[k];
-                                a0 = __fmaf_rn(ws, cbs[w4 & 255u], a0);
-                                a1 = __fmaf_rn(ws, cbs[(w4 >> 8) & 255u], a1);
-                                a2 = __fmaf_rn(ws, cbs[(w4 >> 16) & 255u], a2);
-                                a3 = __fmaf_rn(ws, cbs[w4 >> 24], a3);
+                                if (RDA) {  // values already scaled
+                                    a0 = __fadd_rn(a0, cbs[w4 & 255u]);
+                                    a1 = __fadd_rn(a1, cbs[(w4 >> 8) & 255u]);
+                                    a2 = __fadd_rn(a2, cbs[(w4 >> 16) & 255u]);
+                                    a3 = __fadd_rn(a3, cbs[w4 >> 24]);
+                                } else {
+                                    a0 = __fmaf_rn(ws, cbs[w4 & 255u], a0);
+                                    a1 = __fmaf_rn(ws, cbs[(w4 >> 8) & 255u], a1);
+                                    a2 = __fmaf_rn(ws, cbs[(w4 >> 16) & 255u], a2);
+                                    a3 = __fmaf_rn(ws, cbs[w4 >> 24], a3);
+                                }
                             }
                         }
                         outer_update(a0, th.x, mm.x, a.lr, a.mu);
@@ -278,7 +288,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                         float acc = 0.f;
                         for (int k = 0; k < np; ++k) {
                             const uint32_t code = l < cvec ? sc[k * kMTile + l] : a.cp[k][e];
-                            acc = __fmaf_rn(a.w[k], scb[k * kNB + code], acc);
+                            const float v = scb[k * kNB + code];
+                            acc = RDA ? __fadd_rn(acc, v) : __fmaf_rn(a.w[k], v, acc);
                         }
                         outer_update(acc, th, mm, a.lr, a.mu);
                         a.g[e] = th;
@@ -293,15 +304,15 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
     }
 }
 
-template <int NPM, int STAGES>
+template <int NPM, int STAGES, bool RDA>
 int launch_tma(const MergeArgs& a, cudaStream_t s) {
-    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, STAGES>);
+    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, STAGES, RDA>);
     const size_t smem = static_cast<size_t>(STAGES) * (kMTile * 8 + NPM * kMTile);
     int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(smem)));
     if (st != DL_OK) return st;
     const int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
-    k_merge_tma<NPM, STAGES><<<grid, kPipeThreads, smem, s>>>(a);
+    k_merge_tma<NPM, STAGES, RDA><<<grid, kPipeThreads, smem, s>>>(a);
     return launch_status();
 }
 
@@ -646,7 +657,7 @@ int merge_outer_step_status(float* theta_g, float* momentum, const uint8_t* cons
         if (!status) st2 = library_status_word(&status);
         if (st2 != DL_OK) return st2;
         a.status = status;
-        return launch_tma<4, 3>(a, s);
+        return launch_tma<4, 3, false>(a, s);
     }
     return launch_quantised<false>(a, s);
 }
@@ -719,5 +730,9 @@ extern "C" int dl_rda_merge_outer_step(float* theta_g, float* momentum,
     k_rda_coef<<<f.T, kThreads, 0, s>>>(r);
     if ((st = launch_status()) != DL_OK) return st;
     a.rda_c = r.c;
+    if (a.np <= 4) {  // staged, as the mean merge
+        a.status = reinterpret_cast<uint32_t*>(ws);
+        return launch_tma<4, 3, true>(a, s);
+    }
     return launch_quantised<true>(a, s);
 }

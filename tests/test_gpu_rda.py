@@ -112,3 +112,19 @@ def test_rda_quorum_failure_leaves_state_untouched(dl):
     assert e.value.status == -3
     torch.cuda.synchronize()
     assert np.array_equal(gd.cpu().numpy(), g) and np.array_equal(md.cpu().numpy(), m)
+
+
+def test_staged_rda_merge_equals_the_unstaged_one(dl):
+    """Up to 4 present learners take the staged merge; a fifth present learner
+    of weight 0 (a copy of learner 0) forces the unstaged kernels without
+    changing r, u, ||u|| or any sum. D, theta and momentum must be the same."""
+    K = 4
+    g, m, off, codes, cb, cnt = _oracle_quantised(41, RAGGED, K)
+    w = np.array([0.7, 1.3, 1.0, 0.4], np.float32)
+    a = _gpu_rda(dl, g, m, RAGGED, codes, cb, cnt, weights=w)
+    codes5 = np.concatenate([codes, codes[:1]])
+    cb5 = np.concatenate([cb, cb[:1]])
+    cnt5 = np.concatenate([cnt, cnt[:1]])
+    b = _gpu_rda(dl, g, m, RAGGED, codes5, cb5, cnt5, weights=np.append(w, np.float32(0.0)))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)  # == on floats: +0 and -0 count as equal
