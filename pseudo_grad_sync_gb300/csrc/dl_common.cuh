@@ -107,8 +107,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // elements into a ring of STAGES shared-memory stages with bulk copies;
 // consumer warps wait on the stage's "full" mbarrier and release it through
 // its "empty" mbarrier (one arrival per consumer warp). Waits are bounded: a
-// wait that runs out records kDevErrCopyTimeout and goes on, so no warp ever
-// blocks a barrier the others wait at.
+// wait that runs out records kDevErrCopyTimeout, waits once more (bounded) and
+// goes on, so no warp ever blocks a barrier the others wait at.
 constexpr int kConsumerWarps = kWarps;
 constexpr int kPipeThreads = kThreads + 32;  // + one producer warp
 constexpr int kMaxStages = 4;
@@ -131,8 +131,13 @@ __device__ __forceinline__ void pipe_init(PipeBarriers* pb) {
     __syncthreads();
 }
 
+// A wait that runs out records the failure, then gives the copies in flight
+// one more bounded wait to land before the warp goes on.
 __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
-    if (!mbar_wait_bounded(bar, parity)) atomicOr(status, kDevErrCopyTimeout);
+    if (!mbar_wait_bounded(bar, parity)) {
+        atomicOr(status, kDevErrCopyTimeout);
+        (void)mbar_wait_bounded(bar, parity);
+    }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
