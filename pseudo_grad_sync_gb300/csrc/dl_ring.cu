@@ -49,6 +49,7 @@ struct RingArgs {
     float w;
     float lr;
     float mu;
+    uint32_t* status;       // workspace status word (staged last hop)
 };
 
 template <bool DECODE>
@@ -233,6 +234,136 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                       red_side, red_bad);
 }
 
+// The last hop staged through shared memory: a producer warp streams
+// 2048-element tiles of theta_g, the replica, m and the previous codes into a
+// 3-stage ring with bulk copies (bounded waits), 8 consumer warps apply the
+// hop and the outer step with k_ring_hop's arithmetic and store theta_g, m
+// (and D) with 128-bit stores. Blocks take contiguous chunk runs.
+constexpr int kRTile = 2048;
+constexpr int kRStages = 3;
+constexpr int kRStageBytes = kRTile * 13;  // theta_g, r, m (f32) + codes (u8)
+
+__global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
+    extern __shared__ __align__(128) unsigned char rbuf[];
+    __shared__ float scb[kNB];
+    __shared__ PipeBarriers pb;
+    const int tid = threadIdx.x, lane = tid & 31;
+    int64_t c0, c1;
+    block_chunks(a.n_chunks, c0, c1);
+    pipe_init<kRStages>(&pb);
+
+    if ((tid >> 5) == kConsumerWarps) {  // producer warp
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = c0; c < c1; ++c) {
+                const int64_t base = c * kChunk;
+                const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+                for (int o = 0; o < cn; o += kRTile, ++it) {
+                    const int s = static_cast<int>(it % kRStages);
+                    if (it >= kRStages) wait_or_flag(&pb.empty[s], ((it / kRStages) - 1) & 1u, a.status);
+                    const int tn = min(kRTile, cn - o);
+                    const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;
+                    const uint32_t cbytes = static_cast<uint32_t>(tn >> 4) * 16u;
+                    unsigned char* st = rbuf + s * kRStageBytes;
+                    const int64_t e0 = base + o;
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(&pb.full[s], 3u * fbytes + cbytes);
+                    if (fbytes) {
+                        bulk_copy_g2s(st, a.g + e0, fbytes, &pb.full[s]);
+                        bulk_copy_g2s(st + kRTile * 4, a.r + e0, fbytes, &pb.full[s]);
+                        bulk_copy_g2s(st + kRTile * 8, a.m + e0, fbytes, &pb.full[s]);
+                    }
+                    if (cbytes) bulk_copy_g2s(st + kRTile * 12, a.codes + e0, cbytes, &pb.full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    int cur_t = -1;
+    uint32_t it = 0;
+    for (int64_t c = c0; c < c1; ++c) {
+        const int64_t base = c * kChunk;
+        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+        int t0 = tensor_containing(a.off, a.T, base);
+        for (int o = 0; o < cn; o += kRTile, ++it) {
+            const int s = static_cast<int>(it % kRStages);
+            const int64_t tb = base + o;
+            const int tn = min(kRTile, cn - o);
+            const int fvec = tn & ~3, cvec = tn & ~15;
+            const int64_t tend = tb + tn;
+            wait_or_flag(&pb.full[s], (it / kRStages) & 1u, a.status);
+            const unsigned char* st = rbuf + s * kRStageBytes;
+            const float* sg = reinterpret_cast<const float*>(st);
+            const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
+            const float* sm = reinterpret_cast<const float*>(st + kRTile * 8);
+            const unsigned char* sc = st + kRTile * 12;
+            for (int t = t0; t < a.T; ++t) {
+                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+                if (o0 >= tend) break;
+                const int64_t pa = o0 > tb ? o0 : tb;
+                const int64_t pe = o1 < tend ? o1 : tend;
+                if (pe <= tb) t0 = t + 1;
+                if (pa >= pe) continue;
+                if (t != cur_t) {  // consumer-uniform
+                    consumer_sync();
+                    scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
+                    consumer_sync();
+                    cur_t = t;
+                }
+                if (pa == tb && pe == tb + kRTile) {
+#pragma unroll
+                    for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
+                        const int gi = tid + q * kThreads;
+                        float4 gv = reinterpret_cast<const float4*>(sg)[gi];
+                        const float4 rv = reinterpret_cast<const float4*>(sr)[gi];
+                        float4 mv = reinterpret_cast<const float4*>(sm)[gi];
+                        const uint32_t cw = reinterpret_cast<const uint32_t*>(sc)[gi];
+                        const float v0 = hop_value<true>(gv.x, rv.x, scb[cw & 255u], a.w);
+                        const float v1 = hop_value<true>(gv.y, rv.y, scb[(cw >> 8) & 255u], a.w);
+                        const float v2 = hop_value<true>(gv.z, rv.z, scb[(cw >> 16) & 255u], a.w);
+                        const float v3 = hop_value<true>(gv.w, rv.w, scb[cw >> 24], a.w);
+                        nesterov(v0, gv.x, mv.x, a.lr, a.mu);
+                        nesterov(v1, gv.y, mv.y, a.lr, a.mu);
+                        nesterov(v2, gv.z, mv.z, a.lr, a.mu);
+                        nesterov(v3, gv.w, mv.w, a.lr, a.mu);
+                        reinterpret_cast<float4*>(a.g + tb)[gi] = gv;
+                        reinterpret_cast<float4*>(a.m + tb)[gi] = mv;
+                        if (a.dbar)
+                            reinterpret_cast<float4*>(a.dbar + tb)[gi] = make_float4(v0, v1, v2, v3);
+                    }
+                } else {
+                    for (int64_t e = pa + tid; e < pe; e += kThreads) {
+                        const int l = static_cast<int>(e - tb);
+                        float gv = l < fvec ? sg[l] : a.g[e];
+                        const float rv = l < fvec ? sr[l] : a.r[e];
+                        float mm = l < fvec ? sm[l] : a.m[e];
+                        const uint32_t code = l < cvec ? sc[l] : a.codes[e];
+                        const float v = hop_value<true>(gv, rv, scb[code], a.w);
+                        nesterov(v, gv, mm, a.lr, a.mu);
+                        a.g[e] = gv;
+                        a.m[e] = mm;
+                        if (a.dbar) a.dbar[e] = v;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pb.empty[s]);
+        }
+    }
+}
+
+int launch_last_tma(const RingArgs& a, cudaStream_t s) {
+    const void* k = reinterpret_cast<const void*>(k_ring_last_tma);
+    const size_t smem = static_cast<size_t>(kRStages) * kRStageBytes;
+    int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(smem)));
+    if (st != DL_OK) return st;
+    const int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
+    k_ring_last_tma<<<grid, kPipeThreads, smem, s>>>(a);
+    return launch_status();
+}
+
 // One hop on s. With STATS, the partials of the new P are zeroed first, and
 // *grid_out is the hop's grid (the partials' J).
 template <bool DECODE, bool FINAL, bool STATS>
@@ -368,6 +499,7 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
     a.T = f.T;
     a.lr = lr;
     a.mu = mu;
+    a.status = reinterpret_cast<uint32_t*>(ws);
 
     // statistics of P_s (quantised at hop s + 1): the caller's row s, or the
     // workspace's
@@ -392,7 +524,7 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
         // receive: decode and add this learner's weighted pseudo-gradient
         a.r = theta_k[idx[s]];
         a.w = w_hat[s];
-        st = s == S - 1 ? launch_hop<true, true, false>(a, strm)
+        st = s == S - 1 ? launch_last_tma(a, strm)
                         : launch_hop<true, false, true>(a, strm, &J);
         if (st != DL_OK) return st;
     }
