@@ -14,6 +14,10 @@
 //                 in ascending order, and stores theta and m back with
 //                 128-bit stores. Each byte of codes, theta and m crosses HBM
 //                 once.
+// k_merge_tma<NPM, STAGES, RDA>  the same merge for up to 4 present learners
+//                 with theta, m and the codes staged through shared memory by
+//                 bulk copies (producer warp, bounded waits); used for the
+//                 mean merge and the RDA merge, bitwise equal to k_merge_q.
 // k_merge_u       the unquantised variant: values are the fp32 Delta_k read
 //                 from the learner replicas.
 //

@@ -18,7 +18,9 @@
 // statistics as it writes P, with the exact scheme of the statistics kernel
 // (float-float sums of y = P - c and of y^2 on a power-of-two offset, fp64
 // for values outside the fast range): the quantiser's statistics then cost
-// no extra pass over P. Each block entering a tensor computes its shift c
+// no extra pass over P. The last hop runs as k_ring_last_tma, its inputs
+// staged through shared memory by bulk copies. Each block entering a tensor
+// computes its shift c
 // (one warp, from the hop's own formula at the tensor's first 64 elements,
 // with the statistics kernel's rule; every block gets the same value), and
 // stats_finish turns the partials into mu, sigma, lo, hi.
