@@ -18,8 +18,10 @@
 // statistics as it writes P, with the exact scheme of the statistics kernel
 // (float-float sums of y = P - c and of y^2 on a power-of-two offset, fp64
 // for values outside the fast range): the quantiser's statistics then cost
-// no extra pass over P. The last hop runs as k_ring_last_tma, its inputs
-// staged through shared memory by bulk copies. Each block entering a tensor
+// no extra pass over P. Rings of two or more learners run their hops staged
+// through shared memory by bulk copies (k_ring_mid_tma for the hops that
+// write P, k_ring_last_tma for the last one); k_ring_hop, the same work with
+// plain loads, runs the one-learner ring. Each block entering a tensor
 // computes its shift c
 // (one warp, from the hop's own formula at the tensor's first 64 elements,
 // with the statistics kernel's rule; every block gets the same value), and
@@ -366,6 +368,170 @@ int launch_last_tma(const RingArgs& a, cudaStream_t s) {
     return launch_status();
 }
 
+// A hop before the last one, staged the same way: tiles of theta_g, the
+// replica and (DECODE) the previous codes in a 3-stage ring; the consumers
+// write P and accumulate its statistics as k_ring_hop does (the same scheme,
+// per (block, tensor) partials, the block's shift from the tensor's first 64
+// elements).
+constexpr int kRMidStageBytes = kRTile * 9;  // theta_g, r (f32) + codes (u8)
+
+template <bool DECODE>
+__global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
+    extern __shared__ __align__(128) unsigned char rbuf[];
+    __shared__ float scb[kNB];
+    __shared__ float s_shift;
+    __shared__ float red_ff[kWarps][4];
+    __shared__ double red_side[kWarps][2];
+    __shared__ int red_bad[kWarps];
+    __shared__ PipeBarriers pb;
+    const int tid = threadIdx.x, lane = tid & 31;
+    int64_t c0, c1;
+    block_chunks(a.n_chunks, c0, c1);
+    pipe_init<kRStages>(&pb);
+
+    if ((tid >> 5) == kConsumerWarps) {  // producer warp
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = c0; c < c1; ++c) {
+                const int64_t base = c * kChunk;
+                const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+                for (int o = 0; o < cn; o += kRTile, ++it) {
+                    const int s = static_cast<int>(it % kRStages);
+                    if (it >= kRStages) wait_or_flag(&pb.empty[s], ((it / kRStages) - 1) & 1u, a.status);
+                    const int tn = min(kRTile, cn - o);
+                    const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;
+                    const uint32_t cbytes = DECODE ? static_cast<uint32_t>(tn >> 4) * 16u : 0u;
+                    unsigned char* st = rbuf + s * kRMidStageBytes;
+                    const int64_t e0 = base + o;
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(&pb.full[s], 2u * fbytes + cbytes);
+                    if (fbytes) {
+                        bulk_copy_g2s(st, a.g + e0, fbytes, &pb.full[s]);
+                        bulk_copy_g2s(st + kRTile * 4, a.r + e0, fbytes, &pb.full[s]);
+                    }
+                    if (cbytes) bulk_copy_g2s(st + kRTile * 8, a.codes + e0, cbytes, &pb.full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    int cur_t = -1;
+    float csh = 0.f;
+    bool small = false;
+    Acc acc;
+    acc.reset();
+    uint32_t it = 0;
+    for (int64_t c = c0; c < c1; ++c) {
+        const int64_t base = c * kChunk;
+        const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
+        int t0 = tensor_containing(a.off, a.T, base);
+        for (int o = 0; o < cn; o += kRTile, ++it) {
+            const int s = static_cast<int>(it % kRStages);
+            const int64_t tb = base + o;
+            const int tn = min(kRTile, cn - o);
+            const int fvec = tn & ~3, cvec = tn & ~15;
+            const int64_t tend = tb + tn;
+            wait_or_flag(&pb.full[s], (it / kRStages) & 1u, a.status);
+            const unsigned char* st = rbuf + s * kRMidStageBytes;
+            const float* sg = reinterpret_cast<const float*>(st);
+            const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
+            const unsigned char* sc = st + kRTile * 8;
+            for (int t = t0; t < a.T; ++t) {
+                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+                if (o0 >= tend) break;
+                const int64_t pa = o0 > tb ? o0 : tb;
+                const int64_t pe = o1 < tend ? o1 : tend;
+                if (pe <= tb) t0 = t + 1;
+                if (pa >= pe) continue;
+                if (t != cur_t) {  // consumer-uniform
+                    if (cur_t >= 0)
+                        flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x + blockIdx.x,
+                                      red_ff, red_side, red_bad);
+                    consumer_sync();  // every read of the previous tensor's scb / s_shift is done
+                    if (DECODE) scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
+                    if (tid < 32) {
+                        const float cs = ring_shift<DECODE>(a, t, o0, o1 - o0);
+                        if (tid == 0) {
+                            s_shift = cs;
+                            if (pa == o0) a.shift[t] = cs;  // the one block holding element o0
+                        }
+                    }
+                    consumer_sync();
+                    acc.reset();
+                    csh = s_shift;
+                    small = (o1 - o0) < kSmallTensor;
+                    cur_t = t;
+                }
+                if (pa == tb && pe == tb + kRTile) {
+#pragma unroll
+                    for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
+                        const int gi = tid + q * kThreads;
+                        const float4 gv = reinterpret_cast<const float4*>(sg)[gi];
+                        const float4 rv = reinterpret_cast<const float4*>(sr)[gi];
+                        float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+                        if (DECODE) {
+                            const uint32_t cw = reinterpret_cast<const uint32_t*>(sc)[gi];
+                            e0 = scb[cw & 255u];
+                            e1 = scb[(cw >> 8) & 255u];
+                            e2 = scb[(cw >> 16) & 255u];
+                            e3 = scb[cw >> 24];
+                        }
+                        const float v0 = hop_value<DECODE>(gv.x, rv.x, e0, a.w);
+                        const float v1 = hop_value<DECODE>(gv.y, rv.y, e1, a.w);
+                        const float v2 = hop_value<DECODE>(gv.z, rv.z, e2, a.w);
+                        const float v3 = hop_value<DECODE>(gv.w, rv.w, e3, a.w);
+                        reinterpret_cast<float4*>(a.P + tb)[gi] = make_float4(v0, v1, v2, v3);
+                        acc_group(acc, v0, v1, v2, v3, csh, small);
+                    }
+                    renorm(acc.s2h, acc.s2l);
+                } else {
+                    for (int64_t e = pa + tid; e < pe; e += kThreads) {
+                        const int l = static_cast<int>(e - tb);
+                        const float gv = l < fvec ? sg[l] : a.g[e];
+                        const float rv = l < fvec ? sr[l] : a.r[e];
+                        const float dec = DECODE ? scb[l < cvec ? sc[l] : a.codes[e]] : 0.f;
+                        const float v = hop_value<DECODE>(gv, rv, dec, a.w);
+                        a.P[e] = v;
+                        const float y = __fsub_rn(v, csh);
+                        const float ay = fabsf(y);
+                        if (!small && fast_range(ay)) {
+                            if (ay > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                            ff_add(acc.s1h, acc.s1l, y);
+                            sq_add(acc.s2h, acc.s2l, y);
+                        } else {
+                            acc.side = true;
+                            side_add(v, csh, acc.s1d, acc.s2d, acc.bad);
+                        }
+                    }
+                    renorm(acc.s2h, acc.s2l);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pb.empty[s]);
+        }
+    }
+    if (cur_t >= 0)
+        flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x + blockIdx.x, red_ff,
+                      red_side, red_bad);
+}
+
+template <bool DECODE>
+int launch_mid_tma(const RingArgs& a, cudaStream_t s, int* grid_out) {
+    const void* k = reinterpret_cast<const void*>(k_ring_mid_tma<DECODE>);
+    const size_t smem = static_cast<size_t>(kRStages) * kRMidStageBytes;
+    int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(smem)));
+    if (st != DL_OK) return st;
+    int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
+    if (grid > kMaxBlocksTotal) grid = kMaxBlocksTotal;  // partial slots per tensor
+    const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(a.T) * grid;
+    if ((st = cuda_status(cudaMemsetAsync(a.part, 0, part_bytes, s))) != DL_OK) return st;
+    k_ring_mid_tma<DECODE><<<grid, kPipeThreads, smem, s>>>(a);
+    *grid_out = grid;
+    return launch_status();
+}
+
 // One hop on s. With STATS, the partials of the new P are zeroed first, and
 // *grid_out is the hop's grid (the partials' J).
 template <bool DECODE, bool FINAL, bool STATS>
@@ -513,7 +679,7 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
     a.w = w_hat[0];
     int J = 0;
     if (S == 1) return launch_hop<false, true, false>(a, strm);
-    if ((st = launch_hop<false, false, true>(a, strm, &J)) != DL_OK) return st;
+    if ((st = launch_mid_tma<false>(a, strm, &J)) != DL_OK) return st;
     for (int s = 1; s < S; ++s) {
         // send: finish P_{s-1}'s statistics and quantise it (values mode)
         dl_stats* sp = stats_of(s - 1);
@@ -527,7 +693,7 @@ extern "C" int dl_ring_outer_step(float* theta_g, float* momentum, const float* 
         a.r = theta_k[idx[s]];
         a.w = w_hat[s];
         st = s == S - 1 ? launch_last_tma(a, strm)
-                        : launch_hop<true, false, true>(a, strm, &J);
+                        : launch_mid_tma<true>(a, strm, &J);
         if (st != DL_OK) return st;
     }
     return DL_OK;
