@@ -1,21 +1,28 @@
 """Benchmark of the DiLoCo outer synchronisation step on GB300.
 
-Workload (default): the 1.1B decoder-shaped fp32 tensor set (201 tensors,
-22 layers, d=2048, FFN 5632, 32 q / 4 kv heads, vocab 32000), K=4 learner
-replicas resident in HBM, split by the LPT planner into P=24 fragments. One
-step = one outer synchronisation of the whole model: every fragment goes
-through stats -> quantise -> merge + Nesterov (the planner call is included),
-in one dl_outer_sync call that runs fragment f+1's stats beside fragment f's
-quantise and merge. A second timed pass makes the same step as separate
-C-ABI calls on one stream, with CUDA events around each call: the per-call
-GB/s and the roofline of the dominant call come from it.
-Inputs are synthetic (seeded generator), each fragment call streams >= 0.9 GB,
-far more than the 129 MB L2, so no L2 flush is needed between calls.
+Workload (default, ``decoder_10b``): the 10B decoder-shaped fp32 tensor set
+(381 tensors, 42 layers, d=4096, FFN 14336, 32 q / 8 kv heads, vocab 128256)
+cut by the LPT planner into P=24 fragments; the median fragment (18 tensors,
+415,260,672 elements) is resident in HBM with its K=14 learner replicas. One
+step = one outer synchronisation of that fragment through dl_outer_sync:
+stats -> quantise -> merge + Nesterov, theta_g and momentum carried from step
+to step. A second timed pass makes the same steps as separate C-ABI calls with
+CUDA events around each call: the per-call GB/s and the roofline of the
+dominant call come from it. ``quorum_10b`` is the same fragment with K=16 and
+a random present subset and token weights per step; ``ragged_heavy`` is the
+2000-tensor heavy-tail batch (K=8) synced as one fragment.
+
+``decoder_1b`` keeps the whole 1.1B model (K=4, all 24 fragments) resident and
+syncs every fragment per step, consecutive fragments overlapped on two
+streams; ``learner_1b`` / ``learner_10b`` time the learner-side quantiser.
+Inputs are synthetic (seeded generator); every call streams far more than the
+129 MB L2, so no L2 flush is needed between calls.
 
 Metric: outer-step params/s (whole job) and achieved HBM GB/s of each call,
 against the measured copy bandwidth in MEASURED_PEAKS.json.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
 
 N > 1 runs under torchrun as N independent replicas of the workload (one per
 GPU; the path has no data exchange), timed with a barrier and the max over
@@ -512,6 +519,392 @@ def run_rda(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# one fragment resident: the 10B decoder's median fragment (K=14, or K=16 with
+# a random quorum) and the ragged heavy-tail batch, one dl_outer_sync call per
+# step
+
+
+FRAGMENT_WORKLOADS = ("decoder_10b", "quorum_10b", "ragged_heavy")
+
+
+def bench_fragment(wl, plan):
+    """Tensors of the fragment a step syncs: for a model cut into P fragments
+    the median one by load (ties broken by fragment index), for a one-batch
+    workload every tensor. Returns (tensors, fragment index)."""
+    if wl.n_frags == 1:
+        return list(range(wl.n_tensors)), 0
+    frag_of, load = plan(wl.numels, wl.n_frags)
+    f = int(np.argsort(load, kind="stable")[len(load) // 2])
+    return [t for t in range(wl.n_tensors) if frag_of[t] == f], f
+
+
+def quorum_schedule(wl, step):
+    """Present mask and weights of bench step `step`: with a random quorum the
+    steps walk through every (fragment, outer step) draw of the workload in
+    turn (fragment = step mod P, outer step = step div P mod steps), so the
+    mix of quorum sizes is the workload's; otherwise all present, weight 1."""
+    f, s = step % wl.n_frags, (step // wl.n_frags) % wl.steps
+    return wl.present(f, s), wl.weights(f, s)
+
+
+def fragment_host(wl, ts, pin):
+    """theta_g [n] and the K replicas [K, n] of one fragment as (pinned) host
+    tensors from the seeded generator."""
+    import torch
+
+    n = sum(wl.numels[t] for t in ts)
+    g = torch.empty(n, dtype=torch.float32, pin_memory=pin)
+    # rows padded to 64 elements: every replica starts 256-byte aligned
+    reps = torch.empty((wl.K, -(-n // 64) * 64), dtype=torch.float32, pin_memory=pin)[:, :n]
+    gn, rn = g.numpy(), reps.numpy()
+    o = 0
+    for t in ts:
+        m = wl.numels[t]
+        wl.theta_global(t, out=gn[o:o + m])
+        for k in range(wl.K):
+            wl.replica(k, t, gn[o:o + m], out=rn[k, o:o + m])
+        o += m
+    return g, reps
+
+
+def fragment_device_fill(wl, ts, dev, seed=0):
+    """theta_g and the K replicas filled on the device with the workload's
+    distributions (theta_g ~ N(0, theta_std), Delta = scale * N(0, 1) or
+    scale * Student-t(3)), for batches too large to generate on the host."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    n = sum(wl.numels[t] for t in ts)
+    g = torch.empty(n, dtype=torch.float32, device=dev).normal_(0.0, wl.theta_std, generator=gen)
+    # rows padded to 64 elements: every replica starts 256-byte aligned
+    reps = torch.empty((wl.K, -(-n // 64) * 64), dtype=torch.float32, device=dev)[:, :n]
+    chunk = 1 << 26
+    for k in range(wl.K):
+        o = 0
+        for t in ts:
+            m = wl.numels[t]
+            for a in range(0, m, chunk):
+                b = min(m, a + chunk)
+                x = torch.randn(b - a, device=dev, generator=gen)
+                if wl.delta_dist == 1:  # Student-t(3) = Z / sqrt(chi2_3 / 3)
+                    c = torch.randn(3, b - a, device=dev, generator=gen).square_().sum(0)
+                    x.div_(c.div_(3.0).sqrt_())
+                torch.sub(g[o + a:o + b], x.mul_(wl.tensor_scale(t)), out=reps[k, o + a:o + b])
+            o += m
+    return g, reps
+
+
+def oracle_fragment_pass(g, reps, off, present, weights):
+    """One outer step of the oracle over one fragment with the present
+    learners (what the GPU step computes); returns the seconds it took."""
+    import oracle
+
+    idx = [k for k in range(len(reps)) if present[k]]
+    t0 = time.perf_counter()
+    o = oracle.outer_step(g, np.zeros_like(g), [reps[k] for k in idx], offsets=off,
+                          weights=np.asarray(weights, np.float32)[idx])
+    dt = time.perf_counter() - t0
+    assert o["status"] == 0
+    return dt
+
+
+def fragment_cpu_sample(wl, ts, host, limit):
+    """Host arrays (theta_g, replicas, offsets, elements) of the oracle's
+    bounded sample: the fragment's tensors in order up to `limit` elements
+    (at least one tensor), sliced from the host copy or generated."""
+    sel, tot = [], 0
+    for t in ts:
+        if sel and tot + wl.numels[t] > limit:
+            continue
+        sel.append(t)
+        tot += wl.numels[t]
+    off = synthetic.offsets_of([wl.numels[t] for t in sel])
+    if host is not None and sel == ts[:len(sel)]:
+        g = host[0].numpy()[:tot]
+        reps = [host[1].numpy()[k, :tot] for k in range(wl.K)]
+    else:
+        g = np.empty(tot, dtype=np.float32)
+        reps = [np.empty(tot, dtype=np.float32) for _ in range(wl.K)]
+        for i, t in enumerate(sel):
+            a, b = int(off[i]), int(off[i + 1])
+            wl.theta_global(t, out=g[a:b])
+            for k in range(wl.K):
+                wl.replica(k, t, g[a:b], out=reps[k][a:b])
+    return g, reps, off, tot, sel
+
+
+def fragment_cpu_baseline(wl, ts, host, budget_s):
+    """The oracle on the host cores over (a bounded sample of) the bench
+    fragment, with step 0's quorum; the single-thread figure on its first
+    tensor beside it."""
+    import oracle
+
+    oracle.lib()
+    present, weights = quorum_schedule(wl, 0)
+    g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, host, 1 << 26)
+    total, passes = 0.0, 0
+    while passes == 0 or total < budget_s:
+        total += oracle_fragment_pass(g, reps, off, present, weights)
+        passes += 1
+    cores = oracle.threads()
+    # one thread on one tensor of the sample: the smallest with >= 2^20 elements
+    big = [i for i, t in enumerate(sel) if wl.numels[t] >= 1 << 20]
+    i1 = min(big, key=lambda i: wl.numels[sel[i]]) if big else 0
+    a1, n1 = int(off[i1]), wl.numels[sel[i1]]
+    oracle.set_threads(1)
+    try:
+        t1 = oracle_fragment_pass(g[a1:a1 + n1], [r[a1:a1 + n1] for r in reps],
+                                  np.array([0, n1], np.int64), present, weights)
+    finally:
+        oracle.set_threads(cores)
+    np_ = int(np.count_nonzero(present))
+    whole = "the whole fragment" if len(sel) == len(ts) else f"{len(sel)} of its {len(ts)} tensors"
+    return {"value": tot * passes / total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{whole} ({tot} elements x {np_} present learners), full outer step "
+                      f"(stats+quantise+merge+Nesterov), {passes} pass(es) in {total:.1f} s",
+            "single_thread": {"value": n1 / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"one tensor of it ({n1} elements x {np_} learners), "
+                                        f"one pass in {t1:.1f} s"}}
+
+
+def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
+    """The same step through the public API with host buffers: every step
+    uploads the present learners' replicas of the fragment from pinned host
+    memory (one copy per learner) on an upload stream into one of two device
+    buffers, runs dl_outer_sync as soon as they have landed, and downloads the
+    updated theta_g on a download stream. Uploads of step s+1 run while step s
+    computes and downloads; the step after waits for the download before it
+    updates theta_g again."""
+    import torch
+
+    K, n = wl.K, F.n
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    bufs = [reps_d, torch.empty(K, reps_d.stride(0), dtype=torch.float32, device=dev)[:, :n]]
+    g_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_reps = host[1]
+
+    def run(steps):
+        ready = [torch.cuda.Event() for _ in range(steps)]
+        done = [torch.cuda.Event() for _ in range(steps)]
+        fetched = [torch.cuda.Event() for _ in range(steps)]
+        bi = 0
+        for s in range(steps):
+            present, weights = quorum_schedule(wl, s)
+            buf = bufs[s % 2]
+            with torch.cuda.stream(up):
+                if s >= 2:
+                    up.wait_event(done[s - 2])
+                for k in range(K):
+                    if present[k]:
+                        buf[k].copy_(h_reps[k], non_blocking=True)
+                        bi += n * 4
+                ready[s].record(up)
+            comp.wait_event(ready[s])
+            if s >= 1:
+                comp.wait_event(fetched[s - 1])
+            sync.step([g], [m], [[buf[k] for k in range(K)]], weights=[weights],
+                      present=[present], stream=comp)
+            done[s].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done[s])
+                g_out.copy_(g, non_blocking=True)
+                fetched[s].record(down)
+        comp.wait_stream(up)
+        comp.wait_stream(down)
+        return bi
+
+    steps = max(3, min(args.steps, 6))
+    run(2)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    bi = run(steps)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        dt = max_over_ranks(dt, world, dev)
+    # the host link alone: one large pinned copy of one replica, CUDA events
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    for _ in range(3):
+        bufs[1][0].copy_(h_reps[0], non_blocking=True)
+    b.record(comp)
+    torch.cuda.synchronize()
+    plain = 3 * n * 4 / (a.elapsed_time(b) / 1e3) / 1e9
+    return {"value": world * n * steps / dt, "unit": UNIT, "h2d_bytes_per_step": bi // steps,
+            "d2h_bytes_per_step": n * 4, "steps": steps, "ms_per_step": dt / steps * 1e3,
+            "h2d_gbs": bi / dt / 1e9, "h2d_plain_copy_gbs": plain,
+            "note": "present replicas H2D from pinned memory on an upload stream (two device "
+                    "buffers, step s+1 uploads while step s computes), dl_outer_sync per step, "
+                    "updated theta_g D2H on a download stream; momentum and theta_g stay on "
+                    "the device; h2d_plain_copy_gbs: one pinned replica copied alone"}
+
+
+def run_fragment(args, rank, world, local):
+    """One fragment resident in HBM with its K replicas; a step is one outer
+    synchronisation of that fragment through dl_outer_sync (stats -> quantise
+    -> merge + Nesterov), momentum and theta_g carried from step to step. A
+    second timed pass makes the same steps as separate C-ABI calls with CUDA
+    events around each call."""
+    import torch
+
+    import pseudo_grad_sync_gb300 as dl
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    wl = synthetic.WORKLOADS[args.workload]()
+    K = wl.K
+    ts, fid = bench_fragment(wl, dl.plan_fragments)
+    numels = [wl.numels[t] for t in ts]
+    F = dl.Fragment(numels, dev)
+    n = F.n
+    device_filled = wl.name == "ragged_heavy"  # 2.4G elements x 9 arrays: filled on the device
+    t0 = time.time()
+    host = None
+    if device_filled:
+        g, reps = fragment_device_fill(wl, ts, dev, seed=rank)
+    else:
+        host = fragment_host(wl, ts, pin=not args.no_e2e)
+        g = host[0].to(dev)
+        reps = torch.empty(host[1].shape[0], host[1].stride(0), dtype=torch.float32,
+                           device=dev)[:, :n]
+        reps.copy_(host[1])
+    gen_s = time.time() - t0
+    m = torch.zeros_like(g)
+    rep_list = [reps[k] for k in range(K)]
+    sync = dl.ModelSync([F], K, dev)
+    stats = dl.new_stats(K, F.T, dev)
+    ws_s = dl.new_workspace(dl.stats_workspace_bytes(F, K), dev)
+    ws_q = dl.new_workspace(dl.quantize_workspace_bytes(F, K), dev)
+    codebook = torch.empty((K, F.T, 256), dtype=torch.float32, device=dev)
+    codes = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(K)]
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def sync_step(s):
+        present, weights = quorum_schedule(wl, s)
+        sync.step([g], [m], [rep_list], weights=[weights], present=[present], stream=stream)
+
+    def call_step(s, ev=None):
+        present, weights = quorum_schedule(wl, s)
+        idx = [k for k in range(K) if present[k]]
+        kp = len(idx)
+        rp = [rep_list[k] for k in idx]
+        w = np.asarray(weights, dtype=np.float32)[idx]
+        if ev is not None:
+            ev[0].record(stream)
+        dl.pseudograd_stats(g, rp, F, 6.0, stats[:kp], ws_s, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        dl.quantize(g, rp, F, stats[:kp], codes[:kp], codebook[:kp], None, ws_q, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        dl.merge_outer_step(g, m, F, codes[:kp], codebook[:kp], weights=w, lr=0.7, mu=0.9,
+                            stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        return kp
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for s in range(args.warmup):
+        sync_step(s)
+        call_step(s)
+    barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+
+    def timed(body):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        start.record(stream)
+        for s in range(args.steps):
+            body(s)
+        end.record(stream)
+        barrier()
+        return max_over_ranks(start.elapsed_time(end), world, dev) / args.steps
+
+    ms_per_step = timed(sync_step)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    kps = []
+    ms_calls = timed(lambda s: kps.append(call_step(s, ev[s])))
+    clk = clocks.stop()
+
+    peak, peak_kind = load_peaks()
+    calls = {}
+    for i, name in enumerate(("stats", "quantize", "merge")):
+        tot_ms = sum(e[i].elapsed_time(e[i + 1]) for e in ev)
+        tot_bytes = sum(algo_bytes(kp)[name] * n for kp in kps)
+        gbs = tot_bytes / (tot_ms / 1e3) / 1e9
+        calls[name] = {"ms_per_step": tot_ms / args.steps, "achieved_gbs": gbs,
+                       "frac": gbs / peak,
+                       "algo_bytes_per_elem": sum(algo_bytes(kp)[name] for kp in kps) / len(kps)}
+    step_bytes = sum((10 * kp + 24) * n for kp in kps) / len(kps)
+    full_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+    dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
+    mean_np = sum(kps) / len(kps)
+    kernel_of = {"stats": "k_stats", "quantize": "k_quantize",
+                 "merge": "k_merge_tma" if max(kps) <= 4 else "k_merge_q"}
+    tr = traffic_record(kernel_of[dominant])
+    traffic = None if tr is None else tr["dram_bytes_per_elem"] * n
+    roofline = {"bound": "hbm", "achieved": round(calls[dominant]["achieved_gbs"], 1),
+                "peak": peak, "unit": "GB/s", "frac": round(calls[dominant]["frac"], 4),
+                "traffic": traffic, "kernel": kernel_of[dominant],
+                "note": (f"call '{dominant}' timed with CUDA events around its C-ABI call in "
+                         "the per-call pass; algorithmic bytes per launch = "
+                         f"{calls[dominant]['algo_bytes_per_elem']:.2f} B/elem x {n} elements; "
+                         f"peak = {peak_kind} copy bandwidth from MEASURED_PEAKS.json; traffic "
+                         "= ncu DRAM bytes per launch (null unless captured for this source)")}
+    e2e = None
+    if host is not None and not args.no_e2e:
+        e2e = fragment_e2e(wl, F, g, m, reps, host, sync, args, world, dev)
+    desc = {"decoder_10b": "10B decoder set cut into P=24 by the LPT planner; the median "
+                           f"fragment (#{fid}, {len(ts)} tensors) synced per step with K={K} "
+                           "replicas resident, momentum carried across steps",
+            "quorum_10b": "10B shapes, the median fragment "
+                          f"(#{fid}, {len(ts)} tensors), K={K} learners with a random present "
+                          "subset of 1..16 and weights U[0.5,1.5] per step (the workload's "
+                          "(fragment, outer step) draws in turn), momentum carried",
+            "ragged_heavy": f"{len(ts)} ragged tensors 64..16Mi as one batch, K={K}, "
+                            "Delta = 1e-3 Student-t(3), device-filled"}[wl.name]
+    out = {
+        "metric": METRIC, "value": world * n / (ms_per_step / 1e3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (device-filled)" if device_filled else "synthetic",
+        "config": {"workload": wl.name + ": " + desc, "K": K, "fragment_elems": n,
+                   "fragment_tensors": len(ts), "mean_present_learners": mean_np,
+                   "l2": "no flush: every call streams >= 12 GB, inputs far larger than L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "full_step_gbs": full_gbs, "full_step_frac": full_gbs / peak,
+        "full_step_algo_bytes_per_elem": step_bytes / n,
+        "ms_per_step_serial_calls": ms_calls, "calls": calls, "roofline": roofline,
+        "clocks": clk, "gpu_launches": args.steps * sum(LAUNCHES_PER_FRAGMENT.values()),
+        "gpu_launches_note": "kernels in the headline dl_outer_sync region; the per-call pass "
+                             "launches the same number again",
+        "e2e": e2e, "setup_generate_s": gen_s,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = fragment_cpu_baseline(wl, ts, host, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -763,33 +1156,48 @@ def cpu_baseline(wl, frags, host, budget_s=10.0):
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is one whole-model outer step
-    of the workload on the host cores."""
+    """The oracle as the reference arm: each step is one outer step of the
+    workload on the host cores (for a fragment workload, of a bounded sample
+    of the bench fragment: its tensors in order up to 2^25 elements)."""
     import oracle
 
     if rank != 0:
         return
     wl = synthetic.WORKLOADS[args.workload]()
-    frag_of, _ = oracle.plan_fragments(wl.numels, wl.n_frags)
-    frags = fragment_tensors(wl, frag_of)
-    host = generate_host(wl, frags, pin=False)
-    offsets = fragment_offsets(wl, frags)
     oracle.lib()
-    for _ in range(args.warmup):
-        oracle_pass(wl, host, offsets)
-    dt = sum(oracle_pass(wl, host, offsets) for _ in range(args.steps))
-    value = wl.n_elems * args.steps / dt
+    if wl.name in FRAGMENT_WORKLOADS:
+        ts, fid = bench_fragment(wl, oracle.plan_fragments)
+        g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, None, 1 << 25)
+        for s in range(args.warmup):
+            oracle_fragment_pass(g, reps, off, *quorum_schedule(wl, s))
+        dt = sum(oracle_fragment_pass(g, reps, off, *quorum_schedule(wl, s))
+                 for s in range(args.steps))
+        n_step = tot
+        sample = (f"each step: {len(sel)} of the {len(ts)} tensors of the bench fragment "
+                  f"({tot} elements), full outer step with that step's present learners")
+        config = {"workload": wl.name, "K": wl.K, "fragment_elems": sum(wl.numels[t] for t in ts),
+                  "fragment_tensors": len(ts)}
+    else:
+        frag_of, _ = oracle.plan_fragments(wl.numels, wl.n_frags)
+        frags = fragment_tensors(wl, frag_of)
+        host = generate_host(wl, frags, pin=False)
+        offsets = fragment_offsets(wl, frags)
+        for _ in range(args.warmup):
+            oracle_pass(wl, host, offsets)
+        dt = sum(oracle_pass(wl, host, offsets) for _ in range(args.steps))
+        n_step = wl.n_elems
+        sample = (f"each step: the whole workload ({wl.n_elems} elements x K={wl.K}), full "
+                  "outer step on the host")
+        config = {"workload": wl.name + ": " + wl.description, "K": wl.K,
+                  "fragments": wl.n_frags, "params": wl.n_elems}
+    value = n_step * args.steps / dt
     metric = LEARNER_METRIC if wl.role == "learner" else METRIC
     out = {"impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-           "data": "synthetic",
-           "config": {"workload": wl.name + ": " + wl.description, "K": wl.K,
-                      "fragments": wl.n_frags, "params": wl.n_elems},
+           "data": "synthetic", "config": config,
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
-                            "kind": "oracle",
-                            "sample": f"each step: the whole workload ({wl.n_elems} elements "
-                                      f"x K={wl.K}), full outer step on the host"},
+                            "kind": "oracle", "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -801,7 +1209,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(synthetic.WORKLOADS), default="decoder_1b")
+    ap.add_argument("--workload", choices=sorted(synthetic.WORKLOADS), default="decoder_10b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -822,21 +1230,27 @@ def main():
             dist.init_process_group("gloo")
     wl = synthetic.WORKLOADS[args.workload]()
     learner = wl.role == "learner"
-    # resident footprint: the whole model with every replica in HBM (and, for
-    # the syncer, a host copy of the inputs); refuse before allocating
+    fragment = wl.name in FRAGMENT_WORKLOADS
+    # whole-model workloads keep every fragment and replica resident (and, for
+    # the syncer, a host copy of the inputs): refuse before allocating those
+    # that do not fit; fragment workloads hold one fragment at a time
     dev_gb = (2 * 4 + 1 if learner else (wl.K + 2) * 4 + wl.K) * wl.n_elems / 1e9
     host_gb = 0.0 if learner else (wl.K + 2) * 4 * wl.n_elems / 1e9
-    if dev_gb > 200 or host_gb > 64:
+    if not fragment and (dev_gb > 200 or host_gb > 64):
         if rank == 0:
             print(json.dumps({"error": f"workload {wl.name} needs ~{dev_gb:.0f} GB on the device "
                                        f"and ~{host_gb:.0f} GB on the host as one resident "
-                                       "model; the benchmark runs whole models that fit "
-                                       "(its fragments are covered by the parity tests)"}))
+                                       "model"}))
+        sys.exit(2)
+    if fragment and args.mode != "outer" and rank == 0:
+        print(json.dumps({"error": "--mode ring/rda run whole-model workloads"}))
         sys.exit(2)
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif learner:
         run_learner(args, rank, world, local)
+    elif fragment:
+        run_fragment(args, rank, world, local)
     elif args.mode == "ring":
         run_ring(args, rank, world, local)
     elif args.mode == "rda":

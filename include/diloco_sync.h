@@ -348,9 +348,11 @@ int dl_ring_outer_step(float* theta_g, float* momentum, const float* const* thet
  * array of DL_QUANTIZE_NOALLOC_MAX_BYTES inside the library; every GPU that
  * loads the library holds it until the process exits. Inputs and outputs
  * are the caller's, exactly as for dl_quantize; results are identical.
- *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress; nothing is cached, so the address stays right
+ *    after a device reset or a new primary context). The first lookup on a
+ *    device may load the library's device code there: make the first call
+ *    on each device before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents
  *    (the call clears what must start at zero). Calls whose GPU work may
  *    overlap - on different streams or from different host threads - race
@@ -388,6 +390,27 @@ int dl_read_device_status(void* d_workspace, uint32_t* status_out, void* stream)
  *   d_workspace  any workspace of this library (256-byte aligned)
  */
 int dl_selftest_wait_timeout(void* d_workspace, int32_t polls, void* stream);
+
+/*
+ * Self-test of the abort path of the staged kernels' tile pipeline (a
+ * diagnostic; the pages have no counterpart). One block streams n_tiles tiles
+ * of 1024 floats from d_src through two shared-memory stages and writes each
+ * tile's sum to d_out[tile]; its producer issues only tiles 0 .. stall_tile-1,
+ * as a stalled copy engine would. The consumers' waits for tile stall_tile
+ * give up after `polls` polls (1 .. 2^22): the block's pipeline aborts exactly
+ * as in the staged kernels - no further copy issued, no further stage read
+ * (d_out[tile] = NaN from stall_tile on), every issued copy waited for before
+ * the block retires - and the workspace's status word gets the bit a stalled
+ * copy sets. No trap, no hang, no fault. stall_tile = n_tiles runs the normal
+ * path (every sum written, status untouched).
+ *   d_workspace  any workspace of this library (256-byte aligned)
+ *   d_src        device, n_tiles * 1024 floats, 16-byte aligned
+ *   n_tiles      1 .. 4096; 0 <= stall_tile <= n_tiles
+ *   d_out        device, n_tiles floats
+ * Errors: DL_ERR_ARG, DL_ERR_ALIGN, DL_ERR_CUDA (launch).
+ */
+int dl_selftest_pipeline(void* d_workspace, const float* d_src, int32_t n_tiles,
+                         int32_t stall_tile, int32_t polls, float* d_out, void* stream);
 
 #ifdef __cplusplus
 }

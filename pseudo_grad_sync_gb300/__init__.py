@@ -98,6 +98,8 @@ def lib():
                                          vp, sz, vp]
         L.dl_selftest_wait_timeout.restype = ctypes.c_int
         L.dl_selftest_wait_timeout.argtypes = [vp, i32, vp]
+        L.dl_selftest_pipeline.restype = ctypes.c_int
+        L.dl_selftest_pipeline.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         L.dl_read_device_status.restype = ctypes.c_int
         L.dl_read_device_status.argtypes = [vp, vp, vp]
         _lib = L
@@ -440,6 +442,23 @@ def selftest_wait_timeout(workspace, polls=1000, stream=None):
     _cuda(workspace)
     _check("dl_selftest_wait_timeout",
            lib().dl_selftest_wait_timeout(_ptr(workspace), int(polls), _stream(stream)))
+
+
+def selftest_pipeline(workspace, src, stall_tile, polls=1000, out=None, stream=None):
+    """Run the tile pipeline's abort self-test (dl_selftest_pipeline): src is a
+    device float32 tensor of n_tiles * 1024 elements; returns the per-tile
+    sums (NaN from stall_tile on when the pipeline aborted)."""
+    n_tiles = src.numel() // 1024
+    if out is None:
+        out = torch.empty(n_tiles, dtype=torch.float32, device=src.device)
+    _need(workspace, _U8, 4, "workspace")
+    _need(src, _F32, n_tiles * 1024, "src")
+    _need(out, _F32, n_tiles, "out")
+    _cuda(workspace, src, out)
+    _check("dl_selftest_pipeline",
+           lib().dl_selftest_pipeline(_ptr(workspace), _ptr(src), n_tiles, int(stall_tile),
+                                      int(polls), _ptr(out), _stream(stream)))
+    return out
 
 
 def read_device_status(workspace, stream=None) -> int:

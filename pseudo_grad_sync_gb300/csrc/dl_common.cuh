@@ -103,12 +103,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
-// Tile pipeline: a producer warp streams (theta_g, theta_k) tiles of TILE
-// elements into a ring of STAGES shared-memory stages with bulk copies;
-// consumer warps wait on the stage's "full" mbarrier and release it through
-// its "empty" mbarrier (one arrival per consumer warp). Waits are bounded: a
-// wait that runs out records kDevErrCopyTimeout, waits once more (bounded) and
-// goes on, so no warp ever blocks a barrier the others wait at.
+// Tile pipeline: a producer warp streams tiles into a ring of STAGES
+// shared-memory stages with bulk copies; consumer warps wait on the stage's
+// "full" mbarrier and release it through its "empty" mbarrier (one arrival
+// per consumer warp). Every wait is bounded. A wait that runs out aborts the
+// block's pipeline: it records kDevErrCopyTimeout in the status word and sets
+// the block's abort flag; from then on the producer issues no copy, the
+// consumers read no stage (they still pass every named barrier, so no warp
+// waits for one that left), and before the block retires the producer waits
+// (bounded) until every copy it issued has landed, so no bulk copy is left
+// writing into the shared memory of a retired block. The call's outputs are
+// then undefined; the status word says so.
 constexpr int kConsumerWarps = kWarps;
 constexpr int kPipeThreads = kThreads + 32;  // + one producer warp
 constexpr int kMaxStages = 4;
@@ -116,6 +121,7 @@ constexpr int kMaxStages = 4;
 struct PipeBarriers {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
+    int abort;  // set once a bounded wait ran out
 };
 
 template <int STAGES>
@@ -126,22 +132,82 @@ __device__ __forceinline__ void pipe_init(PipeBarriers* pb) {
             mbar_init(&pb->full[s], 1);
             mbar_init(&pb->empty[s], kConsumerWarps);
         }
+        pb->abort = 0;
         fence_barrier_init();
     }
     __syncthreads();
 }
 
-// A wait that runs out records the failure, then gives the copies in flight
-// one more bounded wait to land before the warp goes on.
-__device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
-    if (!mbar_wait_bounded(bar, parity)) {
+__device__ __forceinline__ bool pipe_aborted(const PipeBarriers* pb) {
+    return *reinterpret_cast<const volatile int*>(&pb->abort) != 0;
+}
+
+__device__ __forceinline__ void pipe_abort(PipeBarriers* pb, uint32_t* status) {
+    if (!pipe_aborted(pb)) {
+        *reinterpret_cast<volatile int*>(&pb->abort) = 1;
         atomicOr(status, kDevErrCopyTimeout);
-        (void)mbar_wait_bounded(bar, parity);
     }
+}
+
+// Bounded wait that also gives up once the block's pipeline is aborted.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity,
+                                                    const PipeBarriers* pb, long limit) {
+    for (long i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31) == 31 && pipe_aborted(pb)) return false;
+    }
+    return false;
+}
+
+// Consumer warp (all lanes): wait until the stage of tile `it` holds it.
+// Warp-uniform result; false once the pipeline is aborted, and then the stage
+// must not be read.
+template <int STAGES>
+__device__ __forceinline__ bool consumer_wait(PipeBarriers* pb, uint32_t it, uint32_t* status,
+                                              long limit = kSpinLimit) {
+    bool ok = !pipe_aborted(pb) &&
+              mbar_wait_abortable(&pb->full[it % STAGES], (it / STAGES) & 1u, pb, limit);
+    ok = __all_sync(kFull, ok);
+    if (!ok) pipe_abort(pb, status);
+    return ok;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Consumer warp (all lanes): done with the stage of tile `it`. After an
+// abort the stage is not released, so that no copy can be issued into it.
+template <int STAGES>
+__device__ __forceinline__ void consumer_release(PipeBarriers* pb, uint32_t it, bool ok) {
+    __syncwarp();
+    if (ok && (threadIdx.x & 31) == 0) mbar_arrive(&pb->empty[it % STAGES]);
+}
+
+// Producer lane: wait until the stage of tile `it` is free to be written;
+// false once the pipeline is aborted (no copy may be issued then).
+template <int STAGES>
+__device__ __forceinline__ bool producer_acquire(PipeBarriers* pb, uint32_t it, uint32_t* status,
+                                                 long limit = kSpinLimit) {
+    if (pipe_aborted(pb)) return false;
+    if (it < STAGES) return true;
+    if (mbar_wait_abortable(&pb->empty[it % STAGES], ((it / STAGES) - 1) & 1u, pb, limit))
+        return true;
+    pipe_abort(pb, status);
+    return false;
+}
+
+// Producer lane, after its last tile or an abort: `issued` tiles were issued;
+// wait (bounded) until the copies of the last tile of every stage have
+// landed, so that the block never retires with a copy in flight.
+template <int STAGES>
+__device__ __forceinline__ void producer_drain(PipeBarriers* pb, uint32_t issued, uint32_t* status,
+                                               long limit = kSpinLimit) {
+    for (uint32_t s = 0; s < STAGES && s < issued; ++s) {
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % STAGES);  // last tile of stage s
+        if (!mbar_wait_bounded(&pb->full[s], (last / STAGES) & 1u, limit))
+            atomicOr(status, kDevErrCopyTimeout);
+    }
 }
 
 // barrier among the consumer warps only (named barrier 1)
@@ -152,12 +218,13 @@ __device__ __forceinline__ void consumer_sync() {
 // Producer side: lane 0 of the producer warp issues the bulk copies of tile
 // number `it` (its stage is it % STAGES) covering [tb, tb + tn) of two arrays
 // (of one when gb is null: values mode, the second array is never staged).
+// false once the pipeline is aborted: nothing was issued.
 template <int TILE, int STAGES>
-__device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float* sb, const float* ga,
+__device__ __forceinline__ bool pipe_produce(PipeBarriers* pb, float* sa, float* sb, const float* ga,
                                              const float* gb, int64_t tb, int tn, uint32_t it,
                                              uint32_t* status) {
+    if (!producer_acquire<STAGES>(pb, it, status)) return false;
     const int s = static_cast<int>(it % STAGES);
-    if (it >= STAGES) wait_or_flag(&pb->empty[s], ((it / STAGES) - 1) & 1u, status);
     const uint32_t bytes = static_cast<uint32_t>(tn >> 2) * 16u;
     fence_proxy_async();
     mbar_arrive_expect_tx(&pb->full[s], gb ? 2u * bytes : bytes);
@@ -165,6 +232,7 @@ __device__ __forceinline__ void pipe_produce(PipeBarriers* pb, float* sa, float*
         bulk_copy_g2s(sa + s * TILE, ga + tb, bytes, &pb->full[s]);
         if (gb) bulk_copy_g2s(sb + s * TILE, gb + tb, bytes, &pb->full[s]);
     }
+    return true;
 }
 
 // ---------------------------------------------------------------------------

@@ -157,7 +157,77 @@ __global__ void k_selftest_wait(uint32_t* status, long polls) {
     dl::fence_barrier_init();
     if (!dl::mbar_wait_bounded(&bar, 0u, polls)) atomicOr(status, dl::kDevErrCopyTimeout);
 }
+
+// Self-test of the tile pipeline's abort path (dl_common.cuh): one block, a
+// producer warp streaming 1024-float tiles of `src` into two stages with bulk
+// copies and eight consumer warps summing each tile into out[tile]. The
+// producer issues tiles 0 .. stall-1 only, as a stalled copy engine would,
+// then drains the copies it issued. The consumers' bounded waits for tile
+// `stall` run out after `polls` polls: the block's pipeline aborts, the
+// status word gets kDevErrCopyTimeout, the remaining tiles are not read
+// (out[tile] = NaN) and the kernel ends. stall = n_tiles: the normal path.
+constexpr int kSelfTile = 1024;
+constexpr int kSelfStages = 2;
+
+__global__ void __launch_bounds__(dl::kPipeThreads) k_selftest_pipeline(const float* src, int n_tiles,
+                                                                        int stall, long polls,
+                                                                        float* out, uint32_t* status) {
+    extern __shared__ __align__(128) float sbuf[];
+    __shared__ dl::PipeBarriers pb;
+    __shared__ float red[dl::kConsumerWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    dl::pipe_init<kSelfStages>(&pb);
+    if (warp == dl::kConsumerWarps) {  // producer warp
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (; it < static_cast<uint32_t>(stall); ++it) {
+                if (!dl::producer_acquire<kSelfStages>(&pb, it, status, polls)) break;
+                const int s = static_cast<int>(it % kSelfStages);
+                dl::fence_proxy_async();
+                dl::mbar_arrive_expect_tx(&pb.full[s], kSelfTile * 4);
+                dl::bulk_copy_g2s(sbuf + s * kSelfTile, src + static_cast<int64_t>(it) * kSelfTile,
+                                  kSelfTile * 4, &pb.full[s]);
+            }
+            dl::producer_drain<kSelfStages>(&pb, it, status, polls);
+        }
+        return;
+    }
+    for (uint32_t it = 0; it < static_cast<uint32_t>(n_tiles); ++it) {
+        const bool ok = dl::consumer_wait<kSelfStages>(&pb, it, status, polls);
+        float v = 0.f;
+        if (ok) {
+            const float4 x = reinterpret_cast<const float4*>(sbuf + (it % kSelfStages) * kSelfTile)[tid];
+            v = (x.x + x.y) + (x.z + x.w);
+        }
+        for (int sh = 16; sh; sh >>= 1) v += __shfl_xor_sync(dl::kFull, v, sh);
+        if (lane == 0) red[warp] = ok ? v : __int_as_float(0x7fc00000);
+        dl::consumer_release<kSelfStages>(&pb, it, ok);
+        dl::consumer_sync();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < dl::kConsumerWarps; ++w) t += red[w];
+            out[it] = t;
+        }
+        dl::consumer_sync();
+    }
+}
 }  // namespace
+
+extern "C" int dl_selftest_pipeline(void* d_workspace, const float* d_src, int32_t n_tiles,
+                                    int32_t stall_tile, int32_t polls, float* d_out,
+                                    void* stream) {
+    if (!d_workspace || !d_src || !d_out || n_tiles <= 0 || n_tiles > 4096 || stall_tile < 0 ||
+        stall_tile > n_tiles || polls <= 0 || polls > dl::kSpinLimit)
+        return DL_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0 || !dl::aligned16(d_src) ||
+        (reinterpret_cast<uintptr_t>(d_out) & 3u) != 0)
+        return DL_ERR_ALIGN;
+    k_selftest_pipeline<<<1, dl::kPipeThreads, kSelfStages * kSelfTile * sizeof(float),
+                          static_cast<cudaStream_t>(stream)>>>(
+        d_src, n_tiles, stall_tile, static_cast<long>(polls), d_out,
+        static_cast<uint32_t*>(d_workspace));
+    return dl::launch_status();
+}
 
 extern "C" int dl_selftest_wait_timeout(void* d_workspace, int32_t polls, void* stream) {
     if (!d_workspace || polls <= 0 || polls > dl::kSpinLimit) return DL_ERR_ARG;

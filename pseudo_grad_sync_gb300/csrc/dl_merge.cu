@@ -14,10 +14,13 @@
 //                 in ascending order, and stores theta and m back with
 //                 128-bit stores. Each byte of codes, theta and m crosses HBM
 //                 once.
-// k_merge_tma<NPM, STAGES, RDA>  the same merge for up to 4 present learners
-//                 with theta, m and the codes staged through shared memory by
-//                 bulk copies (producer warp, bounded waits); used for the
-//                 mean merge and the RDA merge, bitwise equal to k_merge_q.
+// k_merge_tma<NPM, TILE, STAGES, RDA>  the same merge with theta, m and the
+//                 codes staged through shared memory by bulk copies (producer
+//                 warp, bounded waits); instances for up to 4, 8, 16 and 32
+//                 present learners, each sized to keep 2 blocks per SM; used
+//                 for the mean merge and the RDA merge whatever the number of
+//                 learners, bitwise equal to k_merge_q (which
+//                 DL_MERGE_UNSTAGED=1 selects, for tests).
 // k_merge_u       the unquantised variant: values are the fp32 Delta_k read
 //                 from the learner replicas.
 //
@@ -38,8 +41,7 @@
 // k_merge_q<NPM, true> then decodes through codebooks scaled by c_k and adds
 //                 the values in fp32 in ascending k.
 #include <math.h>
-
-#include <mutex>
+#include <stdlib.h>
 
 #include "dl_common.cuh"
 
@@ -168,49 +170,57 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
 }
 
 // Staged variant of k_merge_q for up to NPM present learners: a producer warp
-// streams tiles of theta, m and every learner's codes into a STAGES-deep
-// shared-memory ring with bulk copies (every wait bounded, failures set the
-// status word), 8 consumer warps decode from shared memory and store theta
-// and m back with 128-bit stores. Per element the arithmetic is k_merge_q's,
-// in the same order, so the results are bitwise the same.
-constexpr int kMTile = 2048;  // elements per stage
-
-template <int NPM, int STAGES, bool RDA>
+// streams tiles of theta, m and every present learner's codes into a
+// STAGES-deep shared-memory ring with bulk copies (bounded waits; an abort
+// stops the pipeline as dl_common.cuh describes), 8 consumer warps decode from
+// shared memory and store theta and m back with 128-bit stores. Per element
+// the arithmetic is k_merge_q's, in the same order, so the results are
+// bitwise the same. Dynamic shared memory: the present learners' codebooks
+// [np][256] f32, then STAGES stages of theta [TILE] f32 | m [TILE] f32 |
+// codes [np][TILE] u8, all sized by the actual np.
+template <int NPM, int TILE, int STAGES, bool RDA>
 __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
+    static_assert(TILE % (4 * kThreads) == 0, "whole float4 groups per consumer thread");
     extern __shared__ __align__(128) unsigned char mbuf[];
-    // stage s: theta [kMTile] f32 | m [kMTile] f32 | codes [NPM][kMTile] u8
-    constexpr int kStageBytes = kMTile * 8 + NPM * kMTile;
-    __shared__ float scb[NPM * kNB];
     __shared__ PipeBarriers pb;
     const int tid = threadIdx.x, lane = tid & 31;
     const int np = a.np;
+    float* scb = reinterpret_cast<float*>(mbuf);
+    unsigned char* stages = mbuf + np * kNB * 4;
+    const int stage_bytes = TILE * (8 + np);
     pipe_init<STAGES>(&pb);
 
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+            bool live = true;
+            for (int64_t c = blockIdx.x; live && c < a.n_chunks; c += gridDim.x) {
                 const int64_t base = c * kChunk;
                 const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-                for (int o = 0; o < cn; o += kMTile, ++it) {
+                for (int o = 0; o < cn; o += TILE) {
+                    if (!producer_acquire<STAGES>(&pb, it, a.status)) {
+                        live = false;
+                        break;
+                    }
                     const int s = static_cast<int>(it % STAGES);
-                    if (it >= STAGES) wait_or_flag(&pb.empty[s], ((it / STAGES) - 1) & 1u, a.status);
-                    const int tn = min(kMTile, cn - o);
+                    const int tn = min(TILE, cn - o);
                     const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;  // whole float4s
                     const uint32_t cbytes = static_cast<uint32_t>(tn >> 4) * 16u;  // whole 16-byte runs
-                    unsigned char* st = mbuf + s * kStageBytes;
+                    unsigned char* st = stages + s * stage_bytes;
                     fence_proxy_async();
                     mbar_arrive_expect_tx(&pb.full[s], 2u * fbytes + static_cast<uint32_t>(np) * cbytes);
                     const int64_t e0 = base + o;
                     if (fbytes) {
                         bulk_copy_g2s(st, a.g + e0, fbytes, &pb.full[s]);
-                        bulk_copy_g2s(st + kMTile * 4, a.m + e0, fbytes, &pb.full[s]);
+                        bulk_copy_g2s(st + TILE * 4, a.m + e0, fbytes, &pb.full[s]);
                     }
                     if (cbytes)
                         for (int k = 0; k < np; ++k)
-                            bulk_copy_g2s(st + kMTile * 8 + k * kMTile, a.cp[k] + e0, cbytes, &pb.full[s]);
+                            bulk_copy_g2s(st + TILE * 8 + k * TILE, a.cp[k] + e0, cbytes, &pb.full[s]);
+                    ++it;
                 }
             }
+            producer_drain<STAGES>(&pb, it, a.status);
         }
         return;
     }
@@ -221,17 +231,17 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
         const int64_t base = c * kChunk;
         const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
         int t0 = tensor_containing(a.off, a.T, base);
-        for (int o = 0; o < cn; o += kMTile, ++it) {
+        for (int o = 0; o < cn; o += TILE, ++it) {
             const int s = static_cast<int>(it % STAGES);
             const int64_t tb = base + o;
-            const int tn = min(kMTile, cn - o);
+            const int tn = min(TILE, cn - o);
             const int fvec = tn & ~3, cvec = tn & ~15;  // elements staged
             const int64_t tend = tb + tn;
-            wait_or_flag(&pb.full[s], (it / STAGES) & 1u, a.status);
-            const unsigned char* st = mbuf + s * kStageBytes;
+            const bool ok = consumer_wait<STAGES>(&pb, it, a.status);
+            const unsigned char* st = stages + s * stage_bytes;
             const float* sg = reinterpret_cast<const float*>(st);
-            const float* sm = reinterpret_cast<const float*>(st + kMTile * 4);
-            const unsigned char* sc = st + kMTile * 8;
+            const float* sm = reinterpret_cast<const float*>(st + TILE * 4);
+            const unsigned char* sc = st + TILE * 8;
             for (int t = t0; t < a.T; ++t) {
                 const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
                 if (o0 >= tend) break;
@@ -250,9 +260,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                     consumer_sync();
                     cur_t = t;
                 }
-                if (pa == tb && pe == tb + kMTile) {
+                if (!ok) continue;  // aborted: the stage is not read
+                if (pa == tb && pe == tb + TILE) {
 #pragma unroll
-                    for (int q = 0; q < kMTile / 4 / kThreads; ++q) {
+                    for (int q = 0; q < TILE / 4 / kThreads; ++q) {
                         const int gi = tid + q * kThreads;  // float4 group in the tile
                         float4 th = reinterpret_cast<const float4*>(sg)[gi];
                         float4 mm = reinterpret_cast<const float4*>(sm)[gi];
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
 #pragma unroll
                         for (int k = 0; k < NPM; ++k) {
                             if (k < np) {
-                                const uint32_t w4 = reinterpret_cast<const uint32_t*>(sc + k * kMTile)[gi];
+                                const uint32_t w4 = reinterpret_cast<const uint32_t*>(sc + k * TILE)[gi];
                                 const float* cbs = scb + k * kNB;
                                 const float ws = a.w[k];
                                 if (RDA) {  // values already scaled
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                         float mm = l < fvec ? sm[l] : a.m[e];
                         float acc = 0.f;
                         for (int k = 0; k < np; ++k) {
-                            const uint32_t code = l < cvec ? sc[k * kMTile + l] : a.cp[k][e];
+                            const uint32_t code = l < cvec ? sc[k * TILE + l] : a.cp[k][e];
                             const float v = scb[k * kNB + code];
                             acc = RDA ? __fadd_rn(acc, v) : __fmaf_rn(a.w[k], v, acc);
                         }
@@ -302,22 +313,41 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pb.empty[s]);
+            consumer_release<STAGES>(&pb, it, ok);
         }
     }
 }
 
-template <int NPM, int STAGES, bool RDA>
+// Tile and stage count of the staged merge by the number of present learners
+// it is instantiated for: 2 blocks of 288 threads per SM, each with at most
+// ~112 KB of dynamic shared memory (codebooks + stages).
+template <int NPM> struct MergeShape;
+template <> struct MergeShape<4> { static constexpr int kTile = 2048, kStages = 3; };   //  76 KB
+template <> struct MergeShape<8> { static constexpr int kTile = 2048, kStages = 3; };   // 104 KB
+template <> struct MergeShape<16> { static constexpr int kTile = 1024, kStages = 3; };  //  88 KB
+template <> struct MergeShape<32> { static constexpr int kTile = 1024, kStages = 2; };  // 112 KB
+
+template <int NPM, bool RDA>
 int launch_tma(const MergeArgs& a, cudaStream_t s) {
-    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, STAGES, RDA>);
-    const size_t smem = static_cast<size_t>(STAGES) * (kMTile * 8 + NPM * kMTile);
+    constexpr int TILE = MergeShape<NPM>::kTile, STAGES = MergeShape<NPM>::kStages;
+    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, TILE, STAGES, RDA>);
+    const size_t smem = static_cast<size_t>(a.np) * kNB * 4 +
+                        static_cast<size_t>(STAGES) * TILE * (8 + a.np);
     int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(smem)));
     if (st != DL_OK) return st;
     const int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
-    k_merge_tma<NPM, STAGES, RDA><<<grid, kPipeThreads, smem, s>>>(a);
+    k_merge_tma<NPM, TILE, STAGES, RDA><<<grid, kPipeThreads, smem, s>>>(a);
     return launch_status();
+}
+
+// The staged merge for any number of present learners.
+template <bool RDA>
+int launch_staged(const MergeArgs& a, cudaStream_t s) {
+    if (a.np <= 4) return launch_tma<4, RDA>(a, s);
+    if (a.np <= 8) return launch_tma<8, RDA>(a, s);
+    if (a.np <= 16) return launch_tma<16, RDA>(a, s);
+    return launch_tma<32, RDA>(a, s);
 }
 
 __global__ void __launch_bounds__(kThreads) k_merge_u(MergeArgs a) {
@@ -365,6 +395,13 @@ int launch_q(const MergeArgs& a, cudaStream_t s) {
         grid_for(reinterpret_cast<const void*>(k_merge_q<NPM, RDA>), kThreads, smem, a.n_chunks);
     k_merge_q<NPM, RDA><<<grid, kThreads, smem, s>>>(a);
     return launch_status();
+}
+
+// DL_MERGE_UNSTAGED=1 (environment) selects k_merge_q instead of the staged
+// merge; the two are bitwise equal, and tests use this to compare them.
+bool merge_unstaged() {
+    const char* v = getenv("DL_MERGE_UNSTAGED");
+    return v && v[0] == '1';
 }
 
 template <bool RDA>
@@ -621,22 +658,16 @@ RdaLayout rda_layout(const HostFrag& f, int K) {
 
 // The library's own device status word: bounded waits of calls that take no
 // workspace (the staged merge of dl_merge_outer_step) report here, and
-// dl_read_device_status(NULL, ...) reads it. One per device.
+// dl_read_device_status(NULL, ...) reads it. One per device; its address on
+// the current device is looked up on every call (a cached address would go
+// stale after a device reset or a new primary context).
 static __device__ uint32_t g_library_status;
 
 namespace dl {
 int library_status_word(uint32_t** out) {
-    static std::mutex mu;
-    static uint32_t* p[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DL_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!p[dev]) {
-        void* q = nullptr;
-        if (cudaGetSymbolAddress(&q, g_library_status) != cudaSuccess || !q) return DL_ERR_CUDA;
-        p[dev] = static_cast<uint32_t*>(q);
-    }
-    *out = p[dev];
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_library_status) != cudaSuccess || !q) return DL_ERR_CUDA;
+    *out = static_cast<uint32_t*>(q);
     return DL_OK;
 }
 
@@ -656,14 +687,12 @@ int merge_outer_step_status(float* theta_g, float* momentum, const uint8_t* cons
         k_merge_u<<<grid, kThreads, 0, s>>>(a);
         return launch_status();
     }
-    if (a.np <= 4) {  // staged through shared memory, 3 stages (2 blocks/SM)
-        int st2 = DL_OK;
-        if (!status) st2 = library_status_word(&status);
-        if (st2 != DL_OK) return st2;
-        a.status = status;
-        return launch_tma<4, 3, false>(a, s);
-    }
-    return launch_quantised<false>(a, s);
+    if (merge_unstaged()) return launch_quantised<false>(a, s);
+    int st2 = DL_OK;
+    if (!status) st2 = library_status_word(&status);
+    if (st2 != DL_OK) return st2;
+    a.status = status;
+    return launch_staged<false>(a, s);
 }
 }  // namespace dl
 
@@ -734,9 +763,7 @@ extern "C" int dl_rda_merge_outer_step(float* theta_g, float* momentum,
     k_rda_coef<<<f.T, kThreads, 0, s>>>(r);
     if ((st = launch_status()) != DL_OK) return st;
     a.rda_c = r.c;
-    if (a.np <= 4) {  // staged, as the mean merge
-        a.status = reinterpret_cast<uint32_t*>(ws);
-        return launch_tma<4, 3, true>(a, s);
-    }
-    return launch_quantised<true>(a, s);
+    if (merge_unstaged()) return launch_quantised<true>(a, s);
+    a.status = reinterpret_cast<uint32_t*>(ws);  // staged, as the mean merge
+    return launch_staged<true>(a, s);
 }

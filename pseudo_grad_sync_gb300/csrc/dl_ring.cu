@@ -259,12 +259,16 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t c = c0; c < c1; ++c) {
+            bool live = true;
+            for (int64_t c = c0; live && c < c1; ++c) {
                 const int64_t base = c * kChunk;
                 const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
                 for (int o = 0; o < cn; o += kRTile, ++it) {
+                    if (!producer_acquire<kRStages>(&pb, it, a.status)) {
+                        live = false;
+                        break;
+                    }
                     const int s = static_cast<int>(it % kRStages);
-                    if (it >= kRStages) wait_or_flag(&pb.empty[s], ((it / kRStages) - 1) & 1u, a.status);
                     const int tn = min(kRTile, cn - o);
                     const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;
                     const uint32_t cbytes = static_cast<uint32_t>(tn >> 4) * 16u;
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
                     if (cbytes) bulk_copy_g2s(st + kRTile * 12, a.codes + e0, cbytes, &pb.full[s]);
                 }
             }
+            producer_drain<kRStages>(&pb, it, a.status);
         }
         return;
     }
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
             const int tn = min(kRTile, cn - o);
             const int fvec = tn & ~3, cvec = tn & ~15;
             const int64_t tend = tb + tn;
-            wait_or_flag(&pb.full[s], (it / kRStages) & 1u, a.status);
+            const bool ok = consumer_wait<kRStages>(&pb, it, a.status);
             const unsigned char* st = rbuf + s * kRStageBytes;
             const float* sg = reinterpret_cast<const float*>(st);
             const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
@@ -315,6 +320,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
                     consumer_sync();
                     cur_t = t;
                 }
+                if (!ok) continue;  // aborted: the stage is not read
                 if (pa == tb && pe == tb + kRTile) {
 #pragma unroll
                     for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
@@ -351,8 +357,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pb.empty[s]);
+            consumer_release<kRStages>(&pb, it, ok);
         }
     }
 }
@@ -392,12 +397,16 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t c = c0; c < c1; ++c) {
+            bool live = true;
+            for (int64_t c = c0; live && c < c1; ++c) {
                 const int64_t base = c * kChunk;
                 const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
                 for (int o = 0; o < cn; o += kRTile, ++it) {
+                    if (!producer_acquire<kRStages>(&pb, it, a.status)) {
+                        live = false;
+                        break;
+                    }
                     const int s = static_cast<int>(it % kRStages);
-                    if (it >= kRStages) wait_or_flag(&pb.empty[s], ((it / kRStages) - 1) & 1u, a.status);
                     const int tn = min(kRTile, cn - o);
                     const uint32_t fbytes = static_cast<uint32_t>(tn >> 2) * 16u;
                     const uint32_t cbytes = DECODE ? static_cast<uint32_t>(tn >> 4) * 16u : 0u;
@@ -412,6 +421,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                     if (cbytes) bulk_copy_g2s(st + kRTile * 8, a.codes + e0, cbytes, &pb.full[s]);
                 }
             }
+            producer_drain<kRStages>(&pb, it, a.status);
         }
         return;
     }
@@ -432,7 +442,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
             const int tn = min(kRTile, cn - o);
             const int fvec = tn & ~3, cvec = tn & ~15;
             const int64_t tend = tb + tn;
-            wait_or_flag(&pb.full[s], (it / kRStages) & 1u, a.status);
+            const bool ok = consumer_wait<kRStages>(&pb, it, a.status);
             const unsigned char* st = rbuf + s * kRMidStageBytes;
             const float* sg = reinterpret_cast<const float*>(st);
             const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
@@ -463,6 +473,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                     small = (o1 - o0) < kSmallTensor;
                     cur_t = t;
                 }
+                if (!ok) continue;  // aborted: the stage is not read
                 if (pa == tb && pe == tb + kRTile) {
 #pragma unroll
                     for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
@@ -507,8 +518,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                     renorm(acc.s2h, acc.s2l);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pb.empty[s]);
+            consumer_release<kRStages>(&pb, it, ok);
         }
     }
     if (cur_t >= 0)

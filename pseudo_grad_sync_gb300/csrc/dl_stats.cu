@@ -160,16 +160,20 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     if ((tid >> 5) == kConsumerWarps) {  // producer warp
         if (lane == 0) {
             uint32_t it = 0;
-            for (int r = r_lo; r < r_hi; ++r) {
+            bool live = true;
+            for (int r = r_lo; live && r < r_hi; ++r) {
                 const int64_t c_hi = a.n_chunks * (r + 1) / a.J;
-                for (int64_t c = a.n_chunks * r / a.J; c < c_hi; ++c) {
+                for (int64_t c = a.n_chunks * r / a.J; live && c < c_hi; ++c) {
                     const int64_t base = c * kChunk;
                     const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-                    for (int o = 0; o < cn; o += kTile, ++it)
-                        pipe_produce<kTile, kStages>(&pb, sg, sr, g, rk, base + o, min(kTile, cn - o),
-                                                     it, a.status);
+                    for (int o = 0; live && o < cn; o += kTile) {
+                        live = pipe_produce<kTile, kStages>(&pb, sg, sr, g, rk, base + o,
+                                                            min(kTile, cn - o), it, a.status);
+                        if (live) ++it;
+                    }
                 }
             }
+            producer_drain<kStages>(&pb, it, a.status);
         }
         return;
     }
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                 const int tn = min(kTile, cn - o);
                 const int tvec = tn & ~3;  // elements staged in shared memory
                 const int64_t tend = tb + tn;
-                wait_or_flag(&pb.full[s], (it / kStages) & 1u, a.status);
+                const bool ok = consumer_wait<kStages>(&pb, it, a.status);
                 const float* tg = sg + s * kTile;
                 const float* tr = sr + s * kTile;
                 for (int t = t0; t < a.T; ++t) {
@@ -212,6 +216,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                         small = (o1 - o0) < kSmallTensor;
                         acc.reset();
                     }
+                    if (!ok) continue;  // aborted: the stage is not read
                     if (pa == tb && pe == tb + kTile && !small) {
                         add_tile<VALUES>(acc, tg, tr, tid, csh);
                     } else {
@@ -235,8 +240,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                         renorm(acc.s2h, acc.s2l);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&pb.empty[s]);
+                consumer_release<kStages>(&pb, it, ok);
             }
         }
         if (cur_t >= 0) flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);

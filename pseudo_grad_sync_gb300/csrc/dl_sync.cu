@@ -15,11 +15,12 @@
 //   main: wait stats_done[b]; quantize(f) from S[b]; record quant_done[b];
 //         merge(f)
 // The side stream forks from the caller's stream at entry and joins it at
-// exit, so on return every effect of the call is ordered on `stream`. The
-// statistics run at one block per SM here (two chunk runs per block, the same
-// runs as the full grid, so the same sums): a statistics block then leaves
-// room on its SM for two quantiser blocks, and the kernels share the SMs
-// instead of taking turns.
+// exit, so on return every effect of the call is ordered on `stream`. From
+// the second fragment on, the statistics run at one block per SM (two chunk
+// runs per block, the same runs as the full grid, so the same sums): a
+// statistics block then leaves room on its SM for two quantiser blocks of the
+// fragment before, and the kernels share the SMs instead of taking turns. The
+// first fragment's statistics, with nothing beside them, take the full grid.
 #include <stdint.h>
 #include <string.h>
 
@@ -320,8 +321,11 @@ extern "C" int dl_outer_sync(const dl_fragment_job* jobs, int32_t n_jobs, int32_
         if (!serial && j >= 2 &&
             (st = cuda_status(cudaStreamWaitEvent(side_s, R->quant_done[b], 0))) != DL_OK)
             break;
+        // the first fragment's statistics run alone: the full grid; later ones
+        // share each SM with the quantiser of the fragment before (same runs,
+        // so the same sums either way)
         st = pseudograd_stats_shared(job.theta_g, p.rep, p.np, job.frag, clip_sigmas, stats_arr[b],
-                                     stats_ws, L.stats_ws, side_s, !serial);
+                                     stats_ws, L.stats_ws, side_s, !serial && j >= 1);
         if (st != DL_OK) break;
         if (!serial) {
             if ((st = cuda_status(cudaEventRecord(R->stats_done[b], side_s))) != DL_OK) break;

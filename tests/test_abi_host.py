@@ -47,6 +47,18 @@ def test_read_device_status_arguments(L):
     assert L.dl_read_device_status(None, ctypes.byref(out), None) == -4
 
 
+def test_selftests_validate_before_launch(L):
+    f = L.dl_selftest_pipeline
+    assert f(None, FAKE, 4, 2, 100, FAKE, None) == -1          # no workspace
+    assert f(FAKE, FAKE, 0, 0, 100, FAKE, None) == -1          # no tiles
+    assert f(FAKE, FAKE, 4, 5, 100, FAKE, None) == -1          # stall past the end
+    assert f(FAKE, FAKE, 4, 2, 0, FAKE, None) == -1            # no polls
+    assert f(FAKE, FAKE, 4, 2, (1 << 22) + 1, FAKE, None) == -1
+    assert f(FAKE + 16, FAKE, 4, 2, 100, FAKE, None) == -2     # workspace not 256-aligned
+    assert f(FAKE, FAKE + 4, 4, 2, 100, FAKE, None) == -2      # source not 16-aligned
+    assert L.dl_selftest_wait_timeout(FAKE, 0, None) == -1
+
+
 def test_shutdown_without_resources_is_a_no_op(L):
     # nothing was created on this host (no GPU): no CUDA call is made
     assert L.dl_shutdown() == 0

@@ -2,7 +2,9 @@
 
 * A bounded wait that nothing completes gives up, reports its failure in the
   workspace's status word and returns; the context stays usable (no trap,
-  no hang).
+  no hang). The staged kernels' tile pipeline, its producer stalled on
+  purpose (it stops issuing copies; nothing faults), aborts, drains its
+  issued copies and reports the same way.
 * Canary bytes around every output buffer and every workspace of every entry
   point are untouched after the calls, on ragged sizes (tails of 1-3
   elements, a tensor of 3, an empty tensor, chunk-crossing tensors).
@@ -41,6 +43,30 @@ def test_bounded_wait_reports_and_returns(dl):
     assert torch.isfinite(cb).all()
     with pytest.raises(dl.DLError):
         dl.selftest_wait_timeout(ws, polls=0)
+
+
+def test_pipeline_abort_drains_and_reports(dl):
+    """The staged kernels' tile pipeline with a producer that stops issuing at
+    tile 5 of 12 (a stalled copy engine, simulated without any fault): the
+    consumers' bounded waits run out, the block aborts - no further copy, no
+    further stage read - waits for its issued copies and ends; the status
+    word reports the timeout and the context keeps working. With no stall the
+    same kernel sums every tile and reports nothing."""
+    ws = dl.new_workspace(256)
+    src = torch.arange(12 * 1024, dtype=torch.float32, device="cuda").remainder_(4096)
+    want = src.view(12, 1024).double().sum(1).float().cpu().numpy()
+    got = dl.selftest_pipeline(ws, src, stall_tile=12, polls=1 << 20).cpu().numpy()
+    assert np.array_equal(got, want)
+    assert dl.read_device_status(ws) == 0
+    for stall in (0, 1, 5):
+        got = dl.selftest_pipeline(ws, src, stall_tile=stall, polls=2000).cpu().numpy()
+        assert np.array_equal(got[:stall], want[:stall])
+        assert np.isnan(got[stall:]).all()
+        assert dl.read_device_status(ws) == 1  # the copy-timeout bit, cleared by the read
+    got = dl.selftest_pipeline(ws, src, stall_tile=12, polls=1 << 20).cpu().numpy()
+    assert np.array_equal(got, want) and dl.read_device_status(ws) == 0
+    with pytest.raises(dl.DLError):
+        dl.selftest_pipeline(ws, src, stall_tile=13)
 
 
 PAD = 256  # elements of guard on each side: keeps workspaces 256-byte aligned

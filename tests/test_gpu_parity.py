@@ -213,32 +213,38 @@ def test_unrepresentative_leading_values():
     compare(g, reps, sizes)
 
 
-def test_staged_merge_equals_the_unstaged_one():
-    """Up to 4 present learners take the merge staged through shared memory;
-    a fifth present learner of weight 0 forces the unstaged kernel without
-    changing any weight or any sum (fmaf(0, v, acc) = acc). Both must give the
-    same theta, momentum and D on ragged tensors (tails of 1-3 elements and
-    of under 16 bytes of codes, chunk-crossing tensors, an empty tensor)."""
+@pytest.mark.parametrize("K", [1, 4, 5, 8, 9, 14, 16, 17, 32])
+def test_staged_merge_equals_the_unstaged_one(K, monkeypatch):
+    """The merge staged through shared memory (one instance per bound on the
+    number of present learners: 4, 8, 16, 32) and the unstaged k_merge_q
+    (DL_MERGE_UNSTAGED=1) must give the same theta, momentum and D bit for
+    bit, on ragged tensors (tails of 1-3 elements and of under 16 bytes of
+    codes, chunk-crossing tensors, an empty tensor), with unequal weights and
+    one absent learner when K > 1."""
     import pseudo_grad_sync_gb300 as dl
     sizes = RAGGED
-    g, reps = _make(sizes, 4, seed=21)
+    g, reps = _make(sizes, K, seed=21 + K)
     m = (np.random.default_rng(22).standard_normal(g.size) * 1e-3).astype(np.float32)
     F = dl.Fragment(sizes)
     gd = torch.from_numpy(g).cuda()
     reps_d = [torch.from_numpy(r).cuda() for r in reps]
     st = dl.pseudograd_stats(gd, reps_d, F)
     codes, cb = dl.quantize(gd, reps_d, F, st)
-    cb5 = torch.cat([cb, cb[:1]])
-    w = np.array([0.7, 1.3, 1.0, 0.4], np.float32)
+    w = (0.5 + np.random.default_rng(23).random(K)).astype(np.float32)
+    present = np.ones(K, np.uint8)
+    if K > 1:
+        present[K // 2] = 0
     outs = []
-    for kk in (4, 5):
+    for unstaged in (False, True):
+        if unstaged:
+            monkeypatch.setenv("DL_MERGE_UNSTAGED", "1")
+        else:
+            monkeypatch.delenv("DL_MERGE_UNSTAGED", raising=False)
         ga, ma = gd.clone(), torch.from_numpy(m).cuda()
         da = torch.empty_like(ga)
-        ww = w if kk == 4 else np.append(w, np.float32(0.0))
-        dl.merge_outer_step(ga, ma, F, codes + codes[:1] if kk == 5 else codes,
-                            cb if kk == 4 else cb5, weights=ww, delta_bar=da, K=kk)
+        dl.merge_outer_step(ga, ma, F, codes, cb, weights=w, present=present, delta_bar=da, K=K)
+        torch.cuda.synchronize()
         outs.append([x.cpu().numpy() for x in (ga, ma, da)])
-    torch.cuda.synchronize()
     for a, b in zip(*outs):
         assert np.array_equal(a, b)  # == on floats: +0 and -0 count as equal
     assert dl.read_device_status(None) == 0

@@ -114,17 +114,16 @@ def test_rda_quorum_failure_leaves_state_untouched(dl):
     assert np.array_equal(gd.cpu().numpy(), g) and np.array_equal(md.cpu().numpy(), m)
 
 
-def test_staged_rda_merge_equals_the_unstaged_one(dl):
-    """Up to 4 present learners take the staged merge; a fifth present learner
-    of weight 0 (a copy of learner 0) forces the unstaged kernels without
-    changing r, u, ||u|| or any sum. D, theta and momentum must be the same."""
-    K = 4
-    g, m, off, codes, cb, cnt = _oracle_quantised(41, RAGGED, K)
-    w = np.array([0.7, 1.3, 1.0, 0.4], np.float32)
+@pytest.mark.parametrize("K", [3, 5, 14, 16, 32])
+def test_staged_rda_merge_equals_the_unstaged_one(dl, K, monkeypatch):
+    """The staged merge (any number of present learners) and the unstaged
+    kernels (DL_MERGE_UNSTAGED=1) give the same D, theta and momentum bit for
+    bit in the RDA merge, with unequal weights."""
+    g, m, off, codes, cb, cnt = _oracle_quantised(41 + K, RAGGED, K)
+    w = (0.5 + np.random.default_rng(42).random(K)).astype(np.float32)
+    monkeypatch.delenv("DL_MERGE_UNSTAGED", raising=False)
     a = _gpu_rda(dl, g, m, RAGGED, codes, cb, cnt, weights=w)
-    codes5 = np.concatenate([codes, codes[:1]])
-    cb5 = np.concatenate([cb, cb[:1]])
-    cnt5 = np.concatenate([cnt, cnt[:1]])
-    b = _gpu_rda(dl, g, m, RAGGED, codes5, cb5, cnt5, weights=np.append(w, np.float32(0.0)))
+    monkeypatch.setenv("DL_MERGE_UNSTAGED", "1")
+    b = _gpu_rda(dl, g, m, RAGGED, codes, cb, cnt, weights=w)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)  # == on floats: +0 and -0 count as equal
