@@ -223,7 +223,7 @@ class DeviceRun:
                 events[f][3].record(stream)
 
 
-LAUNCHES_PER_FRAGMENT = {"stats": 3, "quantize": 2, "merge": 1}
+LAUNCHES_PER_FRAGMENT = {"stats": 1, "quantize": 2, "merge": 1}
 
 
 def traffic_record(name):
@@ -344,7 +344,7 @@ def run_learner(args, rank, world, local):
                      "traffic": None, "kernel": {"stats": "k_stats",
                                                  "quantize": "k_quantize"}[dominant],
                      "note": f"peak = {peak_kind} copy bandwidth"},
-        "clocks": clk, "gpu_launches": args.steps * 5, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * 3, "e2e": None,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -511,7 +511,7 @@ def run_rda(args, rank, world, local):
                      "note": f"{ab} algorithmic B/elem per step; peak = {peak_kind} copy "
                              "bandwidth"},
         "per_call_ms_per_step": tot_calls / args.steps,
-        "clocks": clk, "gpu_launches": args.steps * len(frags) * 9, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * 7, "e2e": None,
         "gpu_launches_note": "kernels in the headline dl_outer_sync (DL_SYNC_RDA) region; the "
                              "per-call sequence, timed after it, launches as many again",
     }
@@ -682,9 +682,15 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     K, n = wl.K, F.n
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    bufs = [reps_d, torch.empty(K, reps_d.stride(0), dtype=torch.float32, device=dev)[:, :n]]
+    stride = reps_d.stride(0)
+    # the padded [K, stride] blocks behind the [K, n] views: with every learner
+    # present a step uploads its replicas as one contiguous copy
+    full_d = [reps_d.as_strided((K, stride), (stride, 1)),
+              torch.empty(K, stride, dtype=torch.float32, device=dev)]
+    bufs = [full_d[0][:, :n], full_d[1][:, :n]]
     g_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
     h_reps = host[1]
+    h_full = h_reps.as_strided((K, stride), (stride, 1))
 
     def run(steps):
         ready = [torch.cuda.Event() for _ in range(steps)]
@@ -697,10 +703,14 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
             with torch.cuda.stream(up):
                 if s >= 2:
                     up.wait_event(done[s - 2])
-                for k in range(K):
-                    if present[k]:
-                        buf[k].copy_(h_reps[k], non_blocking=True)
-                        bi += n * 4
+                if present.all():
+                    full_d[s % 2].copy_(h_full, non_blocking=True)
+                    bi += K * stride * 4
+                else:
+                    for k in range(K):
+                        if present[k]:
+                            buf[k].copy_(h_reps[k], non_blocking=True)
+                            bi += n * 4
                 ready[s].record(up)
             comp.wait_event(ready[s])
             if s >= 1:
@@ -727,21 +737,46 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     dt = time.perf_counter() - t0
     if world > 1:
         dt = max_over_ranks(dt, world, dev)
-    # the host link alone: one large pinned copy of one replica, CUDA events
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(comp)
-    for _ in range(3):
-        bufs[1][0].copy_(h_reps[0], non_blocking=True)
-    b.record(comp)
-    torch.cuda.synchronize()
-    plain = 3 * n * 4 / (a.elapsed_time(b) / 1e3) / 1e9
+    # the host link alone, CUDA events: the same replica block copied by
+    # itself from torch's pinned allocator, and one replica copied from a
+    # page-aligned host buffer registered with cudaHostRegister
+    def copy_gbs(dst, src, reps=2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(comp)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(comp)
+        torch.cuda.synchronize()
+        return reps * src.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9
+
+    plain = copy_gbs(full_d[1], h_full)
+    registered = None
+    try:
+        nbytes = n * 4
+        raw = np.empty(nbytes + 4096, dtype=np.uint8)
+        off = (-raw.ctypes.data) % 4096
+        arr = raw[off:off + nbytes].view(np.float32)
+        arr[:] = h_reps[0].numpy()
+        rt = torch.cuda.cudart()
+        if int(rt.cudaHostRegister(arr.ctypes.data, nbytes, 0)) == 0:
+            try:
+                registered = copy_gbs(full_d[1][0, :n], torch.from_numpy(arr))
+            finally:
+                rt.cudaHostUnregister(arr.ctypes.data)
+    except Exception:
+        registered = None
     return {"value": world * n * steps / dt, "unit": UNIT, "h2d_bytes_per_step": bi // steps,
             "d2h_bytes_per_step": n * 4, "steps": steps, "ms_per_step": dt / steps * 1e3,
             "h2d_gbs": bi / dt / 1e9, "h2d_plain_copy_gbs": plain,
-            "note": "present replicas H2D from pinned memory on an upload stream (two device "
-                    "buffers, step s+1 uploads while step s computes), dl_outer_sync per step, "
-                    "updated theta_g D2H on a download stream; momentum and theta_g stay on "
-                    "the device; h2d_plain_copy_gbs: one pinned replica copied alone"}
+            "h2d_registered_copy_gbs": registered,
+            "note": "present replicas H2D from pinned memory on an upload stream (one copy of "
+                    "the whole [K, n] block when every learner is present; two device buffers, "
+                    "step s+1 uploads while step s computes), dl_outer_sync per step, updated "
+                    "theta_g D2H on a download stream; momentum and theta_g stay on the device. "
+                    "h2d_plain_copy_gbs: the same block copied alone from torch's pinned "
+                    "memory; h2d_registered_copy_gbs: one replica from a cudaHostRegister'ed "
+                    "buffer"}
 
 
 def run_fragment(args, rank, world, local):

@@ -10,9 +10,12 @@
 //              enters it (no separate launch); each chunk is loaded in two
 //              halves with 128-bit loads. Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
-//                  fp32 with one fma; when u is within a proven error guard of an integer
-//                  (or outside (0, 256)) the element is redone in fp64 with
-//                  the exact definition, so codes equal the fp64 rule;
+//                  fp32 with one fma; an element clipped well outside the
+//                  range (fp32 u below -1/2 or above 256.5) takes bucket 0
+//                  or 255 with its segment's constant residual; when u is
+//                  within a proven error guard of an integer (or of the range
+//                  ends) the element is redone in fp64 with the exact
+//                  definition, so codes equal the fp64 rule;
 //                * codebook sum: the residual r = clamp(Delta) - e_b, e_b the
 //                  fp32 bucket edge fmaf(b, w_f, lo_f), is exact or within
 //                  2^-24 bucket widths; it becomes a biased fixed-point
@@ -35,8 +38,6 @@
 // k_cb_fin     one thread per (k, t, b): codebook value = reference + mean
 //              residual (fp64, rounded once to fp32), midpoint for an empty
 //              bucket, and the optional counts.
-#include <mutex>
-
 #include "dl_common.cuh"
 
 namespace dl {
@@ -44,8 +45,12 @@ namespace {
 
 struct SegRt {  // quantiser parameters of one (k, t) segment
     SegQuant q;
-    float mid_g;  // 0.5 - guard
+    float mid_g;   // 0.5 - guard
+    uint32_t qb_lo, qb_hi;  // histogram words of an element clipped to lo / hi
 };
+
+constexpr int kQMaxL = 8;                                        // learners per block at most
+constexpr int kQMaxG = (DL_MAX_LEARNERS + kQMaxL - 1) / kQMaxL;  // learner groups at most
 
 struct QuantArgs {
     const float* g;
@@ -61,7 +66,10 @@ struct QuantArgs {
     int64_t n_chunks;
     int T;
     int K;
-    int J;  // blocks per learner
+    int G;                 // learner groups
+    int gk0[kQMaxG + 1];   // first learner of group g; gk0[G] = K
+    int gb0[kQMaxG + 1];   // first block of group g; gb0[G] = grid size
+    unsigned int* work;    // [G] chunk-batch counters (zeroed with the sums)
 };
 
 constexpr uint32_t kLoMask = (1u << 19) - 1;
@@ -70,11 +78,12 @@ constexpr uint32_t kQMax = (1u << 23) - 1;
 constexpr float kFloorMagic = 12582912.0f;    // 1.5 * 2^23
 constexpr int kFloorMagicBits = 0x4B400000;  // its fp32 bit pattern
 
-__device__ __forceinline__ SegRt seg_params(const dl_stats& st) {
-    SegRt p;
-    p.q = seg_quant(st.lo, st.hi, st.nonfinite);
-    p.mid_g = 0.5f - p.q.guard;
-    return p;
+// residual fixed point of the (clamped) value v in bucket bb, fp64
+__device__ __forceinline__ uint32_t residual_q(const SegQuant& q, int bb, double v) {
+    const double r = __dsub_rn(v, seg_ref(q, bb));
+    long long x = llrint(ldexp(r, q.ks)) + kResBias;
+    x = x < 0 ? 0 : (x > static_cast<long long>(kQMax) ? static_cast<long long>(kQMax) : x);
+    return static_cast<uint32_t>(x);
 }
 
 // fp64 path of one element: the exact bucket rule and residual
@@ -85,17 +94,30 @@ __device__ __forceinline__ void rare_code(float d, const SegQuant& q, int& b, ui
     double v = static_cast<double>(d);
     if (v < q.lo) v = q.lo;
     if (v > q.hi) v = q.hi;
-    const double r = __dsub_rn(v, seg_ref(q, bb));
-    long long x = llrint(ldexp(r, q.ks)) + kResBias;
-    x = x < 0 ? 0 : (x > static_cast<long long>(kQMax) ? static_cast<long long>(kQMax) : x);
     b = bb;
-    qv = static_cast<uint32_t>(x);
+    qv = residual_q(q, bb, v);
 }
 
 // q (< 2^23) enters the histogram as qb = 0x4B000000 + q, the bit pattern of
-// the fp32 value 2^23 + q: word A of bin b gets one count plus q >> 19, word B
-// gets the low 19 bits of q (those of qb, as 0x4B000000 has none)
+// the fp32 value 2^23 + q
 constexpr uint32_t kQBits = 0x4B000000u;
+
+__device__ __forceinline__ SegRt seg_params(const dl_stats& st) {
+    SegRt p;
+    p.q = seg_quant(st.lo, st.hi, st.nonfinite);
+    p.mid_g = 0.5f - p.q.guard;
+    // an element clipped to lo (hi) lands in bucket 0 (255) with the value lo
+    // (hi), so its residual is one constant per segment: what rare_code gives
+    p.qb_lo = p.qb_hi = kQBits;
+    if (p.q.kind == kSegFast) {
+        p.qb_lo = kQBits + residual_q(p.q, 0, p.q.lo);
+        p.qb_hi = kQBits + residual_q(p.q, 255, p.q.hi);
+    }
+    return p;
+}
+
+// word A of bin b gets one count plus q >> 19, word B gets the low 19 bits
+// of q (those of qb, as 0x4B000000 has none)
 __device__ __forceinline__ void hist_add(uint32_t* __restrict__ hA, int b, uint32_t qb) {
     atomicAdd(hA + b, (qb >> 19) + (kCountOne - (kQBits >> 19)));
     atomicAdd(hA + kNB + b, qb & kLoMask);
@@ -119,6 +141,14 @@ __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_
     if (static_cast<unsigned>(b) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= p.mid_g) {
         const float r = __fsub_rn(d, __fmaf_rn(bf, p.q.w_f, p.q.lo_f));
         qb = __float_as_uint(__fmaf_rn(r, p.q.scale, p.q.qoff));
+    } else if (uf < -0.5f) {
+        // clipped below: for the fast kind |uf - u| <= 2^-23 |u| + 2^-23 s |lo|
+        // + ... with 2^-23 s |lo| < guard / 4 < 1/16, so u < 0 and d < lo
+        b = 0;
+        qb = p.qb_lo;
+    } else if (uf > 256.5f) {  // clipped above: likewise u > 256 and d > hi
+        b = 255;
+        qb = p.qb_hi;
     } else {
         uint32_t qv;
         rare_code(d, p.q, b, qv);
@@ -148,27 +178,111 @@ __device__ __forceinline__ void flush_bin(const QuantArgs& a, int k, int t, int 
     l2[kNB + b] = 0ull;
 }
 
-// VALUES: values mode (no replica; Delta is theta_g itself, K = 1)
+// The fast-path parameters of one segment, packed into three 16-byte words
+// so that a block reloads them per learner with three broadcast loads.
+struct __align__(16) FastParams {
+    float s_f, c_f, w_f, lo_f;
+    float scale, qoff, mid_g;
+    uint32_t qb_lo, qb_hi;
+    int kind;
+    int pad0, pad1;
+};
+
+__device__ __forceinline__ FastParams fast_params(const SegRt& p) {
+    FastParams f;
+    f.s_f = p.q.s_f;
+    f.c_f = p.q.c_f;
+    f.w_f = p.q.w_f;
+    f.lo_f = p.q.lo_f;
+    f.scale = p.q.scale;
+    f.qoff = p.q.qoff;
+    f.mid_g = p.mid_g;
+    f.qb_lo = p.qb_lo;
+    f.qb_hi = p.qb_hi;
+    f.kind = p.q.kind;
+    f.pad0 = f.pad1 = 0;
+    return f;
+}
+
+// bucket of one value of a fast-kind segment and its histogram update (the
+// same arithmetic as encode_fast; the fp64 rule from the full parameters)
+__device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, const SegRt* full,
+                                              uint32_t* __restrict__ hA) {
+    const float uf = __fmaf_rn(d, f.s_f, f.c_f);
+    const float tf = __fadd_rd(uf, kFloorMagic);
+    int b = __float_as_int(tf) - kFloorMagicBits;
+    const float bf = __fsub_rn(tf, kFloorMagic);
+    const float fr = __fsub_rn(uf, bf);
+    uint32_t qb;
+    if (static_cast<unsigned>(b) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= f.mid_g) {
+        const float r = __fsub_rn(d, __fmaf_rn(bf, f.w_f, f.lo_f));
+        qb = __float_as_uint(__fmaf_rn(r, f.scale, f.qoff));
+    } else if (uf < -0.5f) {
+        b = 0;
+        qb = f.qb_lo;
+    } else if (uf > 256.5f) {
+        b = 255;
+        qb = f.qb_hi;
+    } else {
+        uint32_t qv;
+        rare_code(d, full->q, b, qv);
+        qb = kQBits + qv;
+    }
+    hist_add(hA, b, qb);
+    return static_cast<uint32_t>(b);
+}
+
+constexpr int kBatch = 1;  // chunks a block takes at a time
+
+// Dynamic shared memory of a quantiser block serving L learners: the
+// double-buffered 32-bit histograms [2][L][word A bins | word B bins] and the
+// 64-bit per-bin sums [L][count bins | residual-sum bins].
+__host__ __device__ constexpr size_t quant_smem(int L) {
+    return static_cast<size_t>(L) * (2 * 2 * kNB * 4 + 2 * kNB * 8);
+}
+
+// Learner-group grid: the K learners form G near-equal groups of at most
+// kQMaxL; group g has blocks gb0[g] .. gb0[g+1]-1, as many as its share of the
+// learners. A block takes batches of kBatch chunks from its group's counter
+// until none is left, so blocks that meet costly chunks (many small tensors)
+// take fewer, and the blocks of all groups sweep the fragment together (the
+// theta_g they read is shared through L2). Per half-chunk a thread loads its
+// theta_g values once and then, learner by learner, that learner's replica
+// values: theta_g is read once per group, not once per learner, and each
+// piece's block barrier and histogram fold serve L learners.
+// VALUES: values mode (no replica; Delta is theta_g itself, K = 1).
 template <bool VALUES>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
-    __shared__ uint32_t l1[2][2 * kNB];             // [parity][word A bins | word B bins]
-    __shared__ unsigned long long l2[2 * kNB];       // [count bins | residual-sum bins]
-    __shared__ SegRt s_seg;                          // parameters of the current tensor
+    extern __shared__ __align__(16) unsigned char qsm[];
+    __shared__ SegRt s_seg[kQMaxL];       // parameters of the current tensor, per learner
+    __shared__ FastParams s_fp[kQMaxL];
+    __shared__ unsigned int s_item;
+    int grp = 0;
+    while (grp + 1 < a.G && static_cast<int>(blockIdx.x) >= a.gb0[grp + 1]) ++grp;
+    const int k0 = a.gk0[grp];
+    const int L = a.gk0[grp + 1] - k0;
+    uint32_t* l1 = reinterpret_cast<uint32_t*>(qsm);
+    unsigned long long* l2 = reinterpret_cast<unsigned long long*>(qsm + static_cast<size_t>(L) * 2 * 2 * kNB * 4);
 
     const int tid = threadIdx.x;
-    const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
     const float* __restrict__ g = a.g;
-    const float* __restrict__ rk = a.r[k];
-    uint8_t* __restrict__ ck = a.codes[k];
-    l1[0][tid] = l1[0][kNB + tid] = l1[1][tid] = l1[1][kNB + tid] = 0u;
-    l2[tid] = l2[kNB + tid] = 0ull;
+    for (int i = tid; i < L * 2 * 2 * kNB; i += kThreads) l1[i] = 0u;
+    for (int i = tid; i < L * 2 * kNB; i += kThreads) l2[i] = 0ull;
     __syncthreads();
 
     int cur_t = -1;  // tensor whose sums are in l2
-    int seg_t = -1;  // tensor whose parameters are in p
+    int seg_t = -1;  // tensor whose parameters are in s_seg
     int par = 0;
-    SegRt p;
-    const int64_t c_lo = a.n_chunks * j / a.J, c_hi = a.n_chunks * (j + 1) / a.J;
+    // thread 0 fetches the next batch while the block works on the current one
+    unsigned int next = tid == 0 ? atomicAdd(a.work + grp, 1u) : 0u;
+    for (;;) {
+    if (tid == 0) s_item = next;
+    __syncthreads();
+    const int64_t c_lo = static_cast<int64_t>(s_item) * kBatch;
+    __syncthreads();  // every thread has read s_item
+    if (c_lo >= a.n_chunks) break;
+    if (tid == 0) next = atomicAdd(a.work + grp, 1u);
+    const int64_t c_hi = min(c_lo + kBatch, a.n_chunks);
     for (int64_t c = c_lo; c < c_hi; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + kChunk, a.n);
@@ -178,79 +292,100 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            if (t != seg_t) {  // block-uniform: thread 0 derives the parameters
-                __syncthreads();  // every thread has its copy of the previous ones
-                if (tid == 0) s_seg = seg_params(a.stats[static_cast<int64_t>(k) * a.T + t]);
+            if (t != seg_t) {  // block-uniform: threads 0..L-1 derive the parameters
+                __syncthreads();  // every read of the previous ones is done
+                if (tid < L) {
+                    s_seg[tid] = seg_params(a.stats[static_cast<int64_t>(k0 + tid) * a.T + t]);
+                    s_fp[tid] = fast_params(s_seg[tid]);
+                }
                 __syncthreads();
-                p = s_seg;
                 seg_t = t;
             }
             const bool full = (pa == base) && (pb == base + kChunk);
-            if (p.q.kind >= kSegDegenerate) {  // every code is 0, no sums
-                if (full) {
-#pragma unroll
-                    for (int q = 0; q < kGroups; ++q)
-                        reinterpret_cast<uint32_t*>(ck + base)[tid + q * kThreads] = 0u;
-                } else {
-                    for (int64_t e = pa + tid; e < pb; e += kThreads) ck[e] = 0;
-                }
-                continue;
-            }
-            uint32_t* hA = l1[par];
+            uint32_t* hpar = l1 + static_cast<size_t>(par) * L * 2 * kNB;
             if (full) {
                 const float4* g4 = reinterpret_cast<const float4*>(g + base);
-                const float4* r4 = reinterpret_cast<const float4*>(rk + base);
-                uint32_t* c4 = reinterpret_cast<uint32_t*>(ck + base);
 #pragma unroll 1
                 for (int h = 0; h < kGroups; h += kGroups / 2) {  // two halves: fewer registers
-                    float4 gv[kGroups / 2], rv[kGroups / 2];
+                    float4 gv[kGroups / 2];
 #pragma unroll
                     for (int q = 0; q < kGroups / 2; ++q) gv[q] = __ldg(g4 + tid + (h + q) * kThreads);
+#pragma unroll 1
+                    for (int l = 0; l < L; ++l) {
+                        const FastParams f = s_fp[l];
+                        uint32_t* c4 = reinterpret_cast<uint32_t*>(a.codes[k0 + l] + base);
+                        if (f.kind >= kSegDegenerate) {  // every code is 0, no sums
 #pragma unroll
-                    for (int q = 0; q < kGroups / 2; ++q)
-                        rv[q] = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                       : __ldcs(r4 + tid + (h + q) * kThreads);
-                    if (p.q.kind == kSegFast) {
-#pragma unroll
-                        for (int q = 0; q < kGroups / 2; ++q) {
-                            const uint32_t b0 = encode_fast(__fsub_rn(gv[q].x, rv[q].x), p, hA);
-                            const uint32_t b1 = encode_fast(__fsub_rn(gv[q].y, rv[q].y), p, hA);
-                            const uint32_t b2 = encode_fast(__fsub_rn(gv[q].z, rv[q].z), p, hA);
-                            const uint32_t b3 = encode_fast(__fsub_rn(gv[q].w, rv[q].w), p, hA);
-                            c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
+                            for (int q = 0; q < kGroups / 2; ++q) c4[tid + (h + q) * kThreads] = 0u;
+                            continue;
                         }
-                    } else {
-                        for (int q = 0; q < kGroups / 2; ++q) {
-                            const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
-                            const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
-                            const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
-                            const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
-                            c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
+                        uint32_t* hA = hpar + l * 2 * kNB;
+                        const float4* r4 = reinterpret_cast<const float4*>(a.r[k0 + l] + base);
+                        float4 rv[kGroups / 2];
+#pragma unroll
+                        for (int q = 0; q < kGroups / 2; ++q)
+                            rv[q] = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                           : __ldcs(r4 + tid + (h + q) * kThreads);
+                        if (f.kind == kSegFast) {
+#pragma unroll
+                            for (int q = 0; q < kGroups / 2; ++q) {
+                                const uint32_t b0 = encode_fp(__fsub_rn(gv[q].x, rv[q].x), f, s_seg + l, hA);
+                                const uint32_t b1 = encode_fp(__fsub_rn(gv[q].y, rv[q].y), f, s_seg + l, hA);
+                                const uint32_t b2 = encode_fp(__fsub_rn(gv[q].z, rv[q].z), f, s_seg + l, hA);
+                                const uint32_t b3 = encode_fp(__fsub_rn(gv[q].w, rv[q].w), f, s_seg + l, hA);
+                                c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
+                            }
+                        } else {
+                            const SegRt p = s_seg[l];
+                            for (int q = 0; q < kGroups / 2; ++q) {
+                                const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
+                                const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
+                                const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
+                                const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
+                                c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
+                            }
                         }
                     }
                 }
             } else {
-                for (int64_t e = pa + tid; e < pb; e += kThreads) {
-                    const float d = __fsub_rn(__ldg(g + e), VALUES ? 0.f : __ldcs(rk + e));
-                    ck[e] = static_cast<uint8_t>(encode_one(d, p, hA));
+                for (int l = 0; l < L; ++l) {
+                    uint8_t* __restrict__ ck = a.codes[k0 + l];
+                    const SegRt p = s_seg[l];
+                    if (p.q.kind >= kSegDegenerate) {
+                        for (int64_t e = pa + tid; e < pb; e += kThreads) ck[e] = 0;
+                        continue;
+                    }
+                    const float* __restrict__ rk = a.r[k0 + l];
+                    uint32_t* hA = hpar + l * 2 * kNB;
+                    for (int64_t e = pa + tid; e < pb; e += kThreads) {
+                        const float d = __fsub_rn(__ldg(g + e), VALUES ? 0.f : __ldcs(rk + e));
+                        ck[e] = static_cast<uint8_t>(encode_one(d, p, hA));
+                    }
                 }
             }
             __syncthreads();  // every update of this piece is in l1[par]
             if (cur_t != t) {
-                if (cur_t >= 0) flush_bin(a, k, cur_t, tid, l2);
+                if (cur_t >= 0)
+                    for (int l = 0; l < L; ++l) flush_bin(a, k0 + l, cur_t, tid, l2 + l * 2 * kNB);
                 cur_t = t;
             }
-            const uint32_t va = hA[tid], vb = hA[kNB + tid];
-            if (va != 0u) {
-                l2[tid] += va >> 18;
-                l2[kNB + tid] += (static_cast<unsigned long long>(va & ((1u << 18) - 1)) << 19) + vb;
-                hA[tid] = 0u;
-                hA[kNB + tid] = 0u;
+            for (int l = 0; l < L; ++l) {
+                uint32_t* hA = hpar + l * 2 * kNB;
+                unsigned long long* l2l = l2 + l * 2 * kNB;
+                const uint32_t va = hA[tid], vb = hA[kNB + tid];
+                if (va != 0u) {
+                    l2l[tid] += va >> 18;
+                    l2l[kNB + tid] += (static_cast<unsigned long long>(va & ((1u << 18) - 1)) << 19) + vb;
+                    hA[tid] = 0u;
+                    hA[kNB + tid] = 0u;
+                }
             }
             par ^= 1;
         }
     }
-    if (cur_t >= 0) flush_bin(a, k, cur_t, tid, l2);
+    }
+    if (cur_t >= 0)
+        for (int l = 0; l < L; ++l) flush_bin(a, k0 + l, cur_t, tid, l2 + l * 2 * kNB);
 }
 
 __global__ void __launch_bounds__(kThreads) k_cb_fin(QuantArgs a) {
@@ -288,6 +423,23 @@ size_t acc_bytes(int K, int T) {
     return align256(sizeof(unsigned long long) * 2 * static_cast<size_t>(K) * T * kNB);
 }
 
+// the workspace's zeroed part: the sums, then the groups' batch counters
+size_t zeroed_bytes(int K, int T) { return acc_bytes(K, T) + 256; }
+
+// Learner groups of the quantiser grid (see k_quantize) for K learners and a
+// grid of `blocks`: G near-equal groups, blocks shared in proportion.
+void plan_groups(QuantArgs& a, int K, int blocks) {
+    const int G = (K + kQMaxL - 1) / kQMaxL;
+    a.G = G;
+    a.gk0[0] = 0;
+    for (int g = 0; g < G; ++g) a.gk0[g + 1] = a.gk0[g] + K / G + (g < K % G ? 1 : 0);
+    a.gb0[0] = 0;
+    for (int g = 0; g < G; ++g) {
+        const int64_t share = static_cast<int64_t>(blocks) * a.gk0[g + 1] / K;
+        a.gb0[g + 1] = static_cast<int>(share > a.gb0[g] ? share : a.gb0[g] + 1);
+    }
+}
+
 }  // namespace
 }  // namespace dl
 
@@ -296,7 +448,7 @@ using namespace dl;
 extern "C" size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    return kWsHeader + acc_bytes(K, f.T);
+    return kWsHeader + zeroed_bytes(K, f.T);
 }
 
 extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
@@ -345,15 +497,23 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     a.K = K;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, acc_bytes(K, f.T), s))) != DL_OK) return st;
+    a.work = reinterpret_cast<unsigned int*>(ws + kWsHeader + acc_bytes(K, f.T));
+    if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, zeroed_bytes(K, f.T), s))) != DL_OK) return st;
     if (a.n_chunks > 0) {
         const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true>)
                                   : reinterpret_cast<const void*>(k_quantize<false>);
-        a.J = blocks_per_learner(kern, kThreads, 0, K, a.n_chunks);
+        const int Lmax = (K + (K + kQMaxL - 1) / kQMaxL - 1) / ((K + kQMaxL - 1) / kQMaxL);
+        const size_t smem = quant_smem(Lmax);
+        if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(quant_smem(kQMaxL))))) != DL_OK)
+            return st;
+        const int64_t batches = (a.n_chunks + kBatch - 1) / kBatch;
+        plan_groups(a, K, grid_for(kern, kThreads, smem, batches * ((K + kQMaxL - 1) / kQMaxL)));
+        const int grid = a.gb0[a.G];
         if (values)
-            k_quantize<true><<<K * a.J, kThreads, 0, s>>>(a);
+            k_quantize<true><<<grid, kThreads, smem, s>>>(a);
         else
-            k_quantize<false><<<K * a.J, kThreads, 0, s>>>(a);
+            k_quantize<false><<<grid, kThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     const int64_t cells = static_cast<int64_t>(K) * f.T * kNB;
@@ -364,25 +524,17 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
 // ---------------------------------------------------------------------------
 // dl_quantize for callers that cannot allocate: the workspace is this static
 // device array (one per device, alive until the process exits). In host code
-// the symbol is only a stand-in; its device address comes from
-// cudaGetSymbolAddress, looked up once per device on the first call.
+// the symbol is only a stand-in; its device address on the current device
+// comes from cudaGetSymbolAddress, looked up on every call (a cached address
+// would go stale after a device reset or a new primary context).
 
 namespace {
 static __device__ __align__(256) unsigned char g_quant_scratch[DL_QUANTIZE_NOALLOC_MAX_BYTES];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};
-
 int scratch_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DL_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_quant_scratch) != cudaSuccess || !p) return DL_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_quant_scratch) != cudaSuccess || !p) return DL_ERR_CUDA;
+    *out = p;
     return DL_OK;
 }
 }  // namespace

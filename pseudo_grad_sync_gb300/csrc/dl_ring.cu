@@ -98,7 +98,7 @@ __device__ __forceinline__ void acc_group(Acc& acc, float v0, float v1, float v2
     const float y2 = __fsub_rn(v2, csh), y3 = __fsub_rn(v3, csh);
     const float mx = absmax_nan(y3, absmax_nan(y2, absmax_nan(y1, absmax_nan(y0, 0.f))));
     if (!small && fast_range(mx)) {
-        if (mx > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, mx);
+        if (mx > acc.yt) rebase(acc, mx);
         ff_add(acc.s1h, acc.s1l, __fadd_rn(__fadd_rn(y0, y1), __fadd_rn(y2, y3)));
         sq_add(acc.s2h, acc.s2l, y0);
         sq_add(acc.s2h, acc.s2l, y1);
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kThreads) k_ring_hop(RingArgs a) {
                             const float ay = fabsf(y);
                             if (!small && fast_range(ay)) {
                                 if (ay > acc.yt)
-                                    rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                                    rebase(acc, ay);
                                 ff_add(acc.s1h, acc.s1l, y);
                                 sq_add(acc.s2h, acc.s2l, y);
                             } else {
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                         const float y = __fsub_rn(v, csh);
                         const float ay = fabsf(y);
                         if (!small && fast_range(ay)) {
-                            if (ay > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                            if (ay > acc.yt) rebase(acc, ay);
                             ff_add(acc.s1h, acc.s1l, y);
                             sq_add(acc.s2h, acc.s2l, y);
                         } else {

@@ -2,34 +2,35 @@
 // section 4.1 step 1: one mu and one sigma per tensor; step 2: the clip
 // range mu +- 6 sigma).
 //
-// Three launches on the caller's stream:
-//  k_shift     one warp per (k, t): c = mean of the first min(N, 64) values
-//              of Delta in fp64, snapped to a power-of-two grid below their
-//              spread and rounded to fp32. Every block later sums
-//              y = Delta - c, which keeps the one-pass variance free of
-//              cancellation when |mu| >> sigma; c is computed once so all
-//              chunks of a tensor share it. The snapping keeps the fp32
-//              rounding of y unbiased (a shift with low-order bits below
-//              ulp(y) biases every rounding the same way).
+// One launch (after a small memset of the per-(k, t) tickets):
 //  k_stats     learner-major persistent grid: block b serves learner
 //              k = b % K and the j-th of J contiguous runs of 8192-element
 //              chunks (j = b / K), so the K blocks that read one chunk of
 //              theta_g run together and theta_g comes from HBM once, then
-//              from L2. A producer warp streams the
-//              (theta_g, theta_k) tiles into a 3-stage shared-memory ring
-//              with bulk copies (TMA engine), 8 consumer warps compute from
-//              shared memory. Per thread: fp32
-//              sums over groups of four, folded into float-float (hi + lo)
-//              sums that persist across all chunks of a tensor (squares on
-//              a power-of-two offset with exact error terms, so no rounding
-//              of a square biases the sum); the block
-//              reduces them (float-float butterfly, fp64 over the 8 warps)
-//              only when it moves to another tensor, into partial slot
-//              (k, t, j). Tensors shorter than 4096 elements and groups of
-//              rare huge, tiny (squares would leave the fp32 normal range) or
-//              non-finite values take an fp64 path.
-//  k_stats_fin one block per (k, t): fixed-order fp64 sum of its J partials, then
-//              mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population).
+//              from L2. A producer warp streams the (theta_g, theta_k) tiles
+//              into a 2-stage shared-memory ring with bulk copies (TMA
+//              engine), 8 consumer warps compute from shared memory; 3
+//              blocks per SM. Entering a tensor, one warp derives the tensor's shift c from
+//              its first min(N, 64) values of Delta (their fp64 mean,
+//              snapped to a power-of-two grid below their spread, rounded to
+//              fp32); every block entering the tensor derives the same c.
+//              The sums are of y = Delta - c, which keeps the one-pass
+//              variance free of cancellation when |mu| >> sigma; the
+//              snapping keeps the fp32 rounding of y unbiased (a shift with
+//              low-order bits below ulp(y) biases every rounding the same
+//              way). Per thread: fp32 sums over groups of four, folded into
+//              float-float (hi + lo) sums that persist across all chunks of
+//              a tensor, squares two at a time with fp32x2 instructions on a
+//              power-of-two offset with exact error terms (so no rounding of
+//              a square biases the sum); the block reduces them
+//              (float-float butterfly, fp64 over the 8 warps) when it leaves
+//              the tensor, into partial slot (k, t, run), and counts it on
+//              the (k, t) ticket. The block whose count completes the
+//              tensor's runs sums the partials in a fixed order (fp64) and
+//              writes mu = c + S1/N, sigma^2 = S2/N - (S1/N)^2 (population),
+//              lo/hi = mu -+ clip sigma. Tensors shorter than 4096 elements
+//              and groups of rare huge, tiny (squares would leave the fp32
+//              normal range) or non-finite values take an fp64 path.
 // The result is deterministic: every sum has a fixed order.
 #include "dl_stats_acc.cuh"
 
@@ -42,6 +43,8 @@ struct StatsArgs {
     const int64_t* off;
     float* shift;
     Partial* part;
+    unsigned int* ticket;  // [K*T] partials written so far (zeroed per call)
+    dl_stats* out;
     uint32_t* status;
     int64_t n;
     int64_t n_chunks;
@@ -51,24 +54,6 @@ struct StatsArgs {
     int RPB;  // runs per block: block j takes runs j * RPB .. (j + 1) * RPB - 1
     double clip;
 };
-
-__global__ void __launch_bounds__(kThreads) k_shift(StatsArgs a) {
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= a.K * a.T) return;
-    const int k = w / a.T, t = w % a.T;
-    const int64_t o = a.off[t];
-    const int64_t N = a.off[t + 1] - o;
-    const int m = N < 64 ? static_cast<int>(N) : 64;
-    const bool h0 = lane < m, h1 = lane + 32 < m;
-    const float* rk = a.r[k];  // null: values mode, Delta = theta_g itself
-    const double v0 =
-        h0 ? static_cast<double>(__fsub_rn(a.g[o + lane], rk ? rk[o + lane] : 0.f)) : 0.0;
-    const double v1 =
-        h1 ? static_cast<double>(__fsub_rn(a.g[o + lane + 32], rk ? rk[o + lane + 32] : 0.f)) : 0.0;
-    const float c = warp_shift(v0, v1, h0, h1, m);
-    if (lane == 0) a.shift[w] = c;
-}
 
 constexpr int kTile = 4096;  // elements per pipeline tile
 
@@ -81,33 +66,40 @@ constexpr int kGroupsPerTile = kTile / 4 / kThreads;
 template <bool VALUES>
 __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float* tr, int tid,
                                          float csh) {
-    float y[kGroupsPerTile][4];
+    // y = fl(fl(g - r) - c) two at a time: fma(r, -1, g) and fl(d + (-c)) round
+    // exactly as the scalar subtractions
+    const float2 m1 = make_float2(-1.f, -1.f);
+    const float2 nc = make_float2(-csh, -csh);
+    float2 y[kGroupsPerTile][2];  // (y0, y1), (y2, y3) of each group of four
     float mx = 0.f;
 #pragma unroll
     for (int q = 0; q < kGroupsPerTile; ++q) {
         const float4 gv = reinterpret_cast<const float4*>(tg)[tid + q * kThreads];
         const float4 rv = VALUES ? make_float4(0.f, 0.f, 0.f, 0.f)
                                  : reinterpret_cast<const float4*>(tr)[tid + q * kThreads];
-        y[q][0] = __fsub_rn(__fsub_rn(gv.x, rv.x), csh);
-        y[q][1] = __fsub_rn(__fsub_rn(gv.y, rv.y), csh);
-        y[q][2] = __fsub_rn(__fsub_rn(gv.z, rv.z), csh);
-        y[q][3] = __fsub_rn(__fsub_rn(gv.w, rv.w), csh);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) mx = absmax_nan(y[q][e], mx);
+        y[q][0] = __fadd2_rn(__ffma2_rn(make_float2(rv.x, rv.y), m1, make_float2(gv.x, gv.y)), nc);
+        y[q][1] = __fadd2_rn(__ffma2_rn(make_float2(rv.z, rv.w), m1, make_float2(gv.z, gv.w)), nc);
+        mx = absmax_nan(y[q][0].x, mx);
+        mx = absmax_nan(y[q][0].y, mx);
+        mx = absmax_nan(y[q][1].x, mx);
+        mx = absmax_nan(y[q][1].y, mx);
     }
     // squares, their error terms and H0 stay normal and finite for
     // 2^-50 <= |y| <= 2^48 (smaller values lose at most 2^-149); mx is NaN if
     // any y is, so the fp64 path (which counts it) takes that share
     if (fast_range(mx)) {
-        if (mx > acc.yt) rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, mx);
+        if (mx > acc.yt) rebase(acc, mx);
 #pragma unroll
         for (int q = 0; q < kGroupsPerTile; ++q) {
-            const float b1 = __fadd_rn(__fadd_rn(y[q][0], y[q][1]), __fadd_rn(y[q][2], y[q][3]));
-            ff_add(acc.s1h, acc.s1l, b1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sq_add(acc.s2h, acc.s2l, y[q][e]);
+            // (y0 + y1, y2 + y3) in one paired add, then their sum
+            const float2 p = __fadd2_rn(make_float2(y[q][0].x, y[q][1].x),
+                                        make_float2(y[q][0].y, y[q][1].y));
+            ff_add(acc.s1h, acc.s1l, __fadd_rn(p.x, p.y));
+            sq_add2(acc, y[q][0]);
+            sq_add2(acc, y[q][1]);
         }
         renorm(acc.s2h, acc.s2l);
+        renorm(acc.s2hb, acc.s2lb);
     } else {
         acc.side = true;
 #pragma unroll 1
@@ -123,6 +115,56 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
     }
 }
 
+// The run (of the J runs of chunks) that holds chunk c: the largest r with
+// floor(n_chunks r / J) <= c. Every run has a chunk (J <= n_chunks).
+__device__ __forceinline__ int64_t run_of_chunk(int64_t c, int64_t n_chunks, int J) {
+    return ((c + 1) * J - 1) / n_chunks;
+}
+
+// The statistics of (k, t) from the partials of every run that meets tensor t,
+// summed by one warp in a fixed order (lane-strided, then a fixed butterfly):
+// mu = shift + S1/N, sigma^2 = S2/N - (S1/N)^2 (population), lo/hi = mu -+
+// clip sigma. Called by the warp of the block that wrote the last partial;
+// the partials and the shift come from other blocks, so they are read past L1.
+__device__ void finish_stats(const StatsArgs& a, int k, int t, int64_t o0, int64_t o1) {
+    const int lane = threadIdx.x & 31;
+    const int64_t N = o1 - o0;
+    const int64_t rf = run_of_chunk(o0 / kChunk, a.n_chunks, a.J);
+    const int64_t rl = run_of_chunk((o1 - 1) / kChunk, a.n_chunks, a.J);
+    const Partial* pk = a.part + (static_cast<int64_t>(k) * a.T + t) * a.J;
+    double s1 = 0.0, s2 = 0.0;
+    long long bad = 0;
+    for (int64_t r = rf + lane; r <= rl; r += 32) {
+        s1 += __ldcg(&pk[r].s1);
+        s2 += __ldcg(&pk[r].s2);
+        bad += __ldcg(&pk[r].bad);
+    }
+    for (int sh = 16; sh; sh >>= 1) {
+        s1 += __shfl_xor_sync(kFull, s1, sh);
+        s2 += __shfl_xor_sync(kFull, s2, sh);
+        bad += __shfl_xor_sync(kFull, bad, sh);
+    }
+    if (lane != 0) return;
+    dl_stats st;
+    st.count = N;
+    st.nonfinite = bad;
+    if (bad > 0) {
+        st.mean = st.std = st.lo = st.hi = __longlong_as_double(0x7ff8000000000000LL);
+    } else {
+        const double inv = 1.0 / static_cast<double>(N);
+        const double mrel = s1 * inv;
+        double var = s2 * inv - mrel * mrel;
+        if (!(var > 0.0)) var = 0.0;
+        const double sigma = sqrt(var);
+        const double mu = static_cast<double>(__ldcg(a.shift + static_cast<int64_t>(k) * a.T + t)) + mrel;
+        st.mean = mu;
+        st.std = sigma;
+        st.lo = mu - a.clip * sigma;
+        st.hi = mu + a.clip * sigma;
+    }
+    a.out[static_cast<int64_t>(k) * a.T + t] = st;
+}
+
 // Learner-major persistent grid: block b serves learner k = b % K and the
 // j-th contiguous run of chunks, j = b / K. The K blocks that read the same chunk
 // of theta_g run side by side, so theta_g crosses HBM once and is served to
@@ -130,10 +172,8 @@ __device__ __forceinline__ void add_tile(Acc& acc, const float* tg, const float*
 // tiles of those chunks into a STAGES-deep shared-memory ring with bulk
 // copies; 8 consumer warps compute from shared memory. Each consumer thread
 // keeps its sums across every tile of a tensor; the consumers reduce them
-// only when they move to another tensor. Two shapes: 3 stages with 2 blocks
-// per SM, and 2 stages with 3 blocks per SM (the same bytes in flight, more
-// consumer warps; faster when K is small and every element-learner brings
-// a theta_g value from HBM).
+// only when they move to another tensor. Launched as 2 stages with 3 blocks
+// per SM.
 // VALUES: values mode (no replica; Delta is theta_g itself, K = 1)
 template <int STAGES, int MINB, bool VALUES>
 __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
@@ -145,6 +185,8 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
     __shared__ float red_ff[kConsumerWarps][4];
     __shared__ double red_side[kConsumerWarps][2];
     __shared__ int red_bad[kConsumerWarps];
+    __shared__ float s_shift;
+    __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int k = blockIdx.x % a.K, j = blockIdx.x / a.K;
@@ -178,6 +220,37 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
         return;
     }
 
+    // the first block of each learner writes the statistics of its empty
+    // tensors (no partial ever reaches them)
+    if (j == 0)
+        for (int t = tid; t < a.T; t += kThreads)
+            if (__ldg(a.off + t + 1) == __ldg(a.off + t)) {
+                dl_stats st;
+                st.count = st.nonfinite = 0;
+                st.mean = st.std = st.lo = st.hi = 0.0;
+                a.out[static_cast<int64_t>(k) * a.T + t] = st;
+            }
+
+    // The partial of (k, t) for run r goes to its slot; thread 0 then counts
+    // it on the (k, t) ticket, and the block that completes the count
+    // finishes the statistics of (k, t).
+    auto flush_and_count = [&](Acc& acc_, Partial* slot, int t) {
+        flush_partial(acc_, slot, red_ff, red_side, red_bad);
+        const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
+        if (tid == 0) {
+            __threadfence();  // the partial (and any shift) before the count
+            const int64_t expect = run_of_chunk((o1 - 1) / kChunk, a.n_chunks, a.J) -
+                                   run_of_chunk(o0 / kChunk, a.n_chunks, a.J) + 1;
+            const unsigned int done = atomicAdd(a.ticket + static_cast<int64_t>(k) * a.T + t, 1u) + 1u;
+            s_last = static_cast<int64_t>(done) == expect;
+        }
+        consumer_sync();
+        if (s_last && tid < 32) {
+            __threadfence();
+            finish_stats(a, k, t, o0, o1);
+        }
+    };
+
     uint32_t it = 0;
     for (int r = r_lo; r < r_hi; ++r) {
         // slot (k, t, r) of this run's sums sits at part_k + t * J
@@ -209,10 +282,29 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                     if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
                     if (pa >= pe) continue;
                     if (t != cur_t) {
-                        if (cur_t >= 0)
-                            flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
+                        if (cur_t >= 0) flush_and_count(acc, part_k + cur_t * a.J, cur_t);
+                        // the shift of (k, t), from the tensor's first values:
+                        // every block entering the tensor derives the same one
+                        if (tid < 32) {
+                            const int64_t N = o1 - o0;
+                            const int m = N < 64 ? static_cast<int>(N) : 64;
+                            const bool h0 = tid < m, h1 = tid + 32 < m;
+                            const double v0 = h0 ? static_cast<double>(__fsub_rn(
+                                                       __ldg(g + o0 + tid), VALUES ? 0.f : __ldg(rk + o0 + tid)))
+                                                 : 0.0;
+                            const double v1 = h1 ? static_cast<double>(__fsub_rn(
+                                                       __ldg(g + o0 + tid + 32),
+                                                       VALUES ? 0.f : __ldg(rk + o0 + tid + 32)))
+                                                 : 0.0;
+                            const float cs = warp_shift(v0, v1, h0, h1, m);
+                            if (tid == 0) {
+                                s_shift = cs;
+                                if (pa == o0) a.shift[static_cast<int64_t>(k) * a.T + t] = cs;
+                            }
+                        }
+                        consumer_sync();
                         cur_t = t;
-                        csh = __ldg(a.shift + k * a.T + t);
+                        csh = s_shift;
                         small = (o1 - o0) < kSmallTensor;
                         acc.reset();
                     }
@@ -229,7 +321,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                             const float ay = fabsf(y);
                             if (!small && fast_range(ay)) {
                                 if (ay > acc.yt)
-                                    rebase(acc.s2h, acc.s2l, acc.c2h, acc.c2l, acc.yt, acc.h0, ay);
+                                    rebase(acc, ay);
                                 ff_add(acc.s1h, acc.s1l, y);
                                 sq_add(acc.s2h, acc.s2l, y);
                             } else {
@@ -243,7 +335,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                 consumer_release<kStages>(&pb, it, ok);
             }
         }
-        if (cur_t >= 0) flush_partial(acc, part_k + cur_t * a.J, red_ff, red_side, red_bad);
+        if (cur_t >= 0) flush_and_count(acc, part_k + cur_t * a.J, cur_t);
     }
 }
 
@@ -347,9 +439,10 @@ using namespace dl;
 extern "C" size_t dl_stats_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    // partials for K * T * J blocks, J <= kMaxBlocksTotal / K: sized as
-    // T * kMaxBlocksTotal so that the need never decreases with K
-    return kWsHeader + shift_bytes(K, f.T) +
+    // shifts and tickets per (k, t), then partials for K * T * J runs with
+    // J <= kMaxBlocksTotal / K: sized as T * kMaxBlocksTotal so that the need
+    // never decreases with K
+    return kWsHeader + 2 * shift_bytes(K, f.T) +
            align256(sizeof(Partial) * static_cast<size_t>(f.T) * kMaxBlocksTotal);
 }
 
@@ -394,19 +487,20 @@ int pseudograd_stats_shared(const float* theta_g, const float* const* theta_k, i
     char* ws = static_cast<char*>(d_workspace);
     a.status = reinterpret_cast<uint32_t*>(ws);
     a.shift = reinterpret_cast<float*>(ws + kWsHeader);
-    a.part = reinterpret_cast<Partial*>(ws + kWsHeader + shift_bytes(K, f.T));
+    a.ticket = reinterpret_cast<unsigned int*>(ws + kWsHeader + shift_bytes(K, f.T));
+    a.part = reinterpret_cast<Partial*>(ws + kWsHeader + 2 * shift_bytes(K, f.T));
+    a.out = d_stats;
     a.n = f.n;
     a.n_chunks = n_chunks_of(f.n);
     a.T = f.T;
     a.K = K;
     a.clip = clip_sigmas;
     a.J = 1;
-    const bool shallow = K <= 2;
-    const void* kern =
-        shallow ? (values ? reinterpret_cast<const void*>(k_stats<2, 3, true>)
-                          : reinterpret_cast<const void*>(k_stats<2, 3, false>))
-                : reinterpret_cast<const void*>(k_stats<3, 2, false>);
-    const size_t smem_used = sizeof(float) * 2 * (shallow ? 2 : 3) * kTile;
+    // 2 stages x 3 blocks per SM: more consumer warps for the same bytes in
+    // flight than 3 stages x 2 blocks, which measured slower at every K
+    const void* kern = values ? reinterpret_cast<const void*>(k_stats<2, 3, true>)
+                              : reinterpret_cast<const void*>(k_stats<2, 3, false>);
+    const size_t smem_used = sizeof(float) * 2 * 2 * kTile;
     const size_t smem = smem_used;
     if (a.n_chunks > 0) {
         if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -421,21 +515,15 @@ int pseudograd_stats_shared(const float* theta_g, const float* const* theta_k, i
     const int JB = (a.J + a.RPB - 1) / a.RPB;  // blocks per learner
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const size_t part_bytes = sizeof(Partial) * static_cast<size_t>(K) * f.T * a.J;
-    if ((st = cuda_status(cudaMemsetAsync(a.part, 0, part_bytes, s))) != DL_OK) return st;
-    const int warps = K * f.T;
-    const int small_grid = (warps * 32 + kThreads - 1) / kThreads;
-    k_shift<<<small_grid, kThreads, 0, s>>>(a);
-    if ((st = launch_status()) != DL_OK) return st;
-    if (a.n_chunks > 0) {
-        if (shallow)
-            values ? k_stats<2, 3, true><<<K * JB, kPipeThreads, smem, s>>>(a)
-                   : k_stats<2, 3, false><<<K * JB, kPipeThreads, smem, s>>>(a);
-        else
-            k_stats<3, 2, false><<<K * JB, kPipeThreads, smem, s>>>(a);
-        if ((st = launch_status()) != DL_OK) return st;
-    }
-    return stats_finish(a.off, f.T, K, a.J, a.shift, a.part, a.clip, d_stats, s);
+    // no elements at all: every (k, t) has N = 0, finished without partials
+    if (a.n_chunks == 0) return stats_finish(a.off, f.T, K, 0, a.shift, a.part, a.clip, d_stats, s);
+    const size_t ticket_bytes = sizeof(unsigned int) * static_cast<size_t>(K) * f.T;
+    if ((st = cuda_status(cudaMemsetAsync(a.ticket, 0, ticket_bytes, s))) != DL_OK) return st;
+    if (values)
+        k_stats<2, 3, true><<<K * JB, kPipeThreads, smem, s>>>(a);
+    else
+        k_stats<2, 3, false><<<K * JB, kPipeThreads, smem, s>>>(a);
+    return launch_status();
 }
 }  // namespace dl
 

@@ -43,18 +43,32 @@ __device__ __forceinline__ void side_add(float d, float c, double& s1, double& s
 struct Acc {
     float s1h, s1l;  // float-float sum of y
     float s2h, s2l;  // float-float H0 + sum of y^2 since the last rebase
+    float s2hb, s2lb;  // a second such sum: the odd lane of packed (fp32x2) squares
     float c2h, c2l;  // float-float sum of y^2 before it
     float yt, h0;    // current bound on |y| and H0 = yt^2
     double s1d, s2d; // fp64 side sums
     int bad;
     bool side;
     __device__ __forceinline__ void reset() {
-        s1h = s1l = s2h = s2l = c2h = c2l = yt = h0 = 0.f;
+        s1h = s1l = s2h = s2l = s2hb = s2lb = c2h = c2l = yt = h0 = 0.f;
         s1d = s2d = 0.0;
         bad = 0;
         side = false;
     }
 };
+
+// Join the squares of one offset sum (hi, lo) = H0 + squares into (c2h, c2l):
+// hi >= H0 and H0 is a power of two on hi's ulp grid, so hi - H0 is exact.
+__device__ __forceinline__ void join_squares(float& c2h, float& c2l, float hi, float lo, float h0) {
+    ff_add_ff(c2h, c2l, __fsub_rn(hi, h0), lo);
+}
+
+// The odd-lane sum holds squares only where the packed path ran; elsewhere
+// it stays at (H0, 0) and is left out, so that kernels which never use it
+// keep their sums bit for bit.
+__device__ __forceinline__ bool odd_lane_used(const Acc& acc) {
+    return acc.s2hb != acc.h0 || acc.s2lb != 0.f;
+}
 
 // Reduction over the kThreads accumulating threads (named barrier 1) of the
 // per-thread sums of one tensor into the partial slot *dst. Fixed order
@@ -62,9 +76,10 @@ struct Acc {
 static __device__ void flush_partial(Acc& acc, Partial* dst, float (*red_ff)[4],
                                      double (*red_side)[2], int* red_bad) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // remove the offset (s2h >= H0, a power of two on its ulp grid, so the
+    // remove the offsets (s2h >= H0, a power of two on its ulp grid, so the
     // difference is exact) and join the squares summed before the last rebase
-    ff_add_ff(acc.c2h, acc.c2l, __fsub_rn(acc.s2h, acc.h0), acc.s2l);
+    join_squares(acc.c2h, acc.c2l, acc.s2h, acc.s2l, acc.h0);
+    if (odd_lane_used(acc)) join_squares(acc.c2h, acc.c2l, acc.s2hb, acc.s2lb, acc.h0);
     acc.s2h = acc.c2h;
     acc.s2l = acc.c2l;
 #pragma unroll
@@ -132,16 +147,30 @@ __device__ __forceinline__ void sq_add(float& hi, float& lo, float y) {
 }
 
 // |y| up to mx (positive, normal) is about to be summed and exceeds yt: move
-// the offset sum into (c2h, c2l) and restart on yt = the power of two >= mx.
-// Taken at a thread's first non-zero group of a tensor and then only when a
-// value exceeds every earlier one by enough to cross a power of two.
-__device__ __forceinline__ void rebase(float& s2h, float& s2l, float& c2h, float& c2l, float& yt,
-                                    float& h0, float mx) {
-    ff_add_ff(c2h, c2l, __fsub_rn(s2h, h0), s2l);
-    yt = __int_as_float((__float_as_int(mx) + 0x7FFFFF) & static_cast<int>(0xFF800000u));
-    h0 = __fmul_rn(yt, yt);
-    s2h = h0;
-    s2l = 0.f;
+// the offset sums into (c2h, c2l) and restart them on yt = the power of two
+// >= mx. Taken at a thread's first non-zero group of a tensor and then only
+// when a value exceeds every earlier one by enough to cross a power of two.
+__device__ __forceinline__ void rebase(Acc& acc, float mx) {
+    join_squares(acc.c2h, acc.c2l, acc.s2h, acc.s2l, acc.h0);
+    if (odd_lane_used(acc)) join_squares(acc.c2h, acc.c2l, acc.s2hb, acc.s2lb, acc.h0);
+    acc.yt = __int_as_float((__float_as_int(mx) + 0x7FFFFF) & static_cast<int>(0xFF800000u));
+    acc.h0 = __fmul_rn(acc.yt, acc.yt);
+    acc.s2h = acc.s2hb = acc.h0;
+    acc.s2l = acc.s2lb = 0.f;
+}
+
+// Two squares at once (fp32x2 instructions, each lane rounded as the scalar
+// ones): y.x goes to (s2h, s2l), y.y to (s2hb, s2lb), with sq_add's exact
+// error terms.
+__device__ __forceinline__ void sq_add2(Acc& acc, float2 y) {
+    const float2 hi = make_float2(acc.s2h, acc.s2hb);
+    const float2 s = __ffma2_rn(y, y, hi);
+    const float2 err = __ffma2_rn(y, y, __ffma2_rn(s, make_float2(-1.f, -1.f), hi));
+    const float2 lo = __fadd2_rn(make_float2(acc.s2l, acc.s2lb), err);
+    acc.s2h = s.x;
+    acc.s2hb = s.y;
+    acc.s2l = lo.x;
+    acc.s2lb = lo.y;
 }
 
 // fold lo into hi (|lo| <= ulp(hi) afterwards), so that the roundings of

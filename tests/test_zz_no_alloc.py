@@ -73,11 +73,9 @@ def test_noalloc_matches_quantize_on_two_calls(noalloc, reverse):
         for k in range(K):
             assert torch.equal(codes_a[k], codes_b[k])
         assert torch.equal(counts_a, counts_b)
-        s = dl.stats_to_host(stats)
-        width = (s["hi"] - s["lo"]) / 256
-        a, b = cb_a.cpu().numpy(), cb_b.cpu().numpy()
-        tol = 2 * np.spacing(np.abs(a)).astype(np.float64) + width[..., None] * 2.0**-21
-        assert np.all(np.abs(a.astype(np.float64) - b) <= tol)
+        # the same kernels on the same inputs, with integer bucket sums: the
+        # codebooks agree bit for bit
+        assert torch.equal(cb_a, cb_b)
 
 
 def test_noalloc_rejects_fragments_beyond_its_scratch(noalloc):
