@@ -610,16 +610,19 @@ def oracle_fragment_pass(g, reps, off, present, weights):
     return dt
 
 
-def fragment_cpu_sample(wl, ts, host, limit):
-    """Host arrays (theta_g, replicas, offsets, elements) of the oracle's
-    bounded sample: the fragment's tensors in order up to `limit` elements
-    (at least one tensor), sliced from the host copy or generated."""
+def fragment_cpu_sample(wl, ts, host, limit, generate=True):
+    """Host arrays (theta_g, replicas, offsets, elements, tensors) of the
+    oracle's bounded sample: the fragment's tensors in order up to `limit`
+    elements (at least one tensor), sliced from the host copy or generated
+    (generate=False: the selection only)."""
     sel, tot = [], 0
     for t in ts:
         if sel and tot + wl.numels[t] > limit:
             continue
         sel.append(t)
         tot += wl.numels[t]
+    if not generate:
+        return None, None, None, tot, sel
     off = synthetic.offsets_of([wl.numels[t] for t in sel])
     if host is not None and sel == ts[:len(sel)]:
         g = host[0].numpy()[:tot]
@@ -794,6 +797,10 @@ def run_fragment(args, rank, world, local):
     wl = synthetic.WORKLOADS[args.workload]()
     K = wl.K
     ts, fid = bench_fragment(wl, dl.plan_fragments)
+    if args.sample_elems:
+        # a smaller case of the same kernels (profiling): the fragment's
+        # tensors in order up to that many elements
+        ts = fragment_cpu_sample(wl, ts, None, args.sample_elems, generate=False)[4]
     numels = [wl.numels[t] for t in ts]
     F = dl.Fragment(numels, dev)
     n = F.n
@@ -893,7 +900,7 @@ def run_fragment(args, rank, world, local):
     dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
     mean_np = sum(kps) / len(kps)
     kernel_of = {"stats": "k_stats", "quantize": "k_quantize",
-                 "merge": "k_merge_tma" if max(kps) <= 4 else "k_merge_q"}
+                 "merge": "k_merge_tma"}
     tr = traffic_record(kernel_of[dominant])
     traffic = None if tr is None else tr["dram_bytes_per_elem"] * n
     roofline = {"bound": "hbm", "achieved": round(calls[dominant]["achieved_gbs"], 1),
@@ -924,6 +931,7 @@ def run_fragment(args, rank, world, local):
         "data": "synthetic (device-filled)" if device_filled else "synthetic",
         "config": {"workload": wl.name + ": " + desc, "K": K, "fragment_elems": n,
                    "fragment_tensors": len(ts), "mean_present_learners": mean_np,
+                   "sample_elems": args.sample_elems or None,
                    "l2": "no flush: every call streams >= 12 GB, inputs far larger than L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "full_step_gbs": full_gbs, "full_step_frac": full_gbs / peak,
@@ -1021,7 +1029,7 @@ def run_ours(args, rank, world, local):
     full_gbs = (sum(ab.values()) * n_total) / (ms_per_step / 1e3) / 1e9
     dominant = max(calls, key=lambda c: calls[c]["ms_per_step"])
     kernel_of = {"stats": "k_stats", "quantize": "k_quantize",
-                 "merge": "k_merge_tma" if K <= 4 else "k_merge_q"}
+                 "merge": "k_merge_tma"}
     tr = traffic_record(kernel_of[dominant])
     traffic = None
     if tr is not None:
@@ -1248,6 +1256,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--sample-elems", type=int, default=0,
+                    help="fragment workloads: sync only the bench fragment's tensors in "
+                         "order up to this many elements (a small case for profiling)")
     ap.add_argument("--mode", choices=["outer", "ring", "rda"], default="outer",
                     help="ring: accumulate along a ring, re-quantising at every hop; "
                          "rda: Radial-Directional Averaging merge")

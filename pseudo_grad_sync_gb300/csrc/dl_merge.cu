@@ -14,7 +14,7 @@
 //                 in ascending order, and stores theta and m back with
 //                 128-bit stores. Each byte of codes, theta and m crosses HBM
 //                 once.
-// k_merge_tma<NPM, TILE, STAGES, RDA>  the same merge with theta, m and the
+// k_merge_tma<NPM, TILE, STAGES, MINB, RDA>  the same merge with theta, m and the
 //                 codes staged through shared memory by bulk copies (producer
 //                 warp, bounded waits); instances for up to 4, 8, 16 and 32
 //                 present learners, each sized to keep 2 blocks per SM; used
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kThreads) k_merge_q(MergeArgs a) {
 // bitwise the same. Dynamic shared memory: the present learners' codebooks
 // [np][256] f32, then STAGES stages of theta [TILE] f32 | m [TILE] f32 |
 // codes [np][TILE] u8, all sized by the actual np.
-template <int NPM, int TILE, int STAGES, bool RDA>
-__global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
+template <int NPM, int TILE, int STAGES, int MINB, bool RDA>
+__global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
     static_assert(TILE % (4 * kThreads) == 0, "whole float4 groups per consumer thread");
     extern __shared__ __align__(128) unsigned char mbuf[];
     __shared__ PipeBarriers pb;
@@ -318,26 +318,27 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_merge_tma(MergeArgs a) {
     }
 }
 
-// Tile and stage count of the staged merge by the number of present learners
-// it is instantiated for: 2 blocks of 288 threads per SM, each with at most
-// ~112 KB of dynamic shared memory (codebooks + stages).
+// Tile, stage count and blocks per SM of the staged merge by the number of
+// present learners it is instantiated for: blocks of 288 threads, each with
+// at most ~112 KB of dynamic shared memory (codebooks + stages).
 template <int NPM> struct MergeShape;
-template <> struct MergeShape<4> { static constexpr int kTile = 2048, kStages = 3; };   //  76 KB
-template <> struct MergeShape<8> { static constexpr int kTile = 2048, kStages = 3; };   // 104 KB
-template <> struct MergeShape<16> { static constexpr int kTile = 1024, kStages = 3; };  //  88 KB
-template <> struct MergeShape<32> { static constexpr int kTile = 1024, kStages = 2; };  // 112 KB
+template <> struct MergeShape<4> { static constexpr int kTile = 2048, kStages = 3, kMinB = 2; };   //  76 KB
+template <> struct MergeShape<8> { static constexpr int kTile = 2048, kStages = 3, kMinB = 2; };   // 104 KB
+template <> struct MergeShape<16> { static constexpr int kTile = 2048, kStages = 2, kMinB = 2; };  // 112 KB
+template <> struct MergeShape<32> { static constexpr int kTile = 1024, kStages = 2, kMinB = 2; };  // 112 KB
 
 template <int NPM, bool RDA>
 int launch_tma(const MergeArgs& a, cudaStream_t s) {
     constexpr int TILE = MergeShape<NPM>::kTile, STAGES = MergeShape<NPM>::kStages;
-    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, TILE, STAGES, RDA>);
+    constexpr int MINB = MergeShape<NPM>::kMinB;
+    const void* k = reinterpret_cast<const void*>(k_merge_tma<NPM, TILE, STAGES, MINB, RDA>);
     const size_t smem = static_cast<size_t>(a.np) * kNB * 4 +
                         static_cast<size_t>(STAGES) * TILE * (8 + a.np);
     int st = cuda_status(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(smem)));
     if (st != DL_OK) return st;
     const int grid = grid_for(k, kPipeThreads, smem, a.n_chunks);
-    k_merge_tma<NPM, TILE, STAGES, RDA><<<grid, kPipeThreads, smem, s>>>(a);
+    k_merge_tma<NPM, TILE, STAGES, MINB, RDA><<<grid, kPipeThreads, smem, s>>>(a);
     return launch_status();
 }
 

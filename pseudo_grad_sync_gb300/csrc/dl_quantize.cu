@@ -70,6 +70,7 @@ struct QuantArgs {
     int gk0[kQMaxG + 1];   // first learner of group g; gk0[G] = K
     int gb0[kQMaxG + 1];   // first block of group g; gb0[G] = grid size
     unsigned int* work;    // [G] chunk-batch counters (zeroed with the sums)
+    int batch;             // contiguous chunks per batch
 };
 
 constexpr uint32_t kLoMask = (1u << 19) - 1;
@@ -232,7 +233,8 @@ __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, cons
     return static_cast<uint32_t>(b);
 }
 
-constexpr int kBatch = 1;  // chunks a block takes at a time
+constexpr int kBatchesPerBlock = 32;  // chunk batches a block takes, about
+constexpr int kMaxBatch = 16;         // chunks per batch at most
 
 // Dynamic shared memory of a quantiser block serving L learners: the
 // double-buffered 32-bit histograms [2][L][word A bins | word B bins] and the
@@ -243,15 +245,17 @@ __host__ __device__ constexpr size_t quant_smem(int L) {
 
 // Learner-group grid: the K learners form G near-equal groups of at most
 // kQMaxL; group g has blocks gb0[g] .. gb0[g+1]-1, as many as its share of the
-// learners. A block takes batches of kBatch chunks from its group's counter
-// until none is left, so blocks that meet costly chunks (many small tensors)
-// take fewer, and the blocks of all groups sweep the fragment together (the
-// theta_g they read is shared through L2). Per half-chunk a thread loads its
+// learners. A block takes batches of contiguous chunks (about 32 per block,
+// 1 to 16 chunks each) from its group's counter until none is left, so
+// blocks that meet costly chunks (many small tensors) take fewer, and the
+// blocks of all groups sweep the fragment together (the theta_g they read is
+// shared through L2). Per half-chunk a thread loads its
 // theta_g values once and then, learner by learner, that learner's replica
 // values: theta_g is read once per group, not once per learner, and each
 // piece's block barrier and histogram fold serve L learners.
-// VALUES: values mode (no replica; Delta is theta_g itself, K = 1).
-template <bool VALUES>
+// VALUES: values mode (no replica; Delta is theta_g itself, K = 1). ONE: one
+// learner per block (K = 1), whose parameters stay in registers.
+template <bool VALUES, bool ONE>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     extern __shared__ __align__(16) unsigned char qsm[];
     __shared__ SegRt s_seg[kQMaxL];       // parameters of the current tensor, per learner
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     int grp = 0;
     while (grp + 1 < a.G && static_cast<int>(blockIdx.x) >= a.gb0[grp + 1]) ++grp;
     const int k0 = a.gk0[grp];
-    const int L = a.gk0[grp + 1] - k0;
+    const int L = ONE ? 1 : a.gk0[grp + 1] - k0;
     uint32_t* l1 = reinterpret_cast<uint32_t*>(qsm);
     unsigned long long* l2 = reinterpret_cast<unsigned long long*>(qsm + static_cast<size_t>(L) * 2 * 2 * kNB * 4);
 
@@ -273,16 +277,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     int cur_t = -1;  // tensor whose sums are in l2
     int seg_t = -1;  // tensor whose parameters are in s_seg
     int par = 0;
+    FastParams f_one;  // ONE: the learner's parameters for the current tensor
     // thread 0 fetches the next batch while the block works on the current one
     unsigned int next = tid == 0 ? atomicAdd(a.work + grp, 1u) : 0u;
     for (;;) {
     if (tid == 0) s_item = next;
     __syncthreads();
-    const int64_t c_lo = static_cast<int64_t>(s_item) * kBatch;
+    const int64_t c_lo = static_cast<int64_t>(s_item) * a.batch;
     __syncthreads();  // every thread has read s_item
     if (c_lo >= a.n_chunks) break;
     if (tid == 0) next = atomicAdd(a.work + grp, 1u);
-    const int64_t c_hi = min(c_lo + kBatch, a.n_chunks);
+    const int64_t c_hi = min(c_lo + a.batch, a.n_chunks);
     for (int64_t c = c_lo; c < c_hi; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + kChunk, a.n);
@@ -299,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                     s_fp[tid] = fast_params(s_seg[tid]);
                 }
                 __syncthreads();
+                if (ONE) f_one = s_fp[0];
                 seg_t = t;
             }
             const bool full = (pa == base) && (pb == base + kChunk);
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                     for (int q = 0; q < kGroups / 2; ++q) gv[q] = __ldg(g4 + tid + (h + q) * kThreads);
 #pragma unroll 1
                     for (int l = 0; l < L; ++l) {
-                        const FastParams f = s_fp[l];
+                        const FastParams f = ONE ? f_one : s_fp[l];
                         uint32_t* c4 = reinterpret_cast<uint32_t*>(a.codes[k0 + l] + base);
                         if (f.kind >= kSegDegenerate) {  // every code is 0, no sums
 #pragma unroll
@@ -500,20 +506,27 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     a.work = reinterpret_cast<unsigned int*>(ws + kWsHeader + acc_bytes(K, f.T));
     if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, zeroed_bytes(K, f.T), s))) != DL_OK) return st;
     if (a.n_chunks > 0) {
-        const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true>)
-                                  : reinterpret_cast<const void*>(k_quantize<false>);
+        const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true, true>)
+                           : K == 1 ? reinterpret_cast<const void*>(k_quantize<false, true>)
+                                    : reinterpret_cast<const void*>(k_quantize<false, false>);
         const int Lmax = (K + (K + kQMaxL - 1) / kQMaxL - 1) / ((K + kQMaxL - 1) / kQMaxL);
         const size_t smem = quant_smem(Lmax);
         if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(quant_smem(kQMaxL))))) != DL_OK)
             return st;
-        const int64_t batches = (a.n_chunks + kBatch - 1) / kBatch;
-        plan_groups(a, K, grid_for(kern, kThreads, smem, batches * ((K + kQMaxL - 1) / kQMaxL)));
+        plan_groups(a, K, grid_for(kern, kThreads, smem, a.n_chunks * ((K + kQMaxL - 1) / kQMaxL)));
         const int grid = a.gb0[a.G];
+        // batches of contiguous chunks, about kBatchesPerBlock per block: short
+        // enough that the last ones finish together, long enough that a block
+        // rarely changes tensor between batches
+        const int64_t per_block = a.n_chunks * a.G / (static_cast<int64_t>(grid) * kBatchesPerBlock);
+        a.batch = static_cast<int>(per_block < 1 ? 1 : (per_block > kMaxBatch ? kMaxBatch : per_block));
         if (values)
-            k_quantize<true><<<grid, kThreads, smem, s>>>(a);
+            k_quantize<true, true><<<grid, kThreads, smem, s>>>(a);
+        else if (K == 1)
+            k_quantize<false, true><<<grid, kThreads, smem, s>>>(a);
         else
-            k_quantize<false><<<grid, kThreads, smem, s>>>(a);
+            k_quantize<false, false><<<grid, kThreads, smem, s>>>(a);
         if ((st = launch_status()) != DL_OK) return st;
     }
     const int64_t cells = static_cast<int64_t>(K) * f.T * kNB;
