@@ -254,7 +254,8 @@ __host__ __device__ constexpr size_t quant_smem(int L) {
 // values: theta_g is read once per group, not once per learner, and each
 // piece's block barrier and histogram fold serve L learners.
 // VALUES: values mode (no replica; Delta is theta_g itself, K = 1). ONE: one
-// learner per block (K = 1), whose parameters stay in registers.
+// learner per block (K = 1): its parameters stay in registers and each block
+// takes one static contiguous run of chunks.
 template <bool VALUES, bool ONE>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     extern __shared__ __align__(16) unsigned char qsm[];
@@ -278,16 +279,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     int seg_t = -1;  // tensor whose parameters are in s_seg
     int par = 0;
     FastParams f_one;  // ONE: the learner's parameters for the current tensor
-    // thread 0 fetches the next batch while the block works on the current one
-    unsigned int next = tid == 0 ? atomicAdd(a.work + grp, 1u) : 0u;
-    for (;;) {
-    if (tid == 0) s_item = next;
-    __syncthreads();
-    const int64_t c_lo = static_cast<int64_t>(s_item) * a.batch;
-    __syncthreads();  // every thread has read s_item
-    if (c_lo >= a.n_chunks) break;
-    if (tid == 0) next = atomicAdd(a.work + grp, 1u);
-    const int64_t c_hi = min(c_lo + a.batch, a.n_chunks);
+    // Learner groups: thread 0 fetches the next batch while the block works on
+    // the current one. One learner per block (no group to share theta_g with):
+    // one static contiguous run of chunks per block, no fetches.
+    unsigned int next = (!ONE && tid == 0) ? atomicAdd(a.work + grp, 1u) : 0u;
+    for (int round = 0;; ++round) {
+    int64_t c_lo, c_hi;
+    if (ONE) {
+        if (round > 0) break;
+        c_lo = a.n_chunks * blockIdx.x / gridDim.x;
+        c_hi = a.n_chunks * (blockIdx.x + 1) / gridDim.x;
+    } else {
+        if (tid == 0) s_item = next;
+        __syncthreads();
+        c_lo = static_cast<int64_t>(s_item) * a.batch;
+        __syncthreads();  // every thread has read s_item
+        if (c_lo >= a.n_chunks) break;
+        if (tid == 0) next = atomicAdd(a.work + grp, 1u);
+        c_hi = min(c_lo + a.batch, a.n_chunks);
+    }
     for (int64_t c = c_lo; c < c_hi; ++c) {
         const int64_t base = c * kChunk;
         const int64_t cend = min(base + kChunk, a.n);
