@@ -548,30 +548,11 @@ def quorum_schedule(wl, step):
     return wl.present(f, s), wl.weights(f, s)
 
 
-def fragment_host(wl, ts, pin):
-    """theta_g [n] and the K replicas [K, n] of one fragment as (pinned) host
-    tensors from the seeded generator."""
-    import torch
-
-    n = sum(wl.numels[t] for t in ts)
-    g = torch.empty(n, dtype=torch.float32, pin_memory=pin)
-    # rows padded to 64 elements: every replica starts 256-byte aligned
-    reps = torch.empty((wl.K, -(-n // 64) * 64), dtype=torch.float32, pin_memory=pin)[:, :n]
-    gn, rn = g.numpy(), reps.numpy()
-    o = 0
-    for t in ts:
-        m = wl.numels[t]
-        wl.theta_global(t, out=gn[o:o + m])
-        for k in range(wl.K):
-            wl.replica(k, t, gn[o:o + m], out=rn[k, o:o + m])
-        o += m
-    return g, reps
-
-
 def fragment_device_fill(wl, ts, dev, seed=0):
-    """theta_g and the K replicas filled on the device with the workload's
-    distributions (theta_g ~ N(0, theta_std), Delta = scale * N(0, 1) or
-    scale * Student-t(3)), for batches too large to generate on the host."""
+    """theta_g and the K replicas (rows padded to 64 elements) filled on the
+    device from a seeded generator with the workload's distributions
+    (theta_g ~ N(0, theta_std), Delta = scale * N(0, 1) or scale *
+    Student-t(3))."""
     import torch
 
     gen = torch.Generator(device=dev)
@@ -804,17 +785,19 @@ def run_fragment(args, rank, world, local):
     numels = [wl.numels[t] for t in ts]
     F = dl.Fragment(numels, dev)
     n = F.n
-    device_filled = wl.name == "ragged_heavy"  # 2.4G elements x 9 arrays: filled on the device
+    # inputs filled on the device from a seeded generator (seconds, where the
+    # host generator would take minutes for every rank of a multi-GPU run);
+    # the e2e pass uploads a pinned host copy of the same values
     t0 = time.time()
-    host = None
-    if device_filled:
-        g, reps = fragment_device_fill(wl, ts, dev, seed=rank)
-    else:
-        host = fragment_host(wl, ts, pin=not args.no_e2e)
-        g = host[0].to(dev)
-        reps = torch.empty(host[1].shape[0], host[1].stride(0), dtype=torch.float32,
-                           device=dev)[:, :n]
-        reps.copy_(host[1])
+    g, reps = fragment_device_fill(wl, ts, dev, seed=rank)
+    host, e2e_error = None, None
+    if not args.no_e2e and wl.name != "ragged_heavy":
+        try:
+            h_reps = torch.empty(K, reps.stride(0), dtype=torch.float32, pin_memory=True)[:, :n]
+            h_reps.copy_(reps)
+            host = (None, h_reps)
+        except RuntimeError as exc:  # pinned host memory exhausted (many ranks per node)
+            e2e_error = f"pinned host buffer of {K * reps.stride(0) * 4 / 1e9:.1f} GB: {exc}"[:300]
     gen_s = time.time() - t0
     m = torch.zeros_like(g)
     rep_list = [reps[k] for k in range(K)]
@@ -912,8 +895,11 @@ def run_fragment(args, rank, world, local):
                          f"peak = {peak_kind} copy bandwidth from MEASURED_PEAKS.json; traffic "
                          "= ncu DRAM bytes per launch (null unless captured for this source)")}
     e2e = None
-    if host is not None and not args.no_e2e:
+    if host is not None:
         e2e = fragment_e2e(wl, F, g, m, reps, host, sync, args, world, dev)
+    elif e2e_error is not None:
+        e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+               "error": e2e_error}
     desc = {"decoder_10b": "10B decoder set cut into P=24 by the LPT planner; the median "
                            f"fragment (#{fid}, {len(ts)} tensors) synced per step with K={K} "
                            "replicas resident, momentum carried across steps",
@@ -922,13 +908,13 @@ def run_fragment(args, rank, world, local):
                           "subset of 1..16 and weights U[0.5,1.5] per step (the workload's "
                           "(fragment, outer step) draws in turn), momentum carried",
             "ragged_heavy": f"{len(ts)} ragged tensors 64..16Mi as one batch, K={K}, "
-                            "Delta = 1e-3 Student-t(3), device-filled"}[wl.name]
+                            "Delta = 1e-3 Student-t(3)"}[wl.name]
     out = {
         "metric": METRIC, "value": world * n / (ms_per_step / 1e3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (device-filled)" if device_filled else "synthetic",
+        "data": "synthetic (device-filled, seeded)",
         "config": {"workload": wl.name + ": " + desc, "K": K, "fragment_elems": n,
                    "fragment_tensors": len(ts), "mean_present_learners": mean_np,
                    "sample_elems": args.sample_elems or None,
@@ -943,7 +929,7 @@ def run_fragment(args, rank, world, local):
         "e2e": e2e, "setup_generate_s": gen_s,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = fragment_cpu_baseline(wl, ts, host, args.cpu_budget)
+        out["cpu_baseline"] = fragment_cpu_baseline(wl, ts, None, args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
 

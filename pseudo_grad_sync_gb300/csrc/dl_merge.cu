@@ -319,11 +319,11 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
 }
 
 // Tile, stage count and blocks per SM of the staged merge by the number of
-// present learners it is instantiated for: blocks of 288 threads, each with
+// present learners it is instantiated for: blocks of 288 threads (2 or 3 per SM), each with
 // at most ~112 KB of dynamic shared memory (codebooks + stages).
 template <int NPM> struct MergeShape;
 template <> struct MergeShape<4> { static constexpr int kTile = 2048, kStages = 3, kMinB = 2; };   //  76 KB
-template <> struct MergeShape<8> { static constexpr int kTile = 2048, kStages = 3, kMinB = 2; };   // 104 KB
+template <> struct MergeShape<8> { static constexpr int kTile = 2048, kStages = 2, kMinB = 3; };   //  72 KB
 template <> struct MergeShape<16> { static constexpr int kTile = 2048, kStages = 2, kMinB = 2; };  // 112 KB
 template <> struct MergeShape<32> { static constexpr int kTile = 1024, kStages = 2, kMinB = 2; };  // 112 KB
 
