@@ -228,8 +228,9 @@ size_t dl_outer_sync_workspace_bytes(const dl_fragment_job* jobs, int32_t n_jobs
  *
  * Scheduling: the statistics of fragment j+1 run on a library-owned side
  * stream beside the quantisation and merge of fragment j on `stream`
- * (two statistics buffers), with half the blocks of a standalone call (each
- * takes two of the same chunk runs, so the sums and results are the same). The side stream forks from `stream` at entry and
+ * (two statistics buffers); from the second fragment on with half the
+ * blocks of a standalone call (each takes two of the same chunk runs, so the
+ * sums and results are the same). The side stream forks from `stream` at entry and
  * joins it before return, so all effects are ordered on `stream`. The side
  * stream and its events are created on the current device on first use and
  * live until dl_shutdown (or process exit); enqueueing is serialised per
