@@ -155,6 +155,18 @@ def test_flush_path_with_one_block(monkeypatch):
     compare(g, reps, sizes)
 
 
+@pytest.mark.parametrize("grid,K", [(1, 5), (3, 14), (7, 9), (2, 17), (5, 1)])
+def test_small_grids_learner_groups_and_batches(grid, K, monkeypatch):
+    """A capped grid makes the quantiser's blocks take multi-chunk batches from
+    their group's counter (and, for K > 8, serve unequal learner groups with
+    fewer blocks than chunks); the statistics blocks take long chunk runs.
+    Ragged tensors across chunk edges, a tail, a tensor under 4096 elements."""
+    monkeypatch.setenv("DL_GRID_LIMIT", str(grid))
+    sizes = [8192 * 40 + 3, 5000, 8192 * 7 + 100, 64, 8192 * 25]
+    g, reps = _make(sizes, K, seed=40 + K)
+    compare(g, reps, sizes)
+
+
 def test_tail_not_multiple_of_four():
     for n in (1, 2, 3, 5, 8191, 8193, 24579):
         g, reps = _make([n], 2, seed=n)
