@@ -233,6 +233,43 @@ __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, cons
     return static_cast<uint32_t>(b);
 }
 
+
+// Four values of a fast-kind segment, packed codes returned. When all four
+// values of every lane take encode_fp's first branch (the common case), the
+// warp runs that branch's arithmetic straight through, with the four
+// histogram updates back to back; otherwise each value goes through
+// encode_fp. Both routes give the same codes and sums.
+__device__ __forceinline__ uint32_t encode4_fp(float4 gq, float4 rq, const FastParams& f,
+                                               const SegRt* full, uint32_t* __restrict__ hA) {
+    const float d[4] = {__fsub_rn(gq.x, rq.x), __fsub_rn(gq.y, rq.y), __fsub_rn(gq.z, rq.z),
+                        __fsub_rn(gq.w, rq.w)};
+    float bf[4];
+    int b[4];
+    bool ok = true;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float uf = __fmaf_rn(d[e], f.s_f, f.c_f);
+        const float tf = __fadd_rd(uf, kFloorMagic);
+        b[e] = __float_as_int(tf) - kFloorMagicBits;
+        bf[e] = __fsub_rn(tf, kFloorMagic);
+        const float fr = __fsub_rn(uf, bf[e]);
+        ok = ok && static_cast<unsigned>(b[e]) < 256u && fabsf(__fsub_rn(fr, 0.5f)) <= f.mid_g;
+    }
+    if (__all_sync(kFull, ok)) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float r = __fsub_rn(d[e], __fmaf_rn(bf[e], f.w_f, f.lo_f));
+            hist_add(hA, b[e], __float_as_uint(__fmaf_rn(r, f.scale, f.qoff)));
+        }
+        return pack4(b[0], b[1], b[2], b[3]);
+    }
+    const uint32_t c0 = encode_fp(d[0], f, full, hA);
+    const uint32_t c1 = encode_fp(d[1], f, full, hA);
+    const uint32_t c2 = encode_fp(d[2], f, full, hA);
+    const uint32_t c3 = encode_fp(d[3], f, full, hA);
+    return pack4(c0, c1, c2, c3);
+}
+
 constexpr int kBatchesPerBlock = 32;  // chunk batches a block takes, about
 constexpr int kMaxBatch = 16;         // chunks per batch at most
 
@@ -344,13 +381,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                                            : __ldcs(r4 + tid + (h + q) * kThreads);
                         if (f.kind == kSegFast) {
 #pragma unroll
-                            for (int q = 0; q < kGroups / 2; ++q) {
-                                const uint32_t b0 = encode_fp(__fsub_rn(gv[q].x, rv[q].x), f, s_seg + l, hA);
-                                const uint32_t b1 = encode_fp(__fsub_rn(gv[q].y, rv[q].y), f, s_seg + l, hA);
-                                const uint32_t b2 = encode_fp(__fsub_rn(gv[q].z, rv[q].z), f, s_seg + l, hA);
-                                const uint32_t b3 = encode_fp(__fsub_rn(gv[q].w, rv[q].w), f, s_seg + l, hA);
-                                c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
-                            }
+                            for (int q = 0; q < kGroups / 2; ++q)
+                                c4[tid + (h + q) * kThreads] = encode4_fp(gv[q], rv[q], f, s_seg + l, hA);
                         } else {
                             const SegRt p = s_seg[l];
                             for (int q = 0; q < kGroups / 2; ++q) {
