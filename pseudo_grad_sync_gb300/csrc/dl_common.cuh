@@ -260,6 +260,43 @@ __device__ __forceinline__ int tensor_containing(const int64_t* __restrict__ off
     return lo;
 }
 
+// First tensor at or after lo whose end lies past pos (lo <= T - 1): a binary
+// search, kept out of line (it runs once per tensor boundary).
+static __device__ __noinline__ int tensor_from(const int64_t* __restrict__ off, int lo, int T, int64_t pos) {
+    int hi = T - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(off + mid + 1) > pos)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// Bounds [o0, o1) of tensor t held in registers while a block walks forward
+// through the fragment: a tile inside the tensor of the previous tile loads no
+// offsets, whose load latency would otherwise sit on every tile's critical
+// path.
+struct TensorCursor {
+    int t = -1;
+    int64_t o0 = 0, o1 = 0;
+    __device__ __forceinline__ void load(const int64_t* __restrict__ off, int tt) {
+        if (tt != t) {
+            o0 = __ldg(off + tt);
+            o1 = __ldg(off + tt + 1);
+            t = tt;
+        }
+    }
+    // The tensor holding pos (< off[T]), for a pos at or past the start of
+    // the cursor's tensor: the current one while pos is inside it, else the
+    // first later tensor that holds it; the result is loaded into the cursor.
+    __device__ __forceinline__ int seek(const int64_t* __restrict__ off, int T, int64_t pos) {
+        if (t < 0 || pos >= o1) load(off, tensor_from(off, t < 0 ? 0 : min(t + 1, T - 1), T, pos));
+        return t;
+    }
+};
+
 // ---------------------------------------------------------------------------
 // float-float (unevaluated sum hi + lo) accumulation, fp32 operations only.
 __device__ __forceinline__ void ff_add(float& hi, float& lo, float b) {

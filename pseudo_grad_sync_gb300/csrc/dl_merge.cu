@@ -227,10 +227,10 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
 
     int cur_t = -1;
     uint32_t it = 0;
+    TensorCursor tc;
     for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
         const int64_t base = c * kChunk;
         const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        int t0 = tensor_containing(a.off, a.T, base);
         for (int o = 0; o < cn; o += TILE, ++it) {
             const int s = static_cast<int>(it % STAGES);
             const int64_t tb = base + o;
@@ -242,13 +242,13 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
             const float* sg = reinterpret_cast<const float*>(st);
             const float* sm = reinterpret_cast<const float*>(st + TILE * 4);
             const unsigned char* sc = st + TILE * 8;
-            for (int t = t0; t < a.T; ++t) {
-                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-                if (o0 >= tend) break;
+            // the tensors of the tile, from the one holding its first element
+            for (int t = tc.seek(a.off, a.T, tb); t < a.T; ++t) {
+                tc.load(a.off, t);
+                const int64_t o0 = tc.o0, o1 = tc.o1;
                 const int64_t pa = o0 > tb ? o0 : tb;
                 const int64_t pe = o1 < tend ? o1 : tend;
-                if (pe <= tb) t0 = t + 1;
-                if (pa >= pe) continue;
+                if (pa >= pe) continue;  // empty tensor
                 if (t != cur_t) {  // consumer-uniform
                     consumer_sync();
                     for (int i = tid; i < np * kNB; i += kThreads) {
@@ -260,7 +260,10 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
                     consumer_sync();
                     cur_t = t;
                 }
-                if (!ok) continue;  // aborted: the stage is not read
+                if (!ok) {  // aborted: the stage is not read
+                    if (o1 >= tend) break;
+                    continue;
+                }
                 if (pa == tb && pe == tb + TILE) {
 #pragma unroll
                     for (int q = 0; q < TILE / 4 / kThreads; ++q) {
@@ -312,6 +315,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_merge_tma(MergeArgs a) {
                         if (a.dbar) a.dbar[e] = acc;
                     }
                 }
+                if (o1 >= tend) break;  // the next tensor starts at or after the tile's end
             }
             consumer_release<STAGES>(&pb, it, ok);
         }

@@ -290,11 +290,11 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
     }
 
     int cur_t = -1;
+    TensorCursor tc;
     uint32_t it = 0;
     for (int64_t c = c0; c < c1; ++c) {
         const int64_t base = c * kChunk;
         const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        int t0 = tensor_containing(a.off, a.T, base);
         for (int o = 0; o < cn; o += kRTile, ++it) {
             const int s = static_cast<int>(it % kRStages);
             const int64_t tb = base + o;
@@ -307,20 +307,23 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
             const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
             const float* sm = reinterpret_cast<const float*>(st + kRTile * 8);
             const unsigned char* sc = st + kRTile * 12;
-            for (int t = t0; t < a.T; ++t) {
-                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-                if (o0 >= tend) break;
+            // the tensors of the tile, from the one holding its first element
+            for (int t = tc.seek(a.off, a.T, tb); t < a.T; ++t) {
+                tc.load(a.off, t);
+                const int64_t o0 = tc.o0, o1 = tc.o1;
                 const int64_t pa = o0 > tb ? o0 : tb;
                 const int64_t pe = o1 < tend ? o1 : tend;
-                if (pe <= tb) t0 = t + 1;
-                if (pa >= pe) continue;
+                if (pa >= pe) continue;  // empty tensor
                 if (t != cur_t) {  // consumer-uniform
                     consumer_sync();
                     scb[tid] = __ldg(a.cb + static_cast<int64_t>(t) * kNB + tid);
                     consumer_sync();
                     cur_t = t;
                 }
-                if (!ok) continue;  // aborted: the stage is not read
+                if (!ok) {  // aborted: the stage is not read
+                    if (o1 >= tend) break;
+                    continue;
+                }
                 if (pa == tb && pe == tb + kRTile) {
 #pragma unroll
                     for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_last_tma(RingArgs a) {
                         if (a.dbar) a.dbar[e] = v;
                     }
                 }
+                if (o1 >= tend) break;  // the next tensor starts at or after the tile's end
             }
             consumer_release<kRStages>(&pb, it, ok);
         }
@@ -427,6 +431,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
     }
 
     int cur_t = -1;
+    TensorCursor tc;
     float csh = 0.f;
     bool small = false;
     Acc acc;
@@ -435,7 +440,6 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
     for (int64_t c = c0; c < c1; ++c) {
         const int64_t base = c * kChunk;
         const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-        int t0 = tensor_containing(a.off, a.T, base);
         for (int o = 0; o < cn; o += kRTile, ++it) {
             const int s = static_cast<int>(it % kRStages);
             const int64_t tb = base + o;
@@ -447,13 +451,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
             const float* sg = reinterpret_cast<const float*>(st);
             const float* sr = reinterpret_cast<const float*>(st + kRTile * 4);
             const unsigned char* sc = st + kRTile * 8;
-            for (int t = t0; t < a.T; ++t) {
-                const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-                if (o0 >= tend) break;
+            // the tensors of the tile, from the one holding its first element
+            for (int t = tc.seek(a.off, a.T, tb); t < a.T; ++t) {
+                tc.load(a.off, t);
+                const int64_t o0 = tc.o0, o1 = tc.o1;
                 const int64_t pa = o0 > tb ? o0 : tb;
                 const int64_t pe = o1 < tend ? o1 : tend;
-                if (pe <= tb) t0 = t + 1;
-                if (pa >= pe) continue;
+                if (pa >= pe) continue;  // empty tensor
                 if (t != cur_t) {  // consumer-uniform
                     if (cur_t >= 0)
                         flush_partial(acc, a.part + static_cast<int64_t>(cur_t) * gridDim.x + blockIdx.x,
@@ -473,7 +477,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                     small = (o1 - o0) < kSmallTensor;
                     cur_t = t;
                 }
-                if (!ok) continue;  // aborted: the stage is not read
+                if (!ok) {  // aborted: the stage is not read
+                    if (o1 >= tend) break;
+                    continue;
+                }
                 if (pa == tb && pe == tb + kRTile) {
 #pragma unroll
                     for (int q = 0; q < kRTile / 4 / kThreads; ++q) {
@@ -517,6 +524,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) k_ring_mid_tma(RingArgs a) {
                     }
                     renorm(acc.s2h, acc.s2l);
                 }
+                if (o1 >= tend) break;  // the next tensor starts at or after the tile's end
             }
             consumer_release<kRStages>(&pb, it, ok);
         }

@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
         }
     };
 
+    TensorCursor cur;
     uint32_t it = 0;
     for (int r = r_lo; r < r_hi; ++r) {
         // slot (k, t, r) of this run's sums sits at part_k + t * J
@@ -264,7 +265,6 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
         for (int64_t c = c_lo; c < c_hi; ++c) {
             const int64_t base = c * kChunk;
             const int cn = static_cast<int>(min(static_cast<int64_t>(kChunk), a.n - base));
-            int t0 = tensor_containing(a.off, a.T, base);  // first tensor of the chunk
             for (int o = 0; o < cn; o += kTile, ++it) {
                 const int s = static_cast<int>(it % kStages);
                 const int64_t tb = base + o;
@@ -274,13 +274,13 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                 const bool ok = consumer_wait<kStages>(&pb, it, a.status);
                 const float* tg = sg + s * kTile;
                 const float* tr = sr + s * kTile;
-                for (int t = t0; t < a.T; ++t) {
-                    const int64_t o0 = __ldg(a.off + t), o1 = __ldg(a.off + t + 1);
-                    if (o0 >= tend) break;
+                // the tensors of the tile, from the one holding its first element
+                for (int t = cur.seek(a.off, a.T, tb); t < a.T; ++t) {
+                    cur.load(a.off, t);
+                    const int64_t o0 = cur.o0, o1 = cur.o1;
                     const int64_t pa = o0 > tb ? o0 : tb;
                     const int64_t pe = o1 < tend ? o1 : tend;
-                    if (pe <= tb) t0 = t + 1;  // ends before this tile: skip it from now on
-                    if (pa >= pe) continue;
+                    if (pa >= pe) continue;  // empty tensor
                     if (t != cur_t) {
                         if (cur_t >= 0) flush_and_count(acc, part_k + cur_t * a.J, cur_t);
                         // the shift of (k, t), from the tensor's first values:
@@ -308,7 +308,10 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                         small = (o1 - o0) < kSmallTensor;
                         acc.reset();
                     }
-                    if (!ok) continue;  // aborted: the stage is not read
+                    if (!ok) {  // aborted: the stage is not read
+                        if (o1 >= tend) break;
+                        continue;
+                    }
                     if (pa == tb && pe == tb + kTile && !small) {
                         add_tile<VALUES>(acc, tg, tr, tid, csh);
                     } else {
@@ -331,6 +334,7 @@ __global__ void __launch_bounds__(kPipeThreads, MINB) k_stats(StatsArgs a) {
                         }
                         renorm(acc.s2h, acc.s2l);
                     }
+                    if (o1 >= tend) break;  // the next tensor starts at or after the tile's end
                 }
                 consumer_release<kStages>(&pb, it, ok);
             }
