@@ -52,6 +52,18 @@ struct SegRt {  // quantiser parameters of one (k, t) segment
 constexpr int kQMaxL = 8;                                        // learners per block at most
 constexpr int kQMaxG = (DL_MAX_LEARNERS + kQMaxL - 1) / kQMaxL;  // learner groups at most
 
+// One-learner blocks (K = 1: the learner-side quantiser, values mode) spread
+// the learner's histogram over kOneCopies copies, copy = lane mod kOneCopies,
+// laid out [bin][copy]: lane i's word for bin b sits in bank
+// 8 (b mod 4) + i mod 8, so only the four lanes of one class can meet in a
+// bank (for Gaussian codes about 2.8 instead of 3.5 passes per warp-wide
+// atomic). A copy then takes at most 32 threads x 32 values = 1024 values per
+// piece, so its words stay exact over kOneFoldEvery pieces between folds.
+// Blocks serving several learners keep one copy per learner: the copies'
+// shared memory would crowd out the L1 space their loads need.
+constexpr int kOneCopies = 8;
+constexpr int kOneFoldEvery = 8;
+
 struct QuantArgs {
     const float* g;
     const float* r[DL_MAX_LEARNERS];
@@ -118,10 +130,41 @@ __device__ __forceinline__ SegRt seg_params(const dl_stats& st) {
 }
 
 // word A of bin b gets one count plus q >> 19, word B gets the low 19 bits
-// of q (those of qb, as 0x4B000000 has none)
+// of q (those of qb, as 0x4B000000 has none); with R copies the lane's copy
+// of each word
+template <int R>
 __device__ __forceinline__ void hist_add(uint32_t* __restrict__ hA, int b, uint32_t qb) {
-    atomicAdd(hA + b, (qb >> 19) + (kCountOne - (kQBits >> 19)));
-    atomicAdd(hA + kNB + b, qb & kLoMask);
+    const int i = R == 1 ? b : b * R + static_cast<int>(threadIdx.x & (R - 1));
+    atomicAdd(hA + i, (qb >> 19) + (kCountOne - (kQBits >> 19)));
+    atomicAdd(hA + R * kNB + i, qb & kLoMask);
+}
+
+// Folds the R copies of bin b (words A at h[R b ..], words B R * kNB further)
+// into the 64-bit sums l2l[b] (count) and l2l[kNB + b] (biased residual sum)
+// and zeroes them. The 16-byte reads are staggered by b so that a warp's
+// reads spread over all banks.
+template <int R>
+__device__ __forceinline__ void fold_copies(uint32_t* __restrict__ h, unsigned long long* __restrict__ l2l,
+                                            int b) {
+    constexpr int kVec = R / 4;  // 16-byte vectors per bin and word
+    static_assert(kVec == 1 || kVec == 2 || kVec == 4 || kVec == 8, "R in {4, 8, 16, 32}");
+    constexpr int kShift = kVec == 1 ? 3 : (kVec == 2 ? 2 : (kVec == 4 ? 1 : 0));
+    uint4* pa = reinterpret_cast<uint4*>(h + b * R);
+    uint4* pb = reinterpret_cast<uint4*>(h + R * kNB + b * R);
+    unsigned long long cnt = 0, hi = 0, lo = 0;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        const int jj = (j + (b >> kShift)) & (kVec - 1);
+        const uint4 va = pa[jj], vb = pb[jj];
+        cnt += (va.x >> 18) + (va.y >> 18) + (va.z >> 18) + (va.w >> 18);
+        hi += (va.x & (kCountOne - 1)) + (va.y & (kCountOne - 1)) + (va.z & (kCountOne - 1)) +
+              (va.w & (kCountOne - 1));
+        lo += static_cast<unsigned long long>(vb.x) + vb.y + vb.z + vb.w;
+        pa[jj] = make_uint4(0u, 0u, 0u, 0u);
+        pb[jj] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    l2l[b] += cnt;
+    l2l[kNB + b] += (hi << 19) + lo;
 }
 
 // four codes as one 32-bit word, b0 in the lowest byte
@@ -130,6 +173,7 @@ __device__ __forceinline__ uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2,
 }
 
 // bucket of one value and its histogram update; returns the code
+template <int R>
 __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_t* __restrict__ hA) {
     const float uf = __fmaf_rn(d, p.q.s_f, p.q.c_f);
     // floor(uf) for |uf| < 2^22: adding 1.5 * 2^23 rounding down lands on the
@@ -155,16 +199,17 @@ __device__ __forceinline__ uint32_t encode_fast(float d, const SegRt& p, uint32_
         rare_code(d, p.q, b, qv);
         qb = kQBits + qv;
     }
-    hist_add(hA, b, qb);
+    hist_add<R>(hA, b, qb);
     return static_cast<uint32_t>(b);
 }
 
+template <int R>
 __device__ __forceinline__ uint32_t encode_one(float d, const SegRt& p, uint32_t* __restrict__ hA) {
-    if (p.q.kind == kSegFast) return encode_fast(d, p, hA);
+    if (p.q.kind == kSegFast) return encode_fast<R>(d, p, hA);
     int b;
     uint32_t qv;
     rare_code(d, p.q, b, qv);
-    hist_add(hA, b, kQBits + qv);
+    hist_add<R>(hA, b, kQBits + qv);
     return static_cast<uint32_t>(b);
 }
 
@@ -207,6 +252,7 @@ __device__ __forceinline__ FastParams fast_params(const SegRt& p) {
 
 // bucket of one value of a fast-kind segment and its histogram update (the
 // same arithmetic as encode_fast; the fp64 rule from the full parameters)
+template <int R>
 __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, const SegRt* full,
                                               uint32_t* __restrict__ hA) {
     const float uf = __fmaf_rn(d, f.s_f, f.c_f);
@@ -229,7 +275,7 @@ __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, cons
         rare_code(d, full->q, b, qv);
         qb = kQBits + qv;
     }
-    hist_add(hA, b, qb);
+    hist_add<R>(hA, b, qb);
     return static_cast<uint32_t>(b);
 }
 
@@ -239,6 +285,7 @@ __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, cons
 // warp runs that branch's arithmetic straight through, with the four
 // histogram updates back to back; otherwise each value goes through
 // encode_fp. Both routes give the same codes and sums.
+template <int R>
 __device__ __forceinline__ uint32_t encode4_fp(float4 gq, float4 rq, const FastParams& f,
                                                const SegRt* full, uint32_t* __restrict__ hA) {
     const float d[4] = {__fsub_rn(gq.x, rq.x), __fsub_rn(gq.y, rq.y), __fsub_rn(gq.z, rq.z),
@@ -259,25 +306,31 @@ __device__ __forceinline__ uint32_t encode4_fp(float4 gq, float4 rq, const FastP
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float r = __fsub_rn(d[e], __fmaf_rn(bf[e], f.w_f, f.lo_f));
-            hist_add(hA, b[e], __float_as_uint(__fmaf_rn(r, f.scale, f.qoff)));
+            hist_add<R>(hA, b[e], __float_as_uint(__fmaf_rn(r, f.scale, f.qoff)));
         }
         return pack4(b[0], b[1], b[2], b[3]);
     }
-    const uint32_t c0 = encode_fp(d[0], f, full, hA);
-    const uint32_t c1 = encode_fp(d[1], f, full, hA);
-    const uint32_t c2 = encode_fp(d[2], f, full, hA);
-    const uint32_t c3 = encode_fp(d[3], f, full, hA);
+    const uint32_t c0 = encode_fp<R>(d[0], f, full, hA);
+    const uint32_t c1 = encode_fp<R>(d[1], f, full, hA);
+    const uint32_t c2 = encode_fp<R>(d[2], f, full, hA);
+    const uint32_t c3 = encode_fp<R>(d[3], f, full, hA);
     return pack4(c0, c1, c2, c3);
 }
 
 constexpr int kBatchesPerBlock = 32;  // chunk batches a block takes, about
 constexpr int kMaxBatch = 16;         // chunks per batch at most
 
-// Dynamic shared memory of a quantiser block serving L learners: the
-// double-buffered 32-bit histograms [2][L][word A bins | word B bins] and the
+// 32-bit histogram words of a quantiser block: serving L learners, the
+// double-buffered [2][L][word A bins | word B bins]; serving one learner
+// alone, [word A bins x copies | word B bins x copies].
+__host__ __device__ constexpr size_t quant_hist_words(int L, bool one) {
+    return one ? static_cast<size_t>(2) * kOneCopies * kNB : static_cast<size_t>(L) * 2 * 2 * kNB;
+}
+
+// Dynamic shared memory of a quantiser block: the histogram words and the
 // 64-bit per-bin sums [L][count bins | residual-sum bins].
-__host__ __device__ constexpr size_t quant_smem(int L) {
-    return static_cast<size_t>(L) * (2 * 2 * kNB * 4 + 2 * kNB * 8);
+__host__ __device__ constexpr size_t quant_smem(int L, bool one) {
+    return quant_hist_words(L, one) * 4 + static_cast<size_t>(L) * 2 * kNB * 8;
 }
 
 // Learner-group grid: the K learners form G near-equal groups of at most
@@ -291,8 +344,10 @@ __host__ __device__ constexpr size_t quant_smem(int L) {
 // values: theta_g is read once per group, not once per learner, and each
 // piece's block barrier and histogram fold serve L learners.
 // VALUES: values mode (no replica; Delta is theta_g itself, K = 1). ONE: one
-// learner per block (K = 1): its parameters stay in registers and each block
-// takes one static contiguous run of chunks.
+// learner per block (K = 1): its parameters stay in registers, each block
+// takes one static contiguous run of chunks, and its histogram has
+// kOneCopies copies, folded every kOneFoldEvery pieces and when the block
+// moves to another tensor.
 template <bool VALUES, bool ONE>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     extern __shared__ __align__(16) unsigned char qsm[];
@@ -303,18 +358,21 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
     while (grp + 1 < a.G && static_cast<int>(blockIdx.x) >= a.gb0[grp + 1]) ++grp;
     const int k0 = a.gk0[grp];
     const int L = ONE ? 1 : a.gk0[grp + 1] - k0;
+    constexpr int R = ONE ? kOneCopies : 1;  // histogram copies per learner
+    const int hist_words = static_cast<int>(quant_hist_words(L, ONE));
     uint32_t* l1 = reinterpret_cast<uint32_t*>(qsm);
-    unsigned long long* l2 = reinterpret_cast<unsigned long long*>(qsm + static_cast<size_t>(L) * 2 * 2 * kNB * 4);
+    unsigned long long* l2 = reinterpret_cast<unsigned long long*>(qsm + static_cast<size_t>(hist_words) * 4);
 
     const int tid = threadIdx.x;
     const float* __restrict__ g = a.g;
-    for (int i = tid; i < L * 2 * 2 * kNB; i += kThreads) l1[i] = 0u;
+    for (int i = tid; i < hist_words; i += kThreads) l1[i] = 0u;
     for (int i = tid; i < L * 2 * kNB; i += kThreads) l2[i] = 0ull;
     __syncthreads();
 
     int cur_t = -1;  // tensor whose sums are in l2
     int seg_t = -1;  // tensor whose parameters are in s_seg
-    int par = 0;
+    int par = 0;     // learner groups: the histogram buffer of this piece
+    int since = 0;   // one learner: pieces since the copies were folded
     FastParams f_one;  // ONE: the learner's parameters for the current tensor
     // Learner groups: thread 0 fetches the next batch while the block works on
     // the current one. One learner per block (no group to share theta_g with):
@@ -354,8 +412,20 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                 if (ONE) f_one = s_fp[0];
                 seg_t = t;
             }
+            if constexpr (ONE) {
+                if (t != cur_t || since == kOneFoldEvery) {  // block-uniform
+                    __syncthreads();  // every update so far is in the copies
+                    if (cur_t >= 0) {
+                        fold_copies<R>(l1, l2, tid);
+                        if (t != cur_t) flush_bin(a, k0, cur_t, tid, l2);
+                    }
+                    cur_t = t;
+                    since = 0;
+                    __syncthreads();  // the copies are zero again
+                }
+            }
             const bool full = (pa == base) && (pb == base + kChunk);
-            uint32_t* hpar = l1 + static_cast<size_t>(par) * L * 2 * kNB;
+            uint32_t* hpar = ONE ? l1 : l1 + static_cast<size_t>(par) * L * 2 * kNB;
             if (full) {
                 const float4* g4 = reinterpret_cast<const float4*>(g + base);
 #pragma unroll 1
@@ -372,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                             for (int q = 0; q < kGroups / 2; ++q) c4[tid + (h + q) * kThreads] = 0u;
                             continue;
                         }
-                        uint32_t* hA = hpar + l * 2 * kNB;
+                        uint32_t* hA = hpar + l * 2 * R * kNB;
                         const float4* r4 = reinterpret_cast<const float4*>(a.r[k0 + l] + base);
                         float4 rv[kGroups / 2];
 #pragma unroll
@@ -382,14 +452,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                         if (f.kind == kSegFast) {
 #pragma unroll
                             for (int q = 0; q < kGroups / 2; ++q)
-                                c4[tid + (h + q) * kThreads] = encode4_fp(gv[q], rv[q], f, s_seg + l, hA);
+                                c4[tid + (h + q) * kThreads] = encode4_fp<R>(gv[q], rv[q], f, s_seg + l, hA);
                         } else {
                             const SegRt p = s_seg[l];
+#pragma unroll
                             for (int q = 0; q < kGroups / 2; ++q) {
-                                const uint32_t b0 = encode_one(__fsub_rn(gv[q].x, rv[q].x), p, hA);
-                                const uint32_t b1 = encode_one(__fsub_rn(gv[q].y, rv[q].y), p, hA);
-                                const uint32_t b2 = encode_one(__fsub_rn(gv[q].z, rv[q].z), p, hA);
-                                const uint32_t b3 = encode_one(__fsub_rn(gv[q].w, rv[q].w), p, hA);
+                                const uint32_t b0 = encode_one<R>(__fsub_rn(gv[q].x, rv[q].x), p, hA);
+                                const uint32_t b1 = encode_one<R>(__fsub_rn(gv[q].y, rv[q].y), p, hA);
+                                const uint32_t b2 = encode_one<R>(__fsub_rn(gv[q].z, rv[q].z), p, hA);
+                                const uint32_t b3 = encode_one<R>(__fsub_rn(gv[q].w, rv[q].w), p, hA);
                                 c4[tid + (h + q) * kThreads] = pack4(b0, b1, b2, b3);
                             }
                         }
@@ -404,12 +475,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
                         continue;
                     }
                     const float* __restrict__ rk = a.r[k0 + l];
-                    uint32_t* hA = hpar + l * 2 * kNB;
+                    uint32_t* hA = hpar + l * 2 * R * kNB;
                     for (int64_t e = pa + tid; e < pb; e += kThreads) {
                         const float d = __fsub_rn(__ldg(g + e), VALUES ? 0.f : __ldcs(rk + e));
-                        ck[e] = static_cast<uint8_t>(encode_one(d, p, hA));
+                        ck[e] = static_cast<uint8_t>(encode_one<R>(d, p, hA));
                     }
                 }
+            }
+            if constexpr (ONE) {
+                ++since;
+                continue;
             }
             __syncthreads();  // every update of this piece is in l1[par]
             if (cur_t != t) {
@@ -431,6 +506,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
             par ^= 1;
         }
     }
+    }
+    if constexpr (ONE) {
+        __syncthreads();  // every update is in the copies
+        if (cur_t >= 0) fold_copies<R>(l1, l2, tid);
     }
     if (cur_t >= 0)
         for (int l = 0; l < L; ++l) flush_bin(a, k0 + l, cur_t, tid, l2 + l * 2 * kNB);
@@ -552,9 +631,11 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
                            : K == 1 ? reinterpret_cast<const void*>(k_quantize<false, true>)
                                     : reinterpret_cast<const void*>(k_quantize<false, false>);
         const int Lmax = (K + (K + kQMaxL - 1) / kQMaxL - 1) / ((K + kQMaxL - 1) / kQMaxL);
-        const size_t smem = quant_smem(Lmax);
+        const size_t smem = quant_smem(Lmax, K == 1);
+        // the instance's largest need, whatever K this call has
+        const size_t smem_max = K == 1 ? quant_smem(1, true) : quant_smem(kQMaxL, false);
         if ((st = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(quant_smem(kQMaxL))))) != DL_OK)
+                                                   static_cast<int>(smem_max)))) != DL_OK)
             return st;
         plan_groups(a, K, grid_for(kern, kThreads, smem, a.n_chunks * ((K + kQMaxL - 1) / kQMaxL)));
         const int grid = a.gb0[a.G];
