@@ -1,11 +1,13 @@
 // Uniform quantisation with clipping and a bucket-mean codebook (INTELLECT-1
 // notes, section 4.1 steps 2-4), fused with the uint8 encode.
 //
-// k_quantize   learner-major persistent grid: block b serves learner k = b % K
-//              and the j-th of J contiguous runs of 8192-element chunks
-//              (j = b / K), so the K blocks reading one chunk of theta_g run
-//              together (theta_g crosses HBM once, then comes from L2) and a
-//              block meets few tensors; thread 0 derives a tensor's
+// k_quantize   learner-group grid: the K learners form near-equal groups of at
+//              most 7; a block serves one group and takes batches of
+//              contiguous 8192-element chunks from its group's counter, so
+//              the blocks of all groups sweep the fragment together
+//              (theta_g crosses HBM once, then comes from L2) and each
+//              theta_g value a block loads serves every learner of its group;
+//              thread 0 derives a tensor's
 //              quantiser parameters from its statistics when the block
 //              enters it (no separate launch); each chunk is loaded in two
 //              halves with 128-bit loads. Per element of learner k:
@@ -32,8 +34,11 @@
 //              After each piece (chunk x tensor; one block barrier) thread b
 //              folds bin b of the histogram into 64-bit per-bin sums it owns
 //              (the histograms are double-buffered, so one barrier suffices);
-//              those go to a [K][T][256] (count, residual-sum) table with
-//              integer atomics when the block moves to another tensor.
+//              a block serving one learner alone keeps 8 copies of its
+//              histogram (fewer bank conflicts) and folds them every 8
+//              pieces. The sums go to a [K][T][256] (count, residual-sum)
+//              table with integer atomics when the block moves to another
+//              tensor.
 //              Integer sums make the result independent of addition order.
 // k_cb_fin     one thread per (k, t, b): codebook value = reference + mean
 //              residual (fp64, rounded once to fp32), midpoint for an empty
@@ -49,7 +54,12 @@ struct SegRt {  // quantiser parameters of one (k, t) segment
     uint32_t qb_lo, qb_hi;  // histogram words of an element clipped to lo / hi
 };
 
-constexpr int kQMaxL = 8;                                        // learners per block at most
+// Learners per block at most: 7 learners' histograms (8 KB each) with the
+// static and reserved shared memory keep three blocks within a 196 KB
+// shared-memory carveout, which leaves about 60 KB of L1 for the kernel's
+// in-flight 128-bit loads; 8 would need the 228 KB carveout (28 KB of L1),
+// measured 4-5% slower at K = 8 and K = 16.
+constexpr int kQMaxL = 7;
 constexpr int kQMaxG = (DL_MAX_LEARNERS + kQMaxL - 1) / kQMaxL;  // learner groups at most
 
 // One-learner blocks (K = 1: the learner-side quantiser, values mode) spread
