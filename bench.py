@@ -528,14 +528,18 @@ def run_rda(args, rank, world, local):
 FRAGMENT_WORKLOADS = ("decoder_10b", "quorum_10b", "ragged_heavy")
 
 
-def bench_fragment(wl, plan):
+def bench_fragment(wl, plan, which="median"):
     """Tensors of the fragment a step syncs: for a model cut into P fragments
-    the median one by load (ties broken by fragment index), for a one-batch
-    workload every tensor. Returns (tensors, fragment index)."""
+    the median one by load (ties broken by fragment index), or the largest
+    one (the lowest index among equal loads); for a one-batch workload every
+    tensor. Returns (tensors, fragment index)."""
     if wl.n_frags == 1:
         return list(range(wl.n_tensors)), 0
     frag_of, load = plan(wl.numels, wl.n_frags)
-    f = int(np.argsort(load, kind="stable")[len(load) // 2])
+    if which == "largest":
+        f = int(np.argmax(load))
+    else:
+        f = int(np.argsort(load, kind="stable")[len(load) // 2])
     return [t for t in range(wl.n_tensors) if frag_of[t] == f], f
 
 
@@ -591,35 +595,33 @@ def oracle_fragment_pass(g, reps, off, present, weights):
     return dt
 
 
-def fragment_cpu_sample(wl, ts, host, limit, generate=True):
+def fragment_cpu_sample(wl, ts, limit, generate=True):
     """Host arrays (theta_g, replicas, offsets, elements, tensors) of the
     oracle's bounded sample: the fragment's tensors in order up to `limit`
-    elements (at least one tensor), sliced from the host copy or generated
-    (generate=False: the selection only)."""
-    sel, tot = [], 0
+    elements (at least one tensor; a first tensor longer than `limit` is cut
+    to its first `limit` values), generated on the host (generate=False: the
+    selection only)."""
+    sel, sizes, tot = [], [], 0
     for t in ts:
         if sel and tot + wl.numels[t] > limit:
             continue
         sel.append(t)
-        tot += wl.numels[t]
+        sizes.append(min(wl.numels[t], limit))
+        tot += sizes[-1]
     if not generate:
         return None, None, None, tot, sel
-    off = synthetic.offsets_of([wl.numels[t] for t in sel])
-    if host is not None and sel == ts[:len(sel)]:
-        g = host[0].numpy()[:tot]
-        reps = [host[1].numpy()[k, :tot] for k in range(wl.K)]
-    else:
-        g = np.empty(tot, dtype=np.float32)
-        reps = [np.empty(tot, dtype=np.float32) for _ in range(wl.K)]
-        for i, t in enumerate(sel):
-            a, b = int(off[i]), int(off[i + 1])
-            wl.theta_global(t, out=g[a:b])
-            for k in range(wl.K):
-                wl.replica(k, t, g[a:b], out=reps[k][a:b])
+    off = synthetic.offsets_of(sizes)
+    g = np.empty(tot, dtype=np.float32)
+    reps = [np.empty(tot, dtype=np.float32) for _ in range(wl.K)]
+    for i, t in enumerate(sel):
+        a, b = int(off[i]), int(off[i + 1])
+        wl.theta_global(t, out=g[a:b], n=b - a)
+        for k in range(wl.K):
+            wl.replica(k, t, g[a:b], out=reps[k][a:b])
     return g, reps, off, tot, sel
 
 
-def fragment_cpu_baseline(wl, ts, host, budget_s):
+def fragment_cpu_baseline(wl, ts, budget_s):
     """The oracle on the host cores over (a bounded sample of) the bench
     fragment, with step 0's quorum; the single-thread figure on its first
     tensor beside it."""
@@ -627,16 +629,17 @@ def fragment_cpu_baseline(wl, ts, host, budget_s):
 
     oracle.lib()
     present, weights = quorum_schedule(wl, 0)
-    g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, host, 1 << 26)
+    g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, 1 << 26)
     total, passes = 0.0, 0
     while passes == 0 or total < budget_s:
         total += oracle_fragment_pass(g, reps, off, present, weights)
         passes += 1
     cores = oracle.threads()
     # one thread on one tensor of the sample: the smallest with >= 2^20 elements
-    big = [i for i, t in enumerate(sel) if wl.numels[t] >= 1 << 20]
-    i1 = min(big, key=lambda i: wl.numels[sel[i]]) if big else 0
-    a1, n1 = int(off[i1]), wl.numels[sel[i1]]
+    size = [int(off[i + 1] - off[i]) for i in range(len(sel))]
+    big = [i for i in range(len(sel)) if size[i] >= 1 << 20]
+    i1 = min(big, key=lambda i: size[i]) if big else 0
+    a1, n1 = int(off[i1]), size[i1]
     oracle.set_threads(1)
     try:
         t1 = oracle_fragment_pass(g[a1:a1 + n1], [r[a1:a1 + n1] for r in reps],
@@ -644,7 +647,12 @@ def fragment_cpu_baseline(wl, ts, host, budget_s):
     finally:
         oracle.set_threads(cores)
     np_ = int(np.count_nonzero(present))
-    whole = "the whole fragment" if len(sel) == len(ts) else f"{len(sel)} of its {len(ts)} tensors"
+    if tot < sum(wl.numels[t] for t in sel):
+        whole = f"the first {tot} values of its {len(ts)}-tensor fragment"
+    elif len(sel) == len(ts):
+        whole = "the whole fragment"
+    else:
+        whole = f"{len(sel)} of its {len(ts)} tensors"
     return {"value": tot * passes / total, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{whole} ({tot} elements x {np_} present learners), full outer step "
                       f"(stats+quantise+merge+Nesterov), {passes} pass(es) in {total:.1f} s",
@@ -777,11 +785,11 @@ def run_fragment(args, rank, world, local):
     torch.cuda.set_device(local)
     wl = synthetic.WORKLOADS[args.workload]()
     K = wl.K
-    ts, fid = bench_fragment(wl, dl.plan_fragments)
+    ts, fid = bench_fragment(wl, dl.plan_fragments, args.fragment)
     if args.sample_elems:
         # a smaller case of the same kernels (profiling): the fragment's
         # tensors in order up to that many elements
-        ts = fragment_cpu_sample(wl, ts, None, args.sample_elems, generate=False)[4]
+        ts = fragment_cpu_sample(wl, ts, args.sample_elems, generate=False)[4]
     numels = [wl.numels[t] for t in ts]
     F = dl.Fragment(numels, dev)
     n = F.n
@@ -900,10 +908,10 @@ def run_fragment(args, rank, world, local):
     elif e2e_error is not None:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                "error": e2e_error}
-    desc = {"decoder_10b": "10B decoder set cut into P=24 by the LPT planner; the median "
+    desc = {"decoder_10b": f"10B decoder set cut into P=24 by the LPT planner; the {args.fragment} "
                            f"fragment (#{fid}, {len(ts)} tensors) synced per step with K={K} "
                            "replicas resident, momentum carried across steps",
-            "quorum_10b": "10B shapes, the median fragment "
+            "quorum_10b": f"10B shapes, the {args.fragment} fragment "
                           f"(#{fid}, {len(ts)} tensors), K={K} learners with a random present "
                           "subset of 1..16 and weights U[0.5,1.5] per step (the workload's "
                           "(fragment, outer step) draws in turn), momentum carried",
@@ -929,7 +937,7 @@ def run_fragment(args, rank, world, local):
         "e2e": e2e, "setup_generate_s": gen_s,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = fragment_cpu_baseline(wl, ts, None, args.cpu_budget)
+        out["cpu_baseline"] = fragment_cpu_baseline(wl, ts, args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -1195,14 +1203,16 @@ def run_reference(args, rank, world):
     wl = synthetic.WORKLOADS[args.workload]()
     oracle.lib()
     if wl.name in FRAGMENT_WORKLOADS:
-        ts, fid = bench_fragment(wl, oracle.plan_fragments)
-        g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, None, 1 << 25)
+        ts, fid = bench_fragment(wl, oracle.plan_fragments, args.fragment)
+        g, reps, off, tot, sel = fragment_cpu_sample(wl, ts, 1 << 25)
         for s in range(args.warmup):
             oracle_fragment_pass(g, reps, off, *quorum_schedule(wl, s))
         dt = sum(oracle_fragment_pass(g, reps, off, *quorum_schedule(wl, s))
                  for s in range(args.steps))
         n_step = tot
-        sample = (f"each step: {len(sel)} of the {len(ts)} tensors of the bench fragment "
+        part = (f"{len(sel)} of the {len(ts)} tensors" if tot == sum(wl.numels[t] for t in sel)
+                else f"the first {tot} values of the {len(ts)}-tensor")
+        sample = (f"each step: {part} bench fragment "
                   f"({tot} elements), full outer step with that step's present learners")
         config = {"workload": wl.name, "K": wl.K, "fragment_elems": sum(wl.numels[t] for t in ts),
                   "fragment_tensors": len(ts)}
@@ -1245,6 +1255,9 @@ def main():
     ap.add_argument("--sample-elems", type=int, default=0,
                     help="fragment workloads: sync only the bench fragment's tensors in "
                          "order up to this many elements (a small case for profiling)")
+    ap.add_argument("--fragment", choices=["median", "largest"], default="median",
+                    help="decoder_10b, quorum_10b: the fragment a step syncs (the median "
+                         "one by load, or the largest: the embedding's)")
     ap.add_argument("--mode", choices=["outer", "ring", "rda"], default="outer",
                     help="ring: accumulate along a ring, re-quantising at every hop; "
                          "rda: Radial-Directional Averaging merge")

@@ -175,10 +175,11 @@ class Workload:
             self._sigmas = [float(math.exp(lo + (hi - lo) * x)) for x in u]
         return self._sigmas[t]
 
-    def theta_global(self, t: int, out=None) -> np.ndarray:
-        """Initial global parameters of tensor t."""
-        return normal_f32(key(self.seed, _K_THETA, 0, t, 0), 0, self.numels[t], 0.0,
-                          self.theta_std, out)
+    def theta_global(self, t: int, out=None, n=None) -> np.ndarray:
+        """Initial global parameters of tensor t (its first n values if n is
+        given: the generator is counter-based, so a prefix is the same values)."""
+        return normal_f32(key(self.seed, _K_THETA, 0, t, 0), 0,
+                          self.numels[t] if n is None else n, 0.0, self.theta_std, out)
 
     def replica(self, k: int, t: int, base: np.ndarray, step: int = 0, out=None):
         """Learner k's copy of tensor t after its inner steps: base - scale * X."""

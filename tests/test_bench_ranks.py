@@ -57,3 +57,28 @@ def test_single_rank_needs_no_process_group(monkeypatch):
         monkeypatch.delenv(k, raising=False)
     assert bench.env_rank() == (0, 1, 0)
     assert bench.max_over_ranks(3.25, 1, "cpu") == 3.25
+
+
+def test_bench_fragments_and_oracle_sample():
+    """The bench syncs the 10B set's median fragment (18 tensors, 415M
+    elements) or its largest (the embedding alone, 525M); the oracle's
+    bounded sample of the largest is the first values of that one tensor,
+    the same values as the head of the whole tensor."""
+    import numpy as np
+
+    import bench
+    import oracle
+    import synthetic
+
+    oracle.lib()
+    wl = synthetic.WORKLOADS["decoder_10b"]()
+    ts, f = bench.bench_fragment(wl, oracle.plan_fragments)
+    assert (len(ts), sum(wl.numels[t] for t in ts)) == (18, 415260672)
+    ts, f = bench.bench_fragment(wl, oracle.plan_fragments, "largest")
+    assert (f, len(ts), wl.numels[ts[0]]) == (0, 1, 525336576)
+    g, reps, off, tot, sel = bench.fragment_cpu_sample(wl, ts, 1 << 16)
+    assert sel == ts and tot == 1 << 16 and list(off) == [0, 1 << 16]
+    small = synthetic.WORKLOADS["decoder_1b"]()
+    t = 5
+    head = small.theta_global(t)[: 1 << 12]
+    assert np.array_equal(small.theta_global(t, n=1 << 12), head)

@@ -167,6 +167,29 @@ def test_small_grids_learner_groups_and_batches(grid, K, monkeypatch):
     compare(g, reps, sizes)
 
 
+@pytest.mark.parametrize("grid,K", [(0, 7), (0, 8), (6, 15), (0, 22)])
+def test_learner_group_boundaries(grid, K, monkeypatch):
+    """The quantiser serves at most 7 learners per block: K = 7, 8, 15 and 22
+    give one to four groups of near-equal size."""
+    if grid:
+        monkeypatch.setenv("DL_GRID_LIMIT", str(grid))
+    sizes = [8192 * 12 + 9, 700, 8192 * 5, 4100]
+    g, reps = _make(sizes, K, seed=70 + K)
+    compare(g, reps, sizes)
+
+
+@pytest.mark.parametrize("grid", [1, 3])
+def test_one_learner_histogram_copies(grid, monkeypatch):
+    """One learner: the quantiser's histogram copies are folded every 8
+    pieces and at tensor changes. Tensors of exactly 8, 9, 16 and 17 chunks
+    (the last one starting mid-chunk) put folds on and just past that
+    boundary; a capped grid gives each block a long run of pieces."""
+    monkeypatch.setenv("DL_GRID_LIMIT", str(grid))
+    sizes = [8192 * 8, 8192 * 9, 8192 * 16 + 7, 8192 * 17, 100]
+    g, reps = _make(sizes, 1, seed=80 + grid)
+    compare(g, reps, sizes)
+
+
 def test_tail_not_multiple_of_four():
     for n in (1, 2, 3, 5, 8191, 8193, 24579):
         g, reps = _make([n], 2, seed=n)
