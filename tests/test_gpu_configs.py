@@ -93,19 +93,32 @@ class FragmentRun:
             reps.append(r)
         return reps
 
-    def step(self, step, present=None, weights=None):
+    def step(self, step, present=None, weights=None, twin=None):
+        """One outer step through the per-call sequence. With `twin` (a
+        ModelSync over this fragment) the same step also runs through
+        dl_outer_sync, the call bench.py times, on copies of theta and m, and
+        both must give the same bits."""
         # the oracle chain's state of the sampled tensors goes into the GPU
         # buffers (a no-op at step 0, where both hold the initial theta and 0)
         for h in self.host.values():
             self.g[h["a"]:h["b"]].copy_(torch.from_numpy(h["g"]))
             self.m[h["a"]:h["b"]].copy_(torch.from_numpy(h["m"]))
         reps = self.replicas(step)
+        if twin is not None:
+            g2, m2, db2 = self.g.clone(), self.m.clone(), torch.empty_like(self.g)
+            twin.step([g2], [m2], [reps], weights=None if weights is None else [weights],
+                      present=None if present is None else [present], delta_bar=[db2])
         db = torch.empty_like(self.g)
         counts = torch.empty((self.K, self.frag.T, 256), dtype=torch.int32, device="cuda")
         idx = self.sync.step(self.g, self.m, reps, weights=weights, present=present, delta_bar=db,
                              counts=counts)
         torch.cuda.synchronize()
         del reps
+        if twin is not None:
+            for a, b in ((g2, self.g), (m2, self.m), (db2, db)):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+            assert self.dl.read_device_status(twin.workspace) == 0
+            del g2, m2, db2
         return idx, db, counts
 
     def check(self, step, idx, db, counts, present=None, weights=None):
@@ -183,7 +196,8 @@ def test_decoder_1b_every_fragment():
 
 def test_decoder_10b_fragment_three_steps():
     """10B set, K=14: the median (~415M-element) fragment over 3 outer steps
-    with momentum carried."""
+    with momentum carried; each step also through dl_outer_sync (bitwise the
+    same)."""
     wl = synthetic.decoder_10b()
     frags, load = _plan(wl)
     f = int(np.argsort(load, kind="stable")[len(load) // 2])  # bench.py's fragment
@@ -191,8 +205,10 @@ def test_decoder_10b_fragment_three_steps():
     sampled = _sampled(wl, ts)
     run = FragmentRun(wl, ts, sampled, gen_seed=3)
     assert 4e8 < run.n < 4.3e8
+    # the same steps through dl_outer_sync, as bench.py runs them: bitwise equal
+    twin = run.dl.ModelSync([run.frag], run.K)
     for step in range(wl.steps):
-        idx, db, counts = run.step(step)
+        idx, db, counts = run.step(step, twin=twin)
         run.check(step, idx, db, counts)
     assert torch.isfinite(run.g).all()
 
