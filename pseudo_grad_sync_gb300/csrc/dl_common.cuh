@@ -32,8 +32,9 @@ constexpr int64_t kSmallTensor = 4096;
 // workspace header: status word and padding
 constexpr size_t kWsHeader = 256;
 
-// learner-major grids: block b serves learner b % K and every (G/K)-th chunk
-// from b / K; at most this many blocks per learner, and in all
+// learner-major grids (statistics, ring hops): block b serves learner b % K
+// and the (b / K)-th run of contiguous chunks; at most this many blocks per
+// learner, and in all
 constexpr int kMaxBlocksPerLearner = 1024;
 constexpr int kMaxBlocksTotal = 2048;
 
