@@ -289,7 +289,6 @@ __device__ __forceinline__ uint32_t encode_fp(float d, const FastParams& f, cons
     return static_cast<uint32_t>(b);
 }
 
-
 // Four values of a fast-kind segment, packed codes returned. When all four
 // values of every lane take encode_fp's first branch (the common case), the
 // warp runs that branch's arithmetic straight through, with the four
