@@ -1210,10 +1210,11 @@ def run_reference(args, rank, world):
         dt = sum(oracle_fragment_pass(g, reps, off, *quorum_schedule(wl, s))
                  for s in range(args.steps))
         n_step = tot
-        part = (f"{len(sel)} of the {len(ts)} tensors" if tot == sum(wl.numels[t] for t in sel)
-                else f"the first {tot} values of the {len(ts)}-tensor")
-        sample = (f"each step: {part} bench fragment "
-                  f"({tot} elements), full outer step with that step's present learners")
+        part = (f"{len(sel)} of the {len(ts)} tensors of the bench fragment"
+                if tot == sum(wl.numels[t] for t in sel)
+                else f"the first {tot} values of the {len(ts)}-tensor bench fragment")
+        sample = (f"each step: {part} ({tot} elements), full outer step with that step's "
+                  "present learners")
         config = {"workload": wl.name, "K": wl.K, "fragment_elems": sum(wl.numels[t] for t in ts),
                   "fragment_tensors": len(ts)}
     else:
