@@ -58,7 +58,10 @@ def _call_noalloc(dl, fn, g, reps, frag, stats):
 @pytest.mark.parametrize("reverse", [False, True])
 def test_noalloc_matches_quantize_on_two_calls(noalloc, reverse):
     dl, fn = noalloc
-    cases = [(1, [9000, 8192 * 3 + 5, 77], 3), (2, [40000, 3, 8192], 5)]
+    # K = 1 takes the one-learner quantiser (histogram copies), the others
+    # learner groups
+    cases = [(1, [9000, 8192 * 3 + 5, 77], 3), (2, [40000, 3, 8192], 5),
+             (3, [8192 * 10 + 17, 500], 1)]
     if reverse:
         cases = cases[::-1]
     for seed, numels, K in cases:
