@@ -661,12 +661,38 @@ def fragment_cpu_baseline(wl, ts, budget_s):
                                         f"one pass in {t1:.1f} s"}}
 
 
+class RegisteredHost:
+    """A page-aligned host array of `nfloats` fp32 values registered with
+    cudaHostRegister: pinned memory the copy engines read directly. `tensor`
+    views it; release() unregisters it."""
+
+    def __init__(self, nfloats):
+        import torch
+
+        nbytes = nfloats * 4
+        self._raw = np.empty(nbytes + 4096, dtype=np.uint8)
+        off = (-self._raw.ctypes.data) % 4096
+        self._arr = self._raw[off:off + nbytes].view(np.float32)
+        self._rt = torch.cuda.cudart()
+        rc = self._rt.cudaHostRegister(self._arr.ctypes.data, nbytes, 0)
+        if int(rc if not isinstance(rc, tuple) else rc[0]) != 0:
+            raise RuntimeError(f"cudaHostRegister of {nbytes / 1e9:.1f} GB failed: {rc}")
+        self.tensor = torch.from_numpy(self._arr)
+
+    def release(self):
+        if self._arr is not None:
+            self._rt.cudaHostUnregister(self._arr.ctypes.data)
+            self._arr = self.tensor = None
+
+
 def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     """The same step through the public API with host buffers: every step
     uploads the present learners' replicas of the fragment from pinned host
-    memory (one copy per learner) on an upload stream into one of two device
-    buffers, runs dl_outer_sync as soon as they have landed, and downloads the
-    updated theta_g on a download stream. Uploads of step s+1 run while step s
+    memory (a page-aligned buffer registered with cudaHostRegister; one copy
+    of the whole block when every learner is present, else one per learner)
+    on an upload stream into one of two device buffers, runs dl_outer_sync as
+    soon as they have landed, and downloads the updated theta_g on a download
+    stream. Uploads of step s+1 run while step s
     computes and downloads; the step after waits for the download before it
     updates theta_g again."""
     import torch
@@ -730,8 +756,8 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     if world > 1:
         dt = max_over_ranks(dt, world, dev)
     # the host link alone, CUDA events: the same replica block copied by
-    # itself from torch's pinned allocator, and one replica copied from a
-    # page-aligned host buffer registered with cudaHostRegister
+    # itself from the staging buffer, and one replica copied from a buffer of
+    # torch's pinned allocator
     def copy_gbs(dst, src, reps=2):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -743,32 +769,25 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
         return reps * src.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9
 
     plain = copy_gbs(full_d[1], h_full)
-    registered = None
+    torch_pinned = None
     try:
-        nbytes = n * 4
-        raw = np.empty(nbytes + 4096, dtype=np.uint8)
-        off = (-raw.ctypes.data) % 4096
-        arr = raw[off:off + nbytes].view(np.float32)
-        arr[:] = h_reps[0].numpy()
-        rt = torch.cuda.cudart()
-        if int(rt.cudaHostRegister(arr.ctypes.data, nbytes, 0)) == 0:
-            try:
-                registered = copy_gbs(full_d[1][0, :n], torch.from_numpy(arr))
-            finally:
-                rt.cudaHostUnregister(arr.ctypes.data)
-    except Exception:
-        registered = None
+        tp = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        tp.copy_(h_reps[0])
+        torch_pinned = copy_gbs(full_d[1][0, :n], tp)
+        del tp
+    except RuntimeError:
+        torch_pinned = None
     return {"value": world * n * steps / dt, "unit": UNIT, "h2d_bytes_per_step": bi // steps,
             "d2h_bytes_per_step": n * 4, "steps": steps, "ms_per_step": dt / steps * 1e3,
             "h2d_gbs": bi / dt / 1e9, "h2d_plain_copy_gbs": plain,
-            "h2d_registered_copy_gbs": registered,
-            "note": "present replicas H2D from pinned memory on an upload stream (one copy of "
-                    "the whole [K, n] block when every learner is present; two device buffers, "
-                    "step s+1 uploads while step s computes), dl_outer_sync per step, updated "
-                    "theta_g D2H on a download stream; momentum and theta_g stay on the device. "
-                    "h2d_plain_copy_gbs: the same block copied alone from torch's pinned "
-                    "memory; h2d_registered_copy_gbs: one replica from a cudaHostRegister'ed "
-                    "buffer"}
+            "h2d_torch_pinned_copy_gbs": torch_pinned,
+            "note": "present replicas H2D on an upload stream from a page-aligned host buffer "
+                    "registered with cudaHostRegister (one copy of the whole [K, n] block when "
+                    "every learner is present; two device buffers, step s+1 uploads while step "
+                    "s computes), dl_outer_sync per step, updated theta_g D2H on a download "
+                    "stream; momentum and theta_g stay on the device. h2d_plain_copy_gbs: the "
+                    "same block copied alone; h2d_torch_pinned_copy_gbs: one replica copied "
+                    "from torch's pinned allocator"}
 
 
 def run_fragment(args, rank, world, local):
@@ -798,10 +817,11 @@ def run_fragment(args, rank, world, local):
     # the e2e pass uploads a pinned host copy of the same values
     t0 = time.time()
     g, reps = fragment_device_fill(wl, ts, dev, seed=rank)
-    host, e2e_error = None, None
+    host, e2e_error, staging = None, None, None
     if not args.no_e2e and wl.name != "ragged_heavy":
         try:
-            h_reps = torch.empty(K, reps.stride(0), dtype=torch.float32, pin_memory=True)[:, :n]
+            staging = RegisteredHost(K * reps.stride(0))
+            h_reps = staging.tensor.view(K, reps.stride(0))[:, :n]
             h_reps.copy_(reps)
             host = (None, h_reps)
         except RuntimeError as exc:  # pinned host memory exhausted (many ranks per node)
@@ -905,6 +925,8 @@ def run_fragment(args, rank, world, local):
     e2e = None
     if host is not None:
         e2e = fragment_e2e(wl, F, g, m, reps, host, sync, args, world, dev)
+        host = None
+        staging.release()  # every copy from it has completed (fragment_e2e synchronises)
     elif e2e_error is not None:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                "error": e2e_error}
