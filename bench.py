@@ -824,7 +824,7 @@ def run_fragment(args, rank, world, local):
             h_reps = staging.tensor.view(K, reps.stride(0))[:, :n]
             h_reps.copy_(reps)
             host = (None, h_reps)
-        except RuntimeError as exc:  # pinned host memory exhausted (many ranks per node)
+        except (RuntimeError, MemoryError) as exc:  # host memory exhausted (many ranks per node)
             e2e_error = f"pinned host buffer of {K * reps.stride(0) * 4 / 1e9:.1f} GB: {exc}"[:300]
     gen_s = time.time() - t0
     m = torch.zeros_like(g)
