@@ -223,7 +223,7 @@ class DeviceRun:
                 events[f][3].record(stream)
 
 
-LAUNCHES_PER_FRAGMENT = {"stats": 1, "quantize": 2, "merge": 1}
+LAUNCHES_PER_FRAGMENT = {"stats": 1, "quantize": 3, "merge": 1}
 
 
 def traffic_record(name):
@@ -344,7 +344,7 @@ def run_learner(args, rank, world, local):
                      "traffic": None, "kernel": {"stats": "k_stats",
                                                  "quantize": "k_quantize"}[dominant],
                      "note": f"peak = {peak_kind} copy bandwidth"},
-        "clocks": clk, "gpu_launches": args.steps * 3, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * (1 + LAUNCHES_PER_FRAGMENT["quantize"]), "e2e": None,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -363,10 +363,10 @@ def ring_algo_bytes(S):
 
 def ring_launches(S):
     """Kernels of one ring step per fragment: hop 0, then per later hop the
-    statistics finalisation, the quantiser's two kernels and the hop."""
+    statistics finalisation, the quantiser's kernels and the hop."""
     if S == 1:
         return 1
-    return 1 + 4 * (S - 1)
+    return 1 + (2 + LAUNCHES_PER_FRAGMENT["quantize"]) * (S - 1)
 
 
 def run_ring(args, rank, world, local):
@@ -511,7 +511,8 @@ def run_rda(args, rank, world, local):
                      "note": f"{ab} algorithmic B/elem per step; peak = {peak_kind} copy "
                              "bandwidth"},
         "per_call_ms_per_step": tot_calls / args.steps,
-        "clocks": clk, "gpu_launches": args.steps * len(frags) * 7, "e2e": None,
+        "clocks": clk, "gpu_launches": args.steps * len(frags) * (5 + LAUNCHES_PER_FRAGMENT["quantize"]),
+        "e2e": None,
         "gpu_launches_note": "kernels in the headline dl_outer_sync (DL_SYNC_RDA) region; the "
                              "per-call sequence, timed after it, launches as many again",
     }

@@ -80,6 +80,7 @@ struct QuantArgs {
     uint8_t* codes[DL_MAX_LEARNERS];
     const int64_t* off;
     const dl_stats* stats;
+    SegRt* seg;               // [K*T] quantiser parameters, derived once per call by k_quant_setup
     unsigned long long* acc;  // [K*T*256] x (count, biased residual sum)
     float* cb;
     uint32_t* counts;
@@ -411,10 +412,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
             const int64_t pa = o0 > base ? o0 : base;
             const int64_t pb = o1 < cend ? o1 : cend;
             if (pa >= pb) continue;
-            if (t != seg_t) {  // block-uniform: threads 0..L-1 derive the parameters
+            if (t != seg_t) {  // block-uniform: threads 0..L-1 load the parameters
                 __syncthreads();  // every read of the previous ones is done
                 if (tid < L) {
-                    s_seg[tid] = seg_params(a.stats[static_cast<int64_t>(k0 + tid) * a.T + t]);
+                    s_seg[tid] = a.seg[static_cast<int64_t>(k0 + tid) * a.T + t];
                     s_fp[tid] = fast_params(s_seg[tid]);
                 }
                 __syncthreads();
@@ -524,13 +525,26 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize(QuantArgs a) {
         for (int l = 0; l < L; ++l) flush_bin(a, k0 + l, cur_t, tid, l2 + l * 2 * kNB);
 }
 
+// Before the quantiser: zeroes the workspace's zeroed part (per-bin sums and
+// batch counters, n16 16-byte words at zero) and derives the quantiser
+// parameters of every (learner, tensor) once from its statistics, for the
+// quantiser blocks to load when they enter a tensor and for k_cb_fin. (Derived
+// in each block instead, this fp64 work sat on the critical path of every
+// block at every tensor it entered.)
+__global__ void __launch_bounds__(kThreads) k_quant_setup(QuantArgs a, uint4* zero, int64_t n16) {
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = i0; i < n16; i += stride) zero[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t i = i0; i < static_cast<int64_t>(a.K) * a.T; i += stride) a.seg[i] = seg_params(a.stats[i]);
+}
+
 __global__ void __launch_bounds__(kThreads) k_cb_fin(QuantArgs a) {
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= static_cast<int64_t>(a.K) * a.T * kNB) return;
     const int64_t kt = idx >> 8;
     const int b = static_cast<int>(idx & (kNB - 1));
     const dl_stats st = a.stats[kt];
-    const SegQuant q = seg_quant(st.lo, st.hi, st.nonfinite);
+    const SegQuant q = a.seg[kt].q;
     float v;
     unsigned long long cnt = 0;
     if (q.kind == kSegInvalid) {
@@ -562,6 +576,17 @@ size_t acc_bytes(int K, int T) {
 // the workspace's zeroed part: the sums, then the groups' batch counters
 size_t zeroed_bytes(int K, int T) { return acc_bytes(K, T) + 256; }
 
+// the per-(learner, tensor) quantiser parameters, after the zeroed part
+size_t seg_bytes(int K, int T) { return align256(sizeof(SegRt) * static_cast<size_t>(K) * T); }
+
+// The no-allocation entry point's static array holds the workspace of its
+// largest fragment (DL_QUANTIZE_NOALLOC_MAX_SEGMENTS (learner, tensor) pairs).
+static_assert(sizeof(SegRt) <= 96, "per-segment parameters grew");
+static_assert(kWsHeader + 2 * 8 * 256 * static_cast<size_t>(DL_QUANTIZE_NOALLOC_MAX_SEGMENTS) + 256 +
+                      96 * static_cast<size_t>(DL_QUANTIZE_NOALLOC_MAX_SEGMENTS) <=
+                  DL_QUANTIZE_NOALLOC_MAX_BYTES,
+              "the no-allocation scratch no longer holds its largest fragment");
+
 // Learner groups of the quantiser grid (see k_quantize) for K learners and a
 // grid of `blocks`: G near-equal groups, blocks shared in proportion.
 void plan_groups(QuantArgs& a, int K, int blocks) {
@@ -584,7 +609,7 @@ using namespace dl;
 extern "C" size_t dl_quantize_workspace_bytes(const dl_fragment* frag, int32_t K) {
     HostFrag f;
     if (check_fragment(frag, &f) != DL_OK || K <= 0 || K > DL_MAX_LEARNERS) return 0;
-    return kWsHeader + zeroed_bytes(K, f.T);
+    return kWsHeader + zeroed_bytes(K, f.T) + seg_bytes(K, f.T);
 }
 
 extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, int32_t K,
@@ -634,7 +659,15 @@ extern "C" int dl_quantize(const float* theta_g, const float* const* theta_k, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     a.work = reinterpret_cast<unsigned int*>(ws + kWsHeader + acc_bytes(K, f.T));
-    if ((st = cuda_status(cudaMemsetAsync(a.acc, 0, zeroed_bytes(K, f.T), s))) != DL_OK) return st;
+    a.seg = reinterpret_cast<SegRt*>(ws + kWsHeader + zeroed_bytes(K, f.T));
+    {
+        const int64_t n16 = static_cast<int64_t>(zeroed_bytes(K, f.T) / 16);
+        const int64_t items = n16 > static_cast<int64_t>(K) * f.T ? n16 : static_cast<int64_t>(K) * f.T;
+        const int64_t blocks = (items + kThreads - 1) / kThreads;
+        k_quant_setup<<<static_cast<unsigned>(blocks < 1024 ? blocks : 1024), kThreads, 0, s>>>(
+            a, reinterpret_cast<uint4*>(a.acc), n16);
+        if ((st = launch_status()) != DL_OK) return st;
+    }
     if (a.n_chunks > 0) {
         const void* kern = values ? reinterpret_cast<const void*>(k_quantize<true, true>)
                            : K == 1 ? reinterpret_cast<const void*>(k_quantize<false, true>)
