@@ -689,11 +689,10 @@ class RegisteredHost:
 def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     """The same step through the public API with host buffers: every step
     uploads the present learners' replicas of the fragment from pinned host
-    memory (a page-aligned buffer registered with cudaHostRegister; one copy
-    of the whole block when every learner is present, else one per learner)
-    on an upload stream into one of two device buffers, runs dl_outer_sync as
-    soon as they have landed, and downloads the updated theta_g on a download
-    stream. Uploads of step s+1 run while step s
+    memory (torch's pinned allocator; one copy of the whole block when every
+    learner is present, else one per learner) on an upload stream into one of
+    two device buffers, runs dl_outer_sync as soon as they have landed, and
+    downloads the updated theta_g on a download stream. Uploads of step s+1 run while step s
     computes and downloads; the step after waits for the download before it
     updates theta_g again."""
     import torch
@@ -757,8 +756,8 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
     if world > 1:
         dt = max_over_ranks(dt, world, dev)
     # the host link alone, CUDA events: the same replica block copied by
-    # itself from the staging buffer, and one replica copied from a buffer of
-    # torch's pinned allocator
+    # itself from the staging buffer, and one replica copied from a
+    # page-aligned host buffer registered with cudaHostRegister
     def copy_gbs(dst, src, reps=2):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -770,25 +769,27 @@ def fragment_e2e(wl, F, g, m, reps_d, host, sync, args, world, dev):
         return reps * src.numel() * 4 / (a.elapsed_time(b) / 1e3) / 1e9
 
     plain = copy_gbs(full_d[1], h_full)
-    torch_pinned = None
+    registered = None
     try:
-        tp = torch.empty(n, dtype=torch.float32, pin_memory=True)
-        tp.copy_(h_reps[0])
-        torch_pinned = copy_gbs(full_d[1][0, :n], tp)
-        del tp
-    except RuntimeError:
-        torch_pinned = None
+        rh = RegisteredHost(n)
+        try:
+            rh.tensor.copy_(h_reps[0])
+            registered = copy_gbs(full_d[1][0, :n], rh.tensor)
+        finally:
+            rh.release()
+    except (RuntimeError, MemoryError):
+        registered = None
     return {"value": world * n * steps / dt, "unit": UNIT, "h2d_bytes_per_step": bi // steps,
             "d2h_bytes_per_step": n * 4, "steps": steps, "ms_per_step": dt / steps * 1e3,
             "h2d_gbs": bi / dt / 1e9, "h2d_plain_copy_gbs": plain,
-            "h2d_torch_pinned_copy_gbs": torch_pinned,
-            "note": "present replicas H2D on an upload stream from a page-aligned host buffer "
-                    "registered with cudaHostRegister (one copy of the whole [K, n] block when "
-                    "every learner is present; two device buffers, step s+1 uploads while step "
-                    "s computes), dl_outer_sync per step, updated theta_g D2H on a download "
-                    "stream; momentum and theta_g stay on the device. h2d_plain_copy_gbs: the "
-                    "same block copied alone; h2d_torch_pinned_copy_gbs: one replica copied "
-                    "from torch's pinned allocator"}
+            "h2d_registered_copy_gbs": registered,
+            "note": "present replicas H2D from pinned memory on an upload stream (one copy of "
+                    "the whole [K, n] block when every learner is present; two device buffers, "
+                    "step s+1 uploads while step s computes), dl_outer_sync per step, updated "
+                    "theta_g D2H on a download stream; momentum and theta_g stay on the device. "
+                    "h2d_plain_copy_gbs: the same block copied alone from torch's pinned "
+                    "memory; h2d_registered_copy_gbs: one replica from a cudaHostRegister'ed "
+                    "buffer"}
 
 
 def run_fragment(args, rank, world, local):
@@ -818,11 +819,10 @@ def run_fragment(args, rank, world, local):
     # the e2e pass uploads a pinned host copy of the same values
     t0 = time.time()
     g, reps = fragment_device_fill(wl, ts, dev, seed=rank)
-    host, e2e_error, staging = None, None, None
+    host, e2e_error = None, None
     if not args.no_e2e and wl.name != "ragged_heavy":
         try:
-            staging = RegisteredHost(K * reps.stride(0))
-            h_reps = staging.tensor.view(K, reps.stride(0))[:, :n]
+            h_reps = torch.empty(K, reps.stride(0), dtype=torch.float32, pin_memory=True)[:, :n]
             h_reps.copy_(reps)
             host = (None, h_reps)
         except (RuntimeError, MemoryError) as exc:  # host memory exhausted (many ranks per node)
@@ -926,8 +926,6 @@ def run_fragment(args, rank, world, local):
     e2e = None
     if host is not None:
         e2e = fragment_e2e(wl, F, g, m, reps, host, sync, args, world, dev)
-        host = None
-        staging.release()  # every copy from it has completed (fragment_e2e synchronises)
     elif e2e_error is not None:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                "error": e2e_error}
