@@ -7,10 +7,9 @@
 //              the blocks of all groups sweep the fragment together
 //              (theta_g crosses HBM once, then comes from L2) and each
 //              theta_g value a block loads serves every learner of its group;
-//              thread 0 derives a tensor's
-//              quantiser parameters from its statistics when the block
-//              enters it (no separate launch); each chunk is loaded in two
-//              halves with 128-bit loads. Per element of learner k:
+//              a block entering a tensor loads its learners' quantiser
+//              parameters (derived by k_quant_setup); each chunk is loaded
+//              in two halves with 128-bit loads. Per element of learner k:
 //                * bucket: u = (Delta - lo) * 256 / (hi - lo) is evaluated in
 //                  fp32 with one fma; an element clipped well outside the
 //                  range (fp32 u below -1/2 or above 256.5) takes bucket 0
@@ -40,6 +39,9 @@
 //              table with integer atomics when the block moves to another
 //              tensor.
 //              Integer sums make the result independent of addition order.
+// k_quant_setup  before k_quantize: zeroes the per-bin sums and batch
+//              counters and derives each (k, t)'s quantiser parameters once,
+//              in fp64, from its statistics.
 // k_cb_fin     one thread per (k, t, b): codebook value = reference + mean
 //              residual (fp64, rounded once to fp32), midpoint for an empty
 //              bucket, and the optional counts.
