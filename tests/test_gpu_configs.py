@@ -52,6 +52,29 @@ def _delta_device(wl, t, m, gen):
     return x.mul_(wl.tensor_scale(t))
 
 
+def _decode_bound_everywhere(run, g_before, reps, idx):
+    """Every element of every present learner, the whole fragment: the decoded
+    value cb_k[t][code] lies within one bucket width of clamp(Delta, lo, hi).
+    A correct code puts both in the same bucket, a counted boundary exception
+    puts the value in the neighbouring one, still within a width. This holds
+    at any size, so it covers what the oracle cannot run on: a wrong code,
+    codebook entry or tensor mapping anywhere in the fragment fails it."""
+    st = run.dl.stats_to_host(run.sync.stats[:len(idx)])
+    sizes = torch.tensor(run.numels, device="cuda")
+    t_of = torch.repeat_interleave(torch.arange(len(run.numels), device="cuda"), sizes)
+    for s, k in enumerate(idx):
+        lo = torch.tensor(st["lo"][s], device="cuda", dtype=torch.float64)
+        hi = torch.tensor(st["hi"][s], device="cuda", dtype=torch.float64)
+        d = (g_before - reps[k]).double()  # Delta exactly as the kernels form it (fp32)
+        dc = torch.clamp(d, lo[t_of], hi[t_of])
+        del d
+        v = run.sync.codebook[s][t_of, run.sync.codes[s][:run.n].long()].double()
+        bound = (hi - lo)[t_of] / 256.0 * (1 + 1e-5) + 1e-7 * v.abs()
+        bad = int(((v - dc).abs() > bound).sum())
+        assert bad == 0, (k, bad)
+        del dc, v, bound
+
+
 class FragmentRun:
     """Device state of one fragment and host copies of its sampled tensors."""
 
@@ -93,11 +116,12 @@ class FragmentRun:
             reps.append(r)
         return reps
 
-    def step(self, step, present=None, weights=None, twin=None):
+    def step(self, step, present=None, weights=None, twin=None, everywhere=False):
         """One outer step through the per-call sequence. With `twin` (a
         ModelSync over this fragment) the same step also runs through
         dl_outer_sync, the call bench.py times, on copies of theta and m, and
-        both must give the same bits."""
+        both must give the same bits. With `everywhere`, every element of the
+        fragment is held to the decode bound (_decode_bound_everywhere)."""
         # the oracle chain's state of the sampled tensors goes into the GPU
         # buffers (a no-op at step 0, where both hold the initial theta and 0)
         for h in self.host.values():
@@ -110,9 +134,13 @@ class FragmentRun:
                       present=None if present is None else [present], delta_bar=[db2])
         db = torch.empty_like(self.g)
         counts = torch.empty((self.K, self.frag.T, 256), dtype=torch.int32, device="cuda")
+        g_before = self.g.clone() if everywhere else None
         idx = self.sync.step(self.g, self.m, reps, weights=weights, present=present, delta_bar=db,
                              counts=counts)
         torch.cuda.synchronize()
+        if everywhere:
+            _decode_bound_everywhere(self, g_before, reps, idx)
+            del g_before
         del reps
         if twin is not None:
             for a, b in ((g2, self.g), (m2, self.m), (db2, db)):
@@ -197,7 +225,7 @@ def test_decoder_1b_every_fragment():
 def test_decoder_10b_fragment_three_steps():
     """10B set, K=14: the median (~415M-element) fragment over 3 outer steps
     with momentum carried; each step also through dl_outer_sync (bitwise the
-    same)."""
+    same), and every element of every learner held to the decode bound."""
     wl = synthetic.decoder_10b()
     frags, load = _plan(wl)
     f = int(np.argsort(load, kind="stable")[len(load) // 2])  # bench.py's fragment
@@ -208,7 +236,7 @@ def test_decoder_10b_fragment_three_steps():
     # the same steps through dl_outer_sync, as bench.py runs them: bitwise equal
     twin = run.dl.ModelSync([run.frag], run.K)
     for step in range(wl.steps):
-        idx, db, counts = run.step(step, twin=twin)
+        idx, db, counts = run.step(step, twin=twin, everywhere=True)
         run.check(step, idx, db, counts)
     assert torch.isfinite(run.g).all()
 
