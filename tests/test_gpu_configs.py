@@ -60,19 +60,21 @@ def _decode_bound_everywhere(run, g_before, reps, idx):
     at any size, so it covers what the oracle cannot run on: a wrong code,
     codebook entry or tensor mapping anywhere in the fragment fails it."""
     st = run.dl.stats_to_host(run.sync.stats[:len(idx)])
-    sizes = torch.tensor(run.numels, device="cuda")
-    t_of = torch.repeat_interleave(torch.arange(len(run.numels), device="cuda"), sizes)
+    ends = torch.tensor(run.off[1:], device="cuda")
+    step = 1 << 27  # elements per slice: bounds the temporaries at a few GB
     for s, k in enumerate(idx):
         lo = torch.tensor(st["lo"][s], device="cuda", dtype=torch.float64)
         hi = torch.tensor(st["hi"][s], device="cuda", dtype=torch.float64)
-        d = (g_before - reps[k]).double()  # Delta exactly as the kernels form it (fp32)
-        dc = torch.clamp(d, lo[t_of], hi[t_of])
-        del d
-        v = run.sync.codebook[s][t_of, run.sync.codes[s][:run.n].long()].double()
-        bound = (hi - lo)[t_of] / 256.0 * (1 + 1e-5) + 1e-7 * v.abs()
-        bad = int(((v - dc).abs() > bound).sum())
-        assert bad == 0, (k, bad)
-        del dc, v, bound
+        for a in range(0, run.n, step):
+            b = min(run.n, a + step)
+            t_of = torch.searchsorted(ends, torch.arange(a, b, device="cuda"), right=True)
+            d = (g_before[a:b] - reps[k][a:b]).double()  # Delta as the kernels form it (fp32)
+            dc = torch.clamp(d, lo[t_of], hi[t_of])
+            v = run.sync.codebook[s][t_of, run.sync.codes[s][a:b].long()].double()
+            bound = (hi - lo)[t_of] / 256.0 * (1 + 1e-5) + 1e-7 * v.abs()
+            bad = int(((v - dc).abs() > bound).sum())
+            assert bad == 0, (k, a, bad)
+            del t_of, d, dc, v, bound
 
 
 class FragmentRun:
@@ -214,7 +216,7 @@ def test_decoder_1b_every_fragment():
     for f, ts in enumerate(frags):
         sampled = _sampled(wl, ts)
         run = FragmentRun(wl, ts, sampled, gen_seed=f)
-        idx, db, counts = run.step(0)
+        idx, db, counts = run.step(0, everywhere=True)
         assert torch.isfinite(run.g).all() and torch.isfinite(run.m).all()
         total_exc += run.check(0, idx, db, counts)
         del run
@@ -250,7 +252,7 @@ def test_ragged_heavy_single_batch():
     order = np.argsort(sizes)
     sampled = {int(order[0]), 9, int(order[len(order) // 2]), int(order[-200]), int(order[-1])}
     run = FragmentRun(wl, ts, sampled, gen_seed=4)
-    idx, db, counts = run.step(0)
+    idx, db, counts = run.step(0, everywhere=True)
     exc = run.check(0, idx, db, counts)
     st = run.dl.stats_to_host(run.sync.stats)
     assert (st["nonfinite"] == 0).all() and (st["count"] == sizes[None, :]).all()
@@ -275,7 +277,7 @@ def test_quorum_10b_fragments_and_steps():
         for step in range(wl.steps):
             present = wl.present(f, step)
             weights = wl.weights(f, step)
-            idx, db, counts = run.step(step, present=present, weights=weights)
+            idx, db, counts = run.step(step, present=present, weights=weights, everywhere=True)
             assert idx == [k for k in range(wl.K) if present[k]]
             run.check(step, idx, db, counts, present=present, weights=weights)
         assert torch.isfinite(run.g).all()
@@ -294,7 +296,7 @@ def test_quorum_10b_embedding_fragment():
     assert len(ts) == 1 and wl.numels[ts[0]] == 525336576
     run = FragmentRun(wl, ts, {ts[0]}, gen_seed=7)
     present, weights = wl.present(f, 0), wl.weights(f, 0)
-    idx, db, counts = run.step(0, present=present, weights=weights)
+    idx, db, counts = run.step(0, present=present, weights=weights, everywhere=True)
     run.check(0, idx, db, counts, present=present, weights=weights)
 
 
