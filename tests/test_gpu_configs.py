@@ -77,6 +77,48 @@ def _decode_bound_everywhere(run, g_before, reps, idx):
             del t_of, d, dc, v, bound
 
 
+def _merge_everywhere(run, g_before, m_before, db, idx, weights, lr=0.7, mu=0.9):
+    """Every element of the fragment, from the kernel's own codes and codebooks:
+    delta_bar against their fp64 weighted sum, within the error of K fp32
+    multiply-adds and of the fp32 normalised weights, (K + 3) u sum|w v|; then
+    m' = mu m + D and theta' = theta - lr (mu m' + D) against fp64 from the
+    kernel's own D and m', each within the rounding of its fp32 result (with
+    the rounding of the intermediate fp32 mu m' + D for theta'). A wrong
+    codebook row, weight, absent learner read or update term anywhere in the
+    fragment fails it; the oracle holds the sampled tensors to the bits."""
+    u = 2.0 ** -24
+    w = np.ones(len(idx)) if weights is None else np.asarray(weights, np.float32)[idx]
+    w = w.astype(np.float64)
+    w_hat = w / w.sum()
+    mu, lr = float(np.float32(mu)), float(np.float32(lr))  # the fp32 constants the kernels get
+    ends = torch.tensor(run.off[1:], device="cuda")
+    step = 1 << 27
+    for a in range(0, run.n, step):
+        b = min(run.n, a + step)
+        t_of = torch.searchsorted(ends, torch.arange(a, b, device="cuda"), right=True)
+        acc = torch.zeros(b - a, dtype=torch.float64, device="cuda")
+        mag = torch.zeros_like(acc)
+        for s in range(len(idx)):
+            v = run.sync.codebook[s][t_of, run.sync.codes[s][a:b].long()].double() * w_hat[s]
+            acc += v
+            mag += v.abs()
+            del v
+        d = db[a:b].double()
+        bad = int(((d - acc).abs() > (len(idx) + 3) * u * mag + 1e-44).sum())
+        assert bad == 0, ("delta_bar", a, bad)
+        del acc, mag, t_of
+        m_new = run.m[a:b].double()
+        ref = mu * m_before[a:b].double() + d
+        bad = int(((m_new - ref).abs() > 2 * u * ref.abs() + 1e-44).sum())
+        assert bad == 0, ("momentum", a, bad)
+        gn = mu * m_new + d
+        ref = g_before[a:b].double() - lr * gn
+        tol = 2 * u * (ref.abs() + lr * gn.abs()) + 1e-44
+        bad = int(((run.g[a:b].double() - ref).abs() > tol).sum())
+        assert bad == 0, ("theta", a, bad)
+        del d, m_new, ref, gn, tol
+
+
 class FragmentRun:
     """Device state of one fragment and host copies of its sampled tensors."""
 
@@ -123,7 +165,8 @@ class FragmentRun:
         ModelSync over this fragment) the same step also runs through
         dl_outer_sync, the call bench.py times, on copies of theta and m, and
         both must give the same bits. With `everywhere`, every element of the
-        fragment is held to the decode bound (_decode_bound_everywhere)."""
+        fragment is held to the decode bound (_decode_bound_everywhere) and
+        its merge and update to fp64 from the kernel's codes (_merge_everywhere)."""
         # the oracle chain's state of the sampled tensors goes into the GPU
         # buffers (a no-op at step 0, where both hold the initial theta and 0)
         for h in self.host.values():
@@ -137,12 +180,14 @@ class FragmentRun:
         db = torch.empty_like(self.g)
         counts = torch.empty((self.K, self.frag.T, 256), dtype=torch.int32, device="cuda")
         g_before = self.g.clone() if everywhere else None
+        m_before = self.m.clone() if everywhere else None
         idx = self.sync.step(self.g, self.m, reps, weights=weights, present=present, delta_bar=db,
                              counts=counts)
         torch.cuda.synchronize()
         if everywhere:
             _decode_bound_everywhere(self, g_before, reps, idx)
-            del g_before
+            _merge_everywhere(self, g_before, m_before, db, idx, weights)
+            del g_before, m_before
         del reps
         if twin is not None:
             for a, b in ((g2, self.g), (m2, self.m), (db2, db)):
