@@ -22,7 +22,8 @@ import pytest
 
 import oracle
 import synthetic
-from parity import TOL_REL_L2, check_codebook, check_codes, check_merge, check_stats, rel_l2
+from parity import (TOL_REL_L2, TOL_STATS, check_codebook, check_codes, check_merge, check_stats,
+                    rel_l2)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -75,6 +76,37 @@ def _decode_bound_everywhere(run, g_before, reps, idx):
             bad = int(((v - dc).abs() > bound).sum())
             assert bad == 0, (k, a, bad)
             del t_of, d, dc, v, bound
+
+
+def _stats_everywhere(run, g_before, reps, idx, clip=6.0):
+    """Every tensor of every present learner: count, non-finite count, mean,
+    std (population), lo and hi against torch fp64 two-pass sums over the same
+    fp32 Delta, at the oracle's bar (std within TOL_STATS relative, mean
+    within TOL_STATS std, lo and hi within that of mean -/+ 6 std)."""
+    st = run.dl.stats_to_host(run.sync.stats[:len(idx)])
+    T = len(run.numels)
+    assert (st["count"] == np.asarray(run.numels)[None, :]).all()
+    assert (st["nonfinite"] == 0).all()
+    for s, k in enumerate(idx):
+        mus, sds = [], []
+        for i in range(T):
+            a, b = int(run.off[i]), int(run.off[i + 1])
+            if b == a:
+                mus.append(torch.zeros((), dtype=torch.float64, device="cuda"))
+                sds.append(mus[-1])
+                continue
+            d = (g_before[a:b] - reps[k][a:b]).double()
+            mu = d.mean()
+            mus.append(mu)
+            sds.append((d - mu).square_().mean().sqrt())
+            del d
+        mu = torch.stack(mus).cpu().numpy()
+        sd = torch.stack(sds).cpu().numpy()
+        assert (np.abs(st["std"][s] - sd) <= TOL_STATS * sd).all(), k
+        assert (np.abs(st["mean"][s] - mu) <= TOL_STATS * sd + 1e-15 * np.abs(mu)).all(), k
+        for key, ref in (("lo", mu - clip * sd), ("hi", mu + clip * sd)):
+            tol = (1 + clip) * TOL_STATS * sd + 1e-15 * np.abs(ref)
+            assert (np.abs(st[key][s] - ref) <= tol).all(), (k, key)
 
 
 def _merge_everywhere(run, g_before, m_before, db, idx, weights, lr=0.7, mu=0.9):
@@ -165,8 +197,9 @@ class FragmentRun:
         ModelSync over this fragment) the same step also runs through
         dl_outer_sync, the call bench.py times, on copies of theta and m, and
         both must give the same bits. With `everywhere`, every element of the
-        fragment is held to the decode bound (_decode_bound_everywhere) and
-        its merge and update to fp64 from the kernel's codes (_merge_everywhere)."""
+        fragment is held to the decode bound (_decode_bound_everywhere), its
+        statistics to torch fp64 (_stats_everywhere), and its merge and update
+        to fp64 from the kernel's codes (_merge_everywhere)."""
         # the oracle chain's state of the sampled tensors goes into the GPU
         # buffers (a no-op at step 0, where both hold the initial theta and 0)
         for h in self.host.values():
@@ -185,6 +218,7 @@ class FragmentRun:
                              counts=counts)
         torch.cuda.synchronize()
         if everywhere:
+            _stats_everywhere(self, g_before, reps, idx)
             _decode_bound_everywhere(self, g_before, reps, idx)
             _merge_everywhere(self, g_before, m_before, db, idx, weights)
             del g_before, m_before
