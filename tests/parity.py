@@ -209,6 +209,50 @@ def check_merge(gp_vals, o_vals, codes_g, codes_o, cb_g, cb_o, w_hat, t_of=None,
     return out, diff, expl_max
 
 
+def check_merge_elementwise(g0, m0, values, w, out, lr=0.7, mu=0.9):
+    """Every element, from one side's own inputs to its merge: `values` holds
+    one fp32 array per learner taking part (its decoded values, or its
+    pseudo-gradients when unquantised) and `w` their weights as given (fp32,
+    normalised here in fp64). delta_bar lies within the error of K fp32
+    multiply-adds and of the fp32 normalised weights, (K + 3) u sum |w v|, of
+    the fp64 weighted sum; momentum' = mu m + delta_bar and theta' = theta -
+    lr (mu momentum' + delta_bar) lie within the rounding of their fp32
+    results (with that of the intermediate for theta') of fp64 from the side's
+    own delta_bar and momentum'. A relative L2 over a tensor can hide one
+    wrong element; this cannot. Returns the largest error seen as a fraction
+    of its bound, per output."""
+    u = 2.0 ** -24
+    floor = 1e-43  # a few fp32 subnormal spacings
+    w = np.asarray(w, np.float32).astype(np.float64)
+    w = w / w.sum()
+    mu, lr = float(np.float32(mu)), float(np.float32(lr))
+    acc = np.zeros(np.size(g0))
+    mag = np.zeros_like(acc)
+    for wk, v in zip(w, values):
+        x = wk * np.asarray(v, np.float32).astype(np.float64)
+        acc += x
+        mag += np.abs(x)
+    worst = {}
+    d = out["delta_bar"].astype(np.float64)
+    for key, got, ref, tol in _merge_terms(d, acc, mag, len(values), g0, m0, out, lr, mu, u, floor):
+        r = np.abs(got - ref) / tol
+        bad = np.nonzero(r > 1.0)[0]
+        assert bad.size == 0, (key, bad[:5], got[bad[:5]], ref[bad[:5]])
+        worst[key] = float(r.max()) if r.size else 0.0
+    return worst
+
+
+def _merge_terms(d, acc, mag, K, g0, m0, out, lr, mu, u, floor):
+    yield "delta_bar", d, acc, (K + 3) * u * mag + floor
+    mn = out["momentum"].astype(np.float64)
+    ref = mu * np.asarray(m0, np.float64) + d
+    yield "momentum", mn, ref, 2 * u * np.abs(ref) + floor
+    gn = mu * mn + d
+    ref = np.asarray(g0, np.float64) - lr * gn
+    tol = 2 * u * (np.abs(ref) + lr * np.abs(gn)) + floor
+    yield "theta_g", out["theta_g"].astype(np.float64), ref, tol
+
+
 def compare(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, lr=0.7, mu=0.9,
             clip_sigmas=6.0, quantized=True, nan_ok=False):
     offsets = np.zeros(len(numels) + 1, dtype=np.int64)
@@ -234,7 +278,16 @@ def compare(g, reps, numels, m=None, weights=None, present=None, min_quorum=1, l
         res, _, _ = check_merge(gp, o, gp["codes"][pres], o["codes"][pres], gp["codebook"][pres],
                                 o["codebook"][pres], w_hat[pres], t_of)
         report.update(res)
+        w = np.ones(K, np.float32) if weights is None else np.asarray(weights, np.float32)
+        vals = [gp["codebook"][k][t_of, gp["codes"][k]] for k in np.nonzero(pres)[0]]
+        report["elementwise"] = check_merge_elementwise(g, m0, vals, w[pres], gp, lr, mu)
     else:
+        if not nan_ok:
+            K = len(reps)
+            pres = np.ones(K, bool) if present is None else np.asarray(present, bool)
+            w = np.ones(K, np.float32) if weights is None else np.asarray(weights, np.float32)
+            vals = [(g - reps[k]).astype(np.float32) for k in np.nonzero(pres)[0]]
+            report["elementwise"] = check_merge_elementwise(g, m0, vals, w[pres], gp, lr, mu)
         for key in ("delta_bar", "theta_g", "momentum"):
             a, b = gp[key], o[key]
             if nan_ok:
