@@ -8,13 +8,15 @@ pin fail, which shows that the pins tie the oracle to the pages' definitions
 and to the mathematics rather than to its own code. An unmutated copy, built
 and run the same way, must pass, so that a failure means the planted mistake.
 
-The mutated copies live in the test's temporary folder; the oracle itself is
-never touched.
+The mutated copies are built in a scratch folder beside this file
+(``tests/_mutants/``, ignored by git), which the test removes when it ends;
+the oracle itself is never touched.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import shutil
 import subprocess
 import sys
 
@@ -120,7 +122,20 @@ def _run_pins(workdir, tag, source, pins):
     return r.returncode, (failed[0] if failed else r.stdout[-400:])
 
 
-def test_every_planted_mistake_fails_a_pin(tmp_path):
+def test_every_planted_mistake_fails_a_pin():
+    workdir = os.path.join(HERE, "_mutants", str(os.getpid()))
+    os.makedirs(workdir, exist_ok=True)
+    try:
+        _planted_mistakes(workdir)
+    finally:
+        shutil.rmtree(workdir, ignore_errors=True)
+        try:
+            os.rmdir(os.path.dirname(workdir))
+        except OSError:
+            pass
+
+
+def _planted_mistakes(workdir):
     with open(SRC) as fh:
         src = fh.read()
     jobs = {"control": (src, PINS)}
@@ -130,7 +145,7 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
         jobs[f"m{i:02d}"] = (src.replace(old, new), pins)
     workers = max(2, min(8, os.cpu_count() or 2))
     with cf.ThreadPoolExecutor(workers) as ex:
-        futs = {tag: ex.submit(_run_pins, str(tmp_path), tag, s, p) for tag, (s, p) in jobs.items()}
+        futs = {tag: ex.submit(_run_pins, workdir, tag, s, p) for tag, (s, p) in jobs.items()}
         res = {tag: f.result() for tag, f in futs.items()}
     rc, info = res.pop("control")
     assert rc == 0, f"the unmutated oracle fails its own pins: {info}"
