@@ -7,6 +7,7 @@ C entry points (see include/diloco_sync.h) keep their names here:
     plan_fragments       balanced tensor -> fragment assignment (host)
     pseudograd_stats     per-(learner, tensor) mu / sigma / clip range
     quantize             uint8 codes + bucket-mean codebooks
+    quantize_noalloc     quantize with the library's static scratch (no workspace)
     merge_outer_step     decode, weighted fp32 mean, outer Nesterov (in place)
     rda_merge_outer_step Radial-Directional Averaging merge, then the outer step
     ring_outer_step      ring accumulation re-quantised at every hop, then the
@@ -35,6 +36,8 @@ DL_SYNC_UNQUANTIZED = 1
 DL_SYNC_SERIAL = 2
 DL_SYNC_RDA = 4
 DL_SYNC_RING = 8
+DL_ERR_WORKSPACE = -6
+DL_QUANTIZE_NOALLOC_MAX_SEGMENTS = 2000
 STATS_FIELDS = ("count", "nonfinite", "mean", "std", "lo", "hi")
 
 _lib = None
@@ -76,6 +79,8 @@ def lib():
         L.dl_quantize_workspace_bytes.argtypes = [fr, i32]
         L.dl_quantize.restype = ctypes.c_int
         L.dl_quantize.argtypes = [vp, vp, i32, fr, vp, vp, vp, vp, vp, sz, vp]
+        L.dl_quantize_noalloc.restype = ctypes.c_int
+        L.dl_quantize_noalloc.argtypes = [vp, vp, i32, fr, vp, vp, vp, vp, vp]
         L.dl_merge_outer_step.restype = ctypes.c_int
         L.dl_merge_outer_step.argtypes = [vp, vp, vp, vp, vp, i32, fr, vp, vp, i32, f32, f32, vp,
                                           vp]
@@ -270,6 +275,33 @@ def quantize(theta_g, replicas, frag: Fragment, stats, codes=None, codebook=None
         _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
         _ptr(stats), _ptr_array(codes),
         _ptr(codebook), _ptr(counts), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return codes, codebook
+
+
+def quantize_noalloc(theta_g, replicas, frag: Fragment, stats, codes, codebook, counts=None,
+                     stream=None):
+    """quantize() for callers that cannot allocate (dl_quantize_noalloc): the
+    scratch is one static device array inside the library, so the caller
+    passes every output and nothing is allocated on the device, here or in
+    the library. Calls share that array: order calls whose GPU work could
+    overlap on one stream. K * frag.T above DL_QUANTIZE_NOALLOC_MAX_SEGMENTS
+    raises DLError with status DL_ERR_WORKSPACE, before any launch.
+    replicas=None: values mode (quantise theta_g itself, K = 1)."""
+    K = 1 if replicas is None else len(replicas)
+    if codes is None or codebook is None:
+        raise ValueError("quantize_noalloc: codes and codebook are the caller's (no allocation)")
+    _need(theta_g, _F32, frag.n, "theta_g")
+    _need_all(replicas or [], _F32, frag.n, "replicas")
+    _need(stats, _I64, K * frag.T * 6, "stats")
+    if len(codes) < K:
+        raise ValueError(f"codes: {len(codes)} buffers, need {K}")
+    _need_all(codes, _U8, frag.n, "codes")
+    _need(codebook, _F32, K * frag.T * DL_NBUCKETS, "codebook")
+    _need(counts, _U32, K * frag.T * DL_NBUCKETS, "counts")
+    _cuda(theta_g, replicas or [], stats, codes, codebook, counts)
+    _check("dl_quantize_noalloc", lib().dl_quantize_noalloc(
+        _ptr(theta_g), None if replicas is None else _ptr_array(replicas), K, frag.c,
+        _ptr(stats), _ptr_array(codes), _ptr(codebook), _ptr(counts), _stream(stream)))
     return codes, codebook
 
 

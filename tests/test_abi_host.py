@@ -340,3 +340,24 @@ def test_rda_validation_and_quorum_rules(L):
         q = int(rng.integers(0, 4))
         st_or, _ = oracle.merge_weights(w.astype(np.float32), p, Kr, q)
         assert rda(Kr, w, p, q) == (st_or if st_or < 0 else -6)
+
+
+def test_quantize_noalloc_limits_before_any_device_call(L):
+    """dl_quantize_noalloc refuses on the host, before it looks up its static
+    scratch: K outside 1..32 (DL_ERR_ARG), and a fragment whose K * n_tensors
+    exceeds the scratch's segment limit (DL_ERR_WORKSPACE), from just past
+    the limit. Only refusals are called here: an accepted call would go on to
+    the device. The binding's constant matches the header's."""
+    hdr = open(os.path.join(ROOT, "include", "diloco_sync.h")).read()
+    lim = int(re.search(r"#define DL_QUANTIZE_NOALLOC_MAX_SEGMENTS (\d+)", hdr).group(1))
+    assert lim == dl.DL_QUANTIZE_NOALLOC_MAX_SEGMENTS
+    f, off = _frag(np.arange(lim // 2 + 2))  # lim/2 + 1 one-element tensors
+    fb = ctypes.byref(f)
+    q = L.dl_quantize_noalloc
+    assert q(FAKE, _ptrs(FAKE, FAKE), 2, fb, FAKE, _ptrs(FAKE, FAKE), FAKE, None, None) == -6
+    assert q(FAKE, _ptrs(*[FAKE] * 4), 4, fb, FAKE, _ptrs(*[FAKE] * 4), FAKE, None, None) == -6
+    assert q(FAKE, _ptrs(FAKE), 0, fb, FAKE, _ptrs(FAKE), FAKE, None, None) == -1
+    assert q(FAKE, _ptrs(*[FAKE] * 33), 33, fb, FAKE, _ptrs(*[FAKE] * 33), FAKE, None,
+             None) == -1
+    h, _o = _frag([0, 10, 5])
+    assert q(FAKE, _ptrs(FAKE), 1, ctypes.byref(h), FAKE, _ptrs(FAKE), FAKE, None, None) == -5

@@ -76,3 +76,21 @@ def test_outer_sync_checks_every_job(F):
     reps = [[_f32(F.n)] * 2, [_f32(64)] * 2]
     with pytest.raises(ValueError, match=r"momentum\[1\]: 63 elements"):
         dl.outer_sync(frags, g, m, reps, 2, workspace=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_quantize_noalloc_takes_caller_outputs_and_checks_them(F):
+    g = _f32(F.n)
+    reps = [_f32(F.n)] * 2
+    st = dl.new_stats(2, F.T, "cpu")
+    codes = [torch.zeros(F.n, dtype=torch.uint8) for _ in range(2)]
+    cb = torch.zeros((2, F.T, 256))
+    with pytest.raises(ValueError, match="caller's"):
+        dl.quantize_noalloc(g, reps, F, st, None, cb)
+    with pytest.raises(ValueError, match="codes: 1 buffers, need 2"):
+        dl.quantize_noalloc(g, reps, F, st, codes[:1], cb)
+    with pytest.raises(ValueError, match="codebook: .* need at least"):
+        dl.quantize_noalloc(g, reps, F, st, codes, torch.zeros((1, F.T, 256)))
+    with pytest.raises(TypeError, match="counts: dtype"):
+        dl.quantize_noalloc(g, reps, F, st, codes, cb, counts=torch.zeros((2, F.T, 256)))
+    with pytest.raises(ValueError, match="CUDA device"):
+        dl.quantize_noalloc(g, reps, F, st, codes, cb)

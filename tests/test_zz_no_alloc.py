@@ -98,3 +98,32 @@ def test_noalloc_rejects_fragments_beyond_its_scratch(noalloc):
     torch.cuda.synchronize()
     # one-element tensors: sigma = 0, so every code is 0 and cb = the value
     assert int(codes[0].max()) == 0
+
+
+def test_binding_quantize_noalloc_matches_quantize(noalloc):
+    """The Python binding of the same entry point (dl.quantize_noalloc), in
+    values mode and with replicas, against dl.quantize bit for bit; a
+    fragment past the segment limit raises DLError with DL_ERR_WORKSPACE."""
+    dl, _ = noalloc
+    for seed, numels, K in ((5, [70000, 9], 2), (6, [8192 * 5 + 3], 1)):
+        g, reps = _inputs(seed, numels, K)
+        frag = dl.Fragment(numels)
+        reps_or_none = None if K == 1 else reps  # K = 1: values mode (theta_g itself)
+        stats = dl.pseudograd_stats(g, reps_or_none, frag)
+        counts_a = torch.empty((K, frag.T, 256), dtype=torch.int32, device="cuda")
+        codes_a, cb_a = dl.quantize(g, reps_or_none, frag, stats, counts=counts_a)
+        codes_b = [torch.full((frag.n,), 7, dtype=torch.uint8, device="cuda") for _ in range(K)]
+        cb_b = torch.full((K, frag.T, 256), float("nan"), device="cuda")
+        counts_b = torch.full((K, frag.T, 256), -1, dtype=torch.int32, device="cuda")
+        dl.quantize_noalloc(g, reps_or_none, frag, stats, codes_b, cb_b, counts=counts_b)
+        torch.cuda.synchronize()
+        for k in range(K):
+            assert torch.equal(codes_a[k], codes_b[k])
+        assert torch.equal(cb_a, cb_b) and torch.equal(counts_a, counts_b)
+    big = dl.Fragment([1] * 2001)
+    g, _ = _inputs(7, [2001], 1)
+    with pytest.raises(dl.DLError) as e:
+        dl.quantize_noalloc(g, None, big, dl.new_stats(1, 2001),
+                            [torch.empty(2001, dtype=torch.uint8, device="cuda")],
+                            torch.empty((1, 2001, 256), device="cuda"))
+    assert e.value.status == dl.DL_ERR_WORKSPACE
