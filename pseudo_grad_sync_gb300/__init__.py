@@ -126,6 +126,11 @@ def status_string(status: int) -> str:
     return lib().dl_status_string(status).decode()
 
 
+def version() -> int:
+    """The library's ABI version (dl_version)."""
+    return int(lib().dl_version())
+
+
 _F32 = (torch.float32,)
 _U8 = (torch.uint8,)
 _I64 = (torch.int64,)

@@ -361,3 +361,12 @@ def test_quantize_noalloc_limits_before_any_device_call(L):
              None) == -1
     h, _o = _frag([0, 10, 5])
     assert q(FAKE, _ptrs(FAKE), 1, ctypes.byref(h), FAKE, _ptrs(FAKE), FAKE, None, None) == -5
+
+
+def test_binding_has_every_entry_point_under_its_name(L):
+    """Every dl_* function the header declares has a binding function of the
+    same name without the prefix, so a user of the C ABI finds each call in
+    Python under its own name."""
+    missing = [n for n in _declared_functions() if not callable(getattr(dl, n[3:], None))]
+    assert not missing, missing
+    assert dl.version() == L.dl_version()
