@@ -6,10 +6,12 @@ import pytest
 import torch
 
 import pseudo_grad_sync_gb300 as dl
+from pseudo_grad_sync_gb300 import _build
 
 
 @pytest.fixture(scope="module")
 def F():
+    _build.build()  # in-tree, and only when its sources are newer
     dl.lib()
     return dl.Fragment([100, 28], device="cpu")
 
